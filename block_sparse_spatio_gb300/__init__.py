@@ -1,0 +1,294 @@
+"""Python binding of the block-sparse spatio-temporal attention library.
+
+Argument marshalling only: every step runs in the CUDA library ``libbss.so``
+(C ABI in ``include/bss.h``).  PyTorch supplies device memory and the current
+stream.  There is no CPU or PyTorch fallback: if the library is missing or was
+not built for this GPU, every call raises.
+
+Method: blog "Accelerating Spatio-Temporal Attention for Video Diffusion on
+TPUs" (Google Developers) -- per-head spatial / temporal block-sparse
+attention with full / boundary / skipped tiles, optional tile-aligned rounding,
+and the (F,H,W) <-> (H,W,F) token permutation for temporal heads.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import numpy as np
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libbss.so")
+
+KIND_SPATIAL, KIND_TEMPORAL = 0, 1
+CLASS_FULL, CLASS_BOUNDARY, CLASS_PAD = 0, 1, 2
+CLASS_SHIFT = 30
+TILE_INDEX_MASK = (1 << 30) - 1
+STAT_NAMES = ("full", "boundary", "pad", "skip", "retained_pairs", "exact_retained_pairs")
+STATUS_NAMES = {0: "BSS_OK", 1: "BSS_ERR_INVALID_ARG", 2: "BSS_ERR_UNSUPPORTED", 3: "BSS_ERR_CUDA",
+                4: "BSS_ERR_TIMEOUT", 5: "BSS_ERR_OOM"}
+
+_lib = None
+
+
+class BssError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+class _MaskParams(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in ("F", "Hs", "Ws", "head_dim", "spatial_frame_window",
+                                               "temporal_raster_window", "sink_frames", "temporal_permuted",
+                                               "rounding")]
+
+
+@dataclass(frozen=True)
+class MaskParams:
+    """Video geometry and mask windows (see ``bss_mask_params`` in include/bss.h)."""
+    F: int
+    Hs: int
+    Ws: int
+    head_dim: int
+    spatial_frame_window: int
+    temporal_raster_window: int
+    sink_frames: int = 1
+    temporal_permuted: int = 1
+    rounding: int = 0
+
+    @property
+    def S(self) -> int:
+        return self.Hs * self.Ws
+
+    @property
+    def N(self) -> int:
+        return self.F * self.S
+
+    def c(self) -> _MaskParams:
+        return _MaskParams(self.F, self.Hs, self.Ws, self.head_dim, self.spatial_frame_window,
+                           self.temporal_raster_window, self.sink_frames, self.temporal_permuted, self.rounding)
+
+
+EXPORTED = ("bss_build_tile_map", "bss_tile_map_stats", "bss_tile_map_dims", "bss_tile_map_copy_csr",
+            "bss_destroy_tile_map", "bss_permute", "bss_sparse_attention", "bss_dense_attention",
+            "bss_get_device_status", "bss_status_string", "bss_last_error_message", "bss_version",
+            "bss_diag_mma_tile")
+
+
+def load(path: str | None = None):
+    """Load libbss.so (raises if it is missing)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = path or LIB_PATH
+    if not os.path.exists(path):
+        raise RuntimeError(f"{path} is missing: build it with `python -m block_sparse_spatio_gb300.build`")
+    lib = ctypes.CDLL(path)
+    p, i32, st = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int
+    MP = ctypes.POINTER(_MaskParams)
+    lib.bss_build_tile_map.argtypes = [MP, i32, i32, ctypes.POINTER(p), p]
+    lib.bss_build_tile_map.restype = st
+    lib.bss_tile_map_stats.argtypes = [p, i32, ctypes.POINTER(ctypes.c_int64)]
+    lib.bss_tile_map_stats.restype = st
+    lib.bss_tile_map_dims.argtypes = [p, i32, ctypes.POINTER(ctypes.c_int32)]
+    lib.bss_tile_map_dims.restype = st
+    lib.bss_tile_map_copy_csr.argtypes = [p, i32, p, p]
+    lib.bss_tile_map_copy_csr.restype = st
+    lib.bss_destroy_tile_map.argtypes = [p]
+    lib.bss_destroy_tile_map.restype = None
+    lib.bss_permute.argtypes = [p, p, p, i32, MP, i32, p]
+    lib.bss_permute.restype = st
+    lib.bss_sparse_attention.argtypes = [p, p, p, p, p, p, p, i32, ctypes.c_float, p]
+    lib.bss_sparse_attention.restype = st
+    lib.bss_dense_attention.argtypes = [p, p, p, p, p, i32, i32, i32, ctypes.c_float, p]
+    lib.bss_dense_attention.restype = st
+    lib.bss_get_device_status.argtypes = [p]
+    lib.bss_get_device_status.restype = st
+    lib.bss_status_string.argtypes = [st]
+    lib.bss_status_string.restype = ctypes.c_char_p
+    lib.bss_last_error_message.argtypes = []
+    lib.bss_last_error_message.restype = ctypes.c_char_p
+    lib.bss_version.argtypes = []
+    lib.bss_version.restype = i32
+    lib.bss_diag_mma_tile.argtypes = [p, p, p, p, p, p, i32, p]
+    lib.bss_diag_mma_tile.restype = st
+    _lib = lib
+    return lib
+
+
+def _check(status: int):
+    if status != 0:
+        raise BssError(status, load().bss_last_error_message().decode())
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream))
+
+
+def _dev_tensor(t, name, dtype=None):
+    import torch
+    if t is None:
+        return
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+
+
+class TileMap:
+    """Owning wrapper of a ``bss_tile_map`` handle."""
+
+    def __init__(self, handle: ctypes.c_void_p, params: MaskParams, BQ: int, BKV: int):
+        self._h = handle
+        self.params, self.BQ, self.BKV = params, BQ, BKV
+
+    @property
+    def handle(self):
+        if self._h is None:
+            raise ValueError("tile map destroyed")
+        return self._h
+
+    def stats(self, kind: int) -> dict:
+        return tile_map_stats(self, kind)
+
+    def dims(self, kind: int):
+        return tile_map_dims(self, kind)
+
+    def csr(self, kind: int):
+        return tile_map_copy_csr(self, kind)
+
+    def destroy(self):
+        if self._h is not None and _lib is not None:
+            _lib.bss_destroy_tile_map(self._h)
+        self._h = None
+
+    def __del__(self):
+        try:
+            self.destroy()
+        except Exception:
+            pass
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.destroy()
+
+
+def build_tile_map(params: MaskParams, BQ: int = 128, BKV: int = 128, stream=None) -> TileMap:
+    lib = load()
+    h = ctypes.c_void_p()
+    mp = params.c()
+    _check(lib.bss_build_tile_map(ctypes.byref(mp), BQ, BKV, ctypes.byref(h), _stream(stream)))
+    return TileMap(h, params, BQ, BKV)
+
+
+def _raw_handle(m):
+    return m.handle if isinstance(m, TileMap) else m
+
+
+def tile_map_stats(m, kind: int) -> dict:
+    out = (ctypes.c_int64 * 6)()
+    _check(load().bss_tile_map_stats(_raw_handle(m), kind, out))
+    return dict(zip(STAT_NAMES, [int(x) for x in out]))
+
+
+def tile_map_dims(m, kind: int):
+    out = (ctypes.c_int32 * 4)()
+    _check(load().bss_tile_map_dims(_raw_handle(m), kind, out))
+    return tuple(int(x) for x in out)  # nq, nkv, nnz, ncols
+
+
+def tile_map_copy_csr(m, kind: int):
+    nq, nkv, nnz, ncols = tile_map_dims(m, kind)
+    row_ptr = np.zeros(nq + 1, dtype=np.int32)
+    entries = np.zeros(max(nnz, 1), dtype=np.int32)
+    _check(load().bss_tile_map_copy_csr(_raw_handle(m), kind, row_ptr.ctypes.data, entries.ctypes.data))
+    return row_ptr, entries[:nnz]
+
+
+def destroy_tile_map(m):
+    if isinstance(m, TileMap):
+        m.destroy()
+    else:
+        load().bss_destroy_tile_map(m)
+
+
+def permute(x, out, head_is_temporal, params: MaskParams, inverse: bool = False, stream=None):
+    """out <- per-head (F,H,W) -> (H,W,F) permutation of x (inverse=True: back)."""
+    import torch
+    _dev_tensor(x, "x", torch.bfloat16)
+    _dev_tensor(out, "out", torch.bfloat16)
+    _dev_tensor(head_is_temporal, "head_is_temporal", torch.uint8)
+    _check(load().bss_permute(_ptr(x), _ptr(out), _ptr(head_is_temporal), x.shape[0], ctypes.byref(params.c()),
+                              int(bool(inverse)), _stream(stream)))
+    return out
+
+
+def sparse_attention(Q, K, V, O, tile_map: TileMap, head_is_temporal=None, lse=None, softmax_scale: float = 0.0,
+                     stream=None):
+    """O <- block-sparse attention of [H][N][d] bf16 Q, K, V (temporal heads pre-permuted)."""
+    import torch
+    for t, n in ((Q, "Q"), (K, "K"), (V, "V"), (O, "O")):
+        _dev_tensor(t, n, torch.bfloat16)
+    _dev_tensor(head_is_temporal, "head_is_temporal", torch.uint8)
+    _dev_tensor(lse, "lse", torch.float32)
+    _check(load().bss_sparse_attention(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(lse), tile_map.handle,
+                                       _ptr(head_is_temporal), Q.shape[0], float(softmax_scale), _stream(stream)))
+    return O
+
+
+def dense_attention(Q, K, V, O, lse=None, softmax_scale: float = 0.0, stream=None):
+    """O <- dense attention of [H][N][d] bf16 Q, K, V (the control)."""
+    import torch
+    for t, n in ((Q, "Q"), (K, "K"), (V, "V"), (O, "O")):
+        _dev_tensor(t, n, torch.bfloat16)
+    _dev_tensor(lse, "lse", torch.float32)
+    H, N, d = Q.shape
+    _check(load().bss_dense_attention(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(lse), H, N, d, float(softmax_scale),
+                                      _stream(stream)))
+    return O
+
+
+def get_device_status(stream=None) -> int:
+    """Synchronize and return (and clear) the device status word; 0 = OK."""
+    return int(load().bss_get_device_status(_stream(stream)))
+
+
+def status_string(status: int) -> str:
+    return load().bss_status_string(status).decode()
+
+
+def diag_mma_tile(A, B, P, V, S, O, stream=None):
+    """One-tile tensor-core self-test: S = A B^T, O = P V (see include/bss_diag.h)."""
+    _check(load().bss_diag_mma_tile(_ptr(A), _ptr(B), _ptr(P), _ptr(V), _ptr(S), _ptr(O), A.shape[1],
+                                    _stream(stream)))
+    return S, O
+
+
+def attention_step(Q, K, V, O, tile_map: TileMap, head_is_temporal, Qp, Kp, Vp, Op, lse=None, stream=None):
+    """The per-layer path of the blog's Figure 8 on one GPU: permute the temporal
+    heads' Q, K, V to (H,W,F), run block-sparse attention, restore O's order.
+    Q, K, V, O are in (F,H,W) order; Qp, Kp, Vp, Op are caller-owned workspaces."""
+    p = tile_map.params
+    if p.temporal_permuted:
+        permute(Q, Qp, head_is_temporal, p, False, stream)
+        permute(K, Kp, head_is_temporal, p, False, stream)
+        permute(V, Vp, head_is_temporal, p, False, stream)
+        sparse_attention(Qp, Kp, Vp, Op, tile_map, head_is_temporal, lse, stream=stream)
+        permute(Op, O, head_is_temporal, p, True, stream)
+    else:
+        sparse_attention(Q, K, V, O, tile_map, head_is_temporal, lse, stream=stream)
+    return O

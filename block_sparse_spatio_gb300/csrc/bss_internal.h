@@ -1,0 +1,80 @@
+// bss_internal.h -- host-side structures shared by the library's translation
+// units (not part of the C ABI).
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime_api.h>
+
+#include <cstdint>
+
+#include "bss.h"
+
+namespace bss {
+
+constexpr uint64_t kMapMagic = 0x6273735f6d617031ull;  // "bss_map1"
+
+// Mask code used inside kernels: which coordinate predicate a head evaluates.
+enum MaskCode : int32_t {
+    MASK_SPATIAL = 0,        // frame band + sink, (F,H,W) columns
+    MASK_TEMPORAL_VIRT = 1,  // raster band, (H,W,F) rows, sink segment + band columns
+    MASK_TEMPORAL_FHW = 2,   // raster band evaluated in (F,H,W) order (striped)
+    MASK_DENSE = 3           // every real pair
+};
+
+struct KindMap {
+    int32_t code;     // MaskCode of this kind
+    int32_t nkv;      // kv tiles
+    int32_t ncols;    // key columns (N, or S_pad + N)
+    int64_t nnz;      // CSR entries
+    int32_t* d_row_ptr = nullptr;  // [nq + 1]
+    int32_t* d_entries = nullptr;  // [nnz]
+    int32_t* d_order = nullptr;    // [nq] q tiles, most entries first
+    int64_t stats[BSS_STAT_COUNT] = {0, 0, 0, 0, 0, 0};
+};
+
+struct Geom {
+    int32_t F, S, N, wf, ws, S_pad;
+};
+
+// tile-map builder (bss_tilemap.cu)
+bss_status build_kind_map(const Geom& g, int32_t code, int32_t rounding, int32_t BQ, int32_t BKV, int32_t nq,
+                          KindMap* km, cudaStream_t stream);
+
+// permutation kernel launch (bss_permute.cu)
+bss_status launch_permute(const void* in, void* out, const uint8_t* flags, int32_t H, int32_t F, int32_t S,
+                          int32_t d, int32_t inverse, cudaStream_t stream);
+
+// attention launch (bss_attention.cu)
+struct AttnLaunch {
+    const void *Q, *K, *V;
+    void* O;
+    float* lse;
+    const uint8_t* flags;
+    int32_t H, N, d, F, S, S_pad, wf, ws;
+    int32_t code[2];  // mask code of kind 0 / kind 1
+    int32_t dense;
+    int32_t nq;
+    const int32_t* row_ptr[2];
+    const int32_t* entries[2];
+    const int32_t* order[2];
+    float softmax_scale;
+};
+bss_status launch_attention(const AttnLaunch& a, cudaStream_t stream);
+
+// helpers (bss_api.cu)
+bss_status set_error(bss_status st, const char* fmt, ...);
+bss_status cuda_check(cudaError_t e, const char* what);
+int* device_status_ptr();  // per-device status word (device address)
+bss_status encode_tmap_3d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint64_t heads,
+                          uint64_t row_stride_bytes, uint64_t head_stride_bytes, uint32_t box_inner,
+                          uint32_t box_rows);
+int num_sms();
+
+}  // namespace bss
+
+struct bss_tile_map_s {
+    uint64_t magic;
+    bss_mask_params p;
+    int32_t BQ, BKV, nq, device;
+    bss::Geom g;
+    bss::KindMap kind[2];
+};

@@ -1,0 +1,188 @@
+/*
+ * bss.h -- C ABI of the block-sparse spatio-temporal attention library for
+ * one NVIDIA GB300 GPU (sm_103a).
+ *
+ * The method follows the blog "Accelerating Spatio-Temporal Attention for
+ * Video Diffusion on TPUs" (Google Developers).  Each head of a video
+ * diffusion transformer is routed by a boolean flag to a spatial mask (a band
+ * of nearby frames) or a temporal mask (a band of nearby raster positions
+ * across all frames); both masks also keep full attention to the first frame
+ * (Figure 3).  Attention is computed tile by tile; tiles are full, boundary
+ * or skipped (section "Logical sparsity is not physical sparsity"), full tiles
+ * run without any mask (section "Avoid intra-tile masking when there is
+ * nothing to mask"), and optionally the mask is rounded to the tile grid so
+ * that only padding needs masking (section "Align the sparse mask with final
+ * execution").  Temporal heads are permuted from frame-major (F,H,W) to
+ * temporal-major (H,W,F) token order so their band becomes contiguous
+ * (section "Arrange tokens for efficient temporal access", Figure 9).
+ *
+ * Conventions for every call:
+ *  - Tensors are caller-owned device memory, contiguous [H][N][d] bf16
+ *    (head-major, then token, then channel), 16-byte aligned.  N = F*Hs*Ws.
+ *  - Calls are asynchronous on `stream` unless marked "synchronous".
+ *  - Host-detectable errors are returned before anything is launched, and a
+ *    message is available from bss_last_error_message() (thread-local).
+ *  - Device-side problems (a pipeline wait that exceeded its time limit) are
+ *    recorded in a per-device status word read by bss_get_device_status();
+ *    the kernel then returns normally instead of hanging.
+ *  - No call allocates device memory except bss_build_tile_map.
+ *  - Handles are not thread-safe; one GPU, one stream per call.
+ */
+#ifndef BSS_H_
+#define BSS_H_
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    BSS_OK = 0,
+    BSS_ERR_INVALID_ARG = 1, /* null / misaligned pointer, bad size, stale handle */
+    BSS_ERR_UNSUPPORTED = 2, /* valid but not implemented (tile shape, head_dim, ...) */
+    BSS_ERR_CUDA = 3,        /* a CUDA runtime or driver call failed */
+    BSS_ERR_TIMEOUT = 4,     /* a device-side pipeline wait gave up (status word) */
+    BSS_ERR_OOM = 5          /* device memory allocation failed */
+} bss_status;
+
+/* Mask kinds selected per head by the routing flag (section "Support dynamic
+ * routing with fixed tensor shapes": one boolean per head). */
+enum { BSS_KIND_SPATIAL = 0, BSS_KIND_TEMPORAL = 1 };
+
+/* Tile classes stored in the top two bits of a tile-map entry. */
+enum { BSS_CLASS_FULL = 0, BSS_CLASS_BOUNDARY = 1, BSS_CLASS_PAD = 2 };
+#define BSS_CLASS_SHIFT 30
+#define BSS_TILE_INDEX_MASK 0x3FFFFFFF
+
+/* Indices of the statistics returned by bss_tile_map_stats. */
+enum {
+    BSS_STAT_FULL = 0,          /* tiles run without a mask */
+    BSS_STAT_BOUNDARY = 1,      /* tiles that evaluate the coordinate predicate */
+    BSS_STAT_PAD = 2,           /* kept tiles that mask padding columns only */
+    BSS_STAT_SKIP = 3,          /* tiles never visited */
+    BSS_STAT_RETAINED = 4,      /* query-key pairs the result is defined over */
+    BSS_STAT_EXACT_RETAINED = 5,/* pairs retained by the exact (unrounded) mask */
+    BSS_STAT_COUNT = 6
+};
+
+/* Video geometry and mask parameters.
+ *   F, Hs, Ws          latent frames, height and width; S = Hs*Ws, N = F*S.
+ *   head_dim           64 or 128.
+ *   spatial_frame_window   spatial heads keep keys with |f_k - f_q| <= window
+ *                          (a local frame band, Figure 3 left).
+ *   temporal_raster_window temporal heads keep keys with |s_k - s_q| <= window
+ *                          in the raster index s = h*Ws + w, across all frames
+ *                          (Figure 3 right; the band shape is this library's
+ *                          reading of "a small spatial region").
+ *   sink_frames        frames kept by every query (the first-frame attention
+ *                      sink, F00); only 1 is supported.
+ *   temporal_permuted  1: temporal heads are in (H,W,F) order and their keys
+ *                      are addressed as a sink segment (the frame-0 keys,
+ *                      S rounded up to BKV columns) followed by the N permuted
+ *                      rows; 0: temporal heads stay in (F,H,W) order and the
+ *                      kernel evaluates the striped predicate (the blog's
+ *                      "handling temporal access inside the kernel").
+ *   rounding           0: exact mask (full / boundary / skip tiles);
+ *                      1: tile-aligned mask, a tile is kept iff at least half
+ *                      of its real pairs are retained, then only padding
+ *                      columns are masked. */
+typedef struct {
+    int32_t F, Hs, Ws;
+    int32_t head_dim;
+    int32_t spatial_frame_window;
+    int32_t temporal_raster_window;
+    int32_t sink_frames;
+    int32_t temporal_permuted;
+    int32_t rounding;
+} bss_mask_params;
+
+/* Opaque tile map: per mask kind, a CSR list of non-skipped kv tiles for every
+ * q tile (ascending kv index, class in bits 30..31), its statistics and a
+ * longest-first q-tile order.  Owns device memory; free with
+ * bss_destroy_tile_map. */
+typedef struct bss_tile_map_s* bss_tile_map;
+
+/* Build the tile maps of both mask kinds for tiles of BQ query rows by BKV key
+ * columns (section "Logical sparsity is not physical sparsity": full, boundary
+ * and skipped tiles; section "Align the sparse mask with final execution":
+ * tile-aligned rounding).  Counts retained pairs per tile on the GPU, compacts
+ * non-skipped tiles to CSR.  Any BQ, BKV in [16, 65536] builds a map (for
+ * statistics); bss_sparse_attention needs BQ = BKV = 128.
+ * Synchronous: it allocates the map's device memory, synchronizes `stream`
+ * and returns the map in *out.  Errors: INVALID_ARG (null, non-positive or
+ * inconsistent sizes, windows < 0), UNSUPPORTED (sink_frames != 1,
+ * head_dim not 64/128), OOM, CUDA. */
+bss_status bss_build_tile_map(const bss_mask_params* params, int32_t BQ, int32_t BKV, bss_tile_map* out,
+                              cudaStream_t stream);
+
+/* Copy statistics of one kind into host out[BSS_STAT_COUNT] (indices above).
+ * Host-only, no device work.  Errors: INVALID_ARG (null, stale handle, kind). */
+bss_status bss_tile_map_stats(bss_tile_map map, int32_t kind, int64_t* out);
+
+/* Host out[4] = { number of q tiles, number of kv tiles, number of CSR
+ * entries, number of key columns (N, or S_pad + N for permuted temporal) }. */
+bss_status bss_tile_map_dims(bss_tile_map map, int32_t kind, int32_t* out);
+
+/* Copy the CSR of one kind to HOST buffers: row_ptr[nq + 1] and entries[nnz]
+ * (sizes from bss_tile_map_dims).  Synchronous.  Errors: INVALID_ARG, CUDA. */
+bss_status bss_tile_map_copy_csr(bss_tile_map map, int32_t kind, int32_t* row_ptr, int32_t* entries);
+
+/* Free a tile map (no-op for NULL).  The caller must make sure no launch that
+ * uses it is still running.  Using the handle afterwards returns INVALID_ARG. */
+void bss_destroy_tile_map(bss_tile_map map);
+
+/* Flag-driven token permutation (section "Arrange tokens for efficient
+ * temporal access", Figure 9; section "Support dynamic routing with fixed
+ * tensor shapes").  For head h with head_is_temporal[h] != 0:
+ *   forward (inverse = 0):  out[h][s*F + f] = in[h][f*S + s]   (F,H,W)->(H,W,F)
+ *   inverse (inverse = 1):  out[h][f*S + s] = in[h][s*F + f]
+ * heads with flag 0 are copied unchanged.  in, out: device [H][N][d] bf16,
+ * non-overlapping; head_is_temporal: device uint8[H] (NULL = all spatial).
+ * Errors: INVALID_ARG (null / misaligned / overlapping, H <= 0), UNSUPPORTED. */
+bss_status bss_permute(const void* in, void* out, const uint8_t* head_is_temporal, int32_t H,
+                       const bss_mask_params* params, int32_t inverse, cudaStream_t stream);
+
+/* Block-sparse attention O = softmax(Q K^T * scale) V over the retained pairs
+ * of each head's mask (blog: tiles of Q[i1:i2] K[j1:j2]^T with running softmax
+ * statistics; full tiles mask-free, boundary tiles masked, skipped tiles never
+ * visited; both paths combined through the softmax normalisation).
+ *   Q, K, V, O  device [H][N][d] bf16; temporal heads already permuted when
+ *               the map was built with temporal_permuted = 1.
+ *   lse         optional device float[H][N], natural-log log-sum-exp per row
+ *               (-inf for a row with no retained key, whose O row is 0).
+ *   map         built with BQ = BKV = 128 for this geometry.
+ *   head_is_temporal  device uint8[H] (NULL = all spatial); changing flags
+ *               needs no map rebuild.
+ *   softmax_scale    <= 0 selects 1/sqrt(head_dim).
+ * Errors: INVALID_ARG, UNSUPPORTED (map tile shape), CUDA.  A device-side
+ * timeout is reported by bss_get_device_status. */
+bss_status bss_sparse_attention(const void* Q, const void* K, const void* V, void* O, float* lse,
+                                bss_tile_map map, const uint8_t* head_is_temporal, int32_t H,
+                                float softmax_scale, cudaStream_t stream);
+
+/* Dense attention control (the blog's B0 dense baseline): the same kernel
+ * visiting every tile, masking only padding columns of the last kv tile.
+ * Q, K, V, O: device [H][N][d] bf16, d = 64 or 128; lse optional. */
+bss_status bss_dense_attention(const void* Q, const void* K, const void* V, void* O, float* lse, int32_t H,
+                               int32_t N, int32_t d, float softmax_scale, cudaStream_t stream);
+
+/* Synchronizes `stream`, returns the current device's status word (BSS_OK or
+ * the first device-side error since the last call) and clears it. */
+bss_status bss_get_device_status(cudaStream_t stream);
+
+/* Static text for a status code. */
+const char* bss_status_string(bss_status status);
+
+/* Text of the last host-side error on the calling thread ("" if none). */
+const char* bss_last_error_message(void);
+
+/* Library version (major*10000 + minor*100 + patch). */
+int32_t bss_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* BSS_H_ */

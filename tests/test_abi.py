@@ -1,0 +1,126 @@
+"""CPU checks of the C ABI: the library builds, loads, exports every function
+that include/*.h declares, and rejects bad arguments on the host before any
+device work (these calls never touch a GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import block_sparse_spatio_gb300 as bss
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if not fn.endswith(".h"):
+            continue
+        text = open(os.path.join(ROOT, "include", fn)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names.update(re.findall(r"\b(bss_[a-z0-9_]+)\s*\(", text))
+    return sorted(names)
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from block_sparse_spatio_gb300 import build
+    build.build()
+    return bss.load()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_functions()
+    assert len(names) >= 12
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(bss.EXPORTED)
+
+
+def test_status_strings(lib):
+    assert lib.bss_status_string(0) == b"BSS_OK"
+    assert lib.bss_status_string(4) == b"BSS_ERR_TIMEOUT"
+    assert lib.bss_version() >= 100
+
+
+def _params(**kw):
+    base = dict(F=8, Hs=16, Ws=24, head_dim=128, spatial_frame_window=2, temporal_raster_window=40)
+    base.update(kw)
+    return bss.MaskParams(**base).c()
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(F=0), 1), (dict(Hs=-1), 1), (dict(head_dim=96), 2), (dict(spatial_frame_window=-1), 1),
+    (dict(sink_frames=2), 2), (dict(rounding=3), 1), (dict(temporal_permuted=2), 1),
+])
+def test_build_tile_map_rejects_bad_params(lib, kw, code):
+    h = ctypes.c_void_p()
+    p = _params(**kw)
+    assert lib.bss_build_tile_map(ctypes.byref(p), 128, 128, ctypes.byref(h), None) == code
+    assert h.value is None
+    assert lib.bss_last_error_message() != b""
+
+
+def test_build_tile_map_rejects_bad_tiles_and_null(lib):
+    h = ctypes.c_void_p()
+    p = _params()
+    assert lib.bss_build_tile_map(ctypes.byref(p), 8, 128, ctypes.byref(h), None) == 1
+    assert lib.bss_build_tile_map(ctypes.byref(p), 128, 0, ctypes.byref(h), None) == 1
+    assert lib.bss_build_tile_map(None, 128, 128, ctypes.byref(h), None) == 1
+    assert lib.bss_build_tile_map(ctypes.byref(p), 128, 128, None, None) == 1
+
+
+def test_calls_with_stale_or_null_handles(lib):
+    bogus = ctypes.c_void_p(0x1234)
+    out = (ctypes.c_int64 * 6)()
+    assert lib.bss_tile_map_stats(bogus, 0, out) == 1
+    assert lib.bss_tile_map_stats(None, 0, out) == 1
+    dims = (ctypes.c_int32 * 4)()
+    assert lib.bss_tile_map_dims(bogus, 0, dims) == 1
+    assert lib.bss_tile_map_copy_csr(bogus, 0, None, None) == 1
+    x = ctypes.c_void_p(0x10000)
+    assert lib.bss_sparse_attention(x, x, x, x, None, bogus, None, 2, 0.0, None) == 1
+    lib.bss_destroy_tile_map(None)
+    lib.bss_destroy_tile_map(bogus)  # unknown handles are ignored
+
+
+def test_permute_rejects_bad_pointers(lib):
+    p = _params()
+    a, b = ctypes.c_void_p(0x10000), ctypes.c_void_p(0x20008)
+    assert lib.bss_permute(None, a, None, 2, ctypes.byref(p), 0, None) == 1
+    assert lib.bss_permute(a, b, None, 2, ctypes.byref(p), 0, None) == 1          # misaligned
+    assert lib.bss_permute(a, ctypes.c_void_p(0x10010), None, 2, ctypes.byref(p), 0, None) == 1  # overlap
+    assert lib.bss_permute(a, ctypes.c_void_p(0x1000000000), None, 0, ctypes.byref(p), 0, None) == 1  # H
+    assert lib.bss_permute(a, ctypes.c_void_p(0x1000000000), None, 2, ctypes.byref(p), 5, None) == 1  # inverse
+
+
+def test_dense_attention_rejects_bad_args(lib):
+    a = ctypes.c_void_p(0x10000)
+    assert lib.bss_dense_attention(None, a, a, a, None, 1, 256, 128, 0.0, None) == 1
+    assert lib.bss_dense_attention(a, a, a, ctypes.c_void_p(0x10004), None, 1, 256, 128, 0.0, None) == 1
+    assert lib.bss_dense_attention(a, a, a, a, None, 0, 256, 128, 0.0, None) == 1
+    assert lib.bss_dense_attention(a, a, a, a, None, 1, 256, 80, 0.0, None) == 2
+    assert lib.bss_dense_attention(a, a, a, a, None, 1, 256, 128, float("nan"), None) == 1
+
+
+def test_diag_rejects_bad_args(lib):
+    a = ctypes.c_void_p(0x10000)
+    assert lib.bss_diag_mma_tile(None, a, a, a, a, a, 128, None) == 1
+    assert lib.bss_diag_mma_tile(a, a, a, a, a, a, 32, None) == 2
+
+
+def test_product_package_does_not_import_oracle():
+    import ast
+    pkg = os.path.join(ROOT, "block_sparse_spatio_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for fn in files:
+            if fn.endswith(".py"):
+                tree = ast.parse(open(os.path.join(dirpath, fn)).read())
+                for node in ast.walk(tree):
+                    if isinstance(node, ast.Import):
+                        assert all(not a.name.startswith("oracle") for a in node.names), fn
+                    if isinstance(node, ast.ImportFrom):
+                        assert not (node.module or "").startswith("oracle"), fn
+            if fn.endswith((".cu", ".cuh", ".h")):
+                assert "oracle" not in open(os.path.join(dirpath, fn)).read().lower(), fn

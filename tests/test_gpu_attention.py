@@ -1,0 +1,161 @@
+"""GPU block-sparse attention against the fp64 oracle.
+
+Bar (floating point): max |dO| <= 1e-2, mean |dO| <= 1e-3, rel-L2 <= 1e-2 and
+|dLSE| <= 1e-3 on N(0,1) inputs; the coverage (Q = 0) and poison tests pin
+which keys each row sees exactly."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+from _util import compare, oracle_kind, oracle_rows, run_gpu
+
+SMALL_CASES = [  # name, F, Hs, Ws, d, wf, ws, flags
+    ("tiny", 4, 8, 8, 64, 1, 10, [0]),
+    ("small", 8, 16, 24, 128, 2, 40, [0, 1]),
+    ("ragged_s63_d64", 5, 7, 9, 64, 1, 5, [1, 0]),
+    ("ragged_s130_d128", 3, 10, 13, 128, 0, 20, [1, 1, 0]),
+    ("ragged_s130_d64", 3, 10, 13, 64, 1, 200, [0, 1]),
+]
+
+
+def _inputs(H, N, d, seed):
+    w = W.SMALL
+    return W.qkv(w, H=H, N=N, d=d, seed=seed)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("case", SMALL_CASES, ids=[c[0] for c in SMALL_CASES])
+@pytest.mark.parametrize("rounding", [0, 1])
+@pytest.mark.parametrize("tperm", [1, 0])
+def test_attention_matches_oracle_all_rows(bss, case, rounding, tperm):
+    name, F, Hs, Ws, d, wf, ws, flags = case
+    N = F * Hs * Ws
+    q, k, v = _inputs(len(flags), N, d, seed=len(name))
+    p = bss.MaskParams(F, Hs, Ws, d, wf, ws, temporal_permuted=tperm, rounding=rounding)
+    out, lse, stats = run_gpu(bss, q, k, v, flags, p)
+    g = oracle.Geometry(F, Hs, Ws, wf=wf, ws=ws, bkv=128)
+    for h, fl in enumerate(flags):
+        kind = oracle_kind(fl, tperm)
+        Oref, lref = oracle_rows(q, k, v, h, kind, g, None, rounding)
+        compare(out[h].numpy(), lse[h].numpy(), Oref, lref, f"{name} head {h} kind {kind} rounding {rounding}")
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("shape", [(2, 3072, 128), (1, 315, 64), (3, 390, 128), (1, 130, 64)])
+def test_dense_matches_oracle(bss, shape):
+    H, N, d = shape
+    q, k, v = _inputs(H, N, d, seed=N)
+    out, lse, _ = run_gpu(bss, q, k, v, [0] * H, None, dense=True)
+    g = oracle.Geometry(1, 1, N)
+    for h in range(H):
+        Oref, lref = oracle.attention(W.bf16_bits(q[h]), W.bf16_bits(k[h]), W.bf16_bits(v[h]), oracle.DENSE, g)
+        compare(out[h].numpy(), lse[h].numpy(), Oref, lref, f"dense {shape} head {h}")
+
+
+def _row_counts(kind, F, S, wf, ws):
+    t = np.arange(F * S)
+    f, s = t // S, t % S
+    if kind == oracle.SPATIAL:
+        return S * (np.minimum(f + wf, F - 1) - np.maximum(f - wf, 0) + 1 + (f > wf))
+    b = np.minimum(s + ws, S - 1) - np.maximum(s - ws, 0) + 1
+    return F * b + (S - b)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("tperm", [1, 0])
+def test_zero_query_coverage_is_exact(bss, tperm):
+    # Q = 0: every retained key has weight 1, so exp(LSE) = |R_i| exactly and
+    # O = mean of V over R_i -- this pins the set of keys each row sees.
+    F, Hs, Ws, d, wf, ws = 8, 16, 24, 128, 2, 40
+    S, N = Hs * Ws, F * Hs * Ws
+    flags = [0, 1]
+    q, k, v = _inputs(2, N, d, seed=77)
+    q = torch.zeros_like(q)
+    p = bss.MaskParams(F, Hs, Ws, d, wf, ws, temporal_permuted=tperm, rounding=0)
+    out, lse, _ = run_gpu(bss, q, k, v, flags, p)
+    for h, fl in enumerate(flags):
+        kind = oracle.SPATIAL if fl == 0 else oracle.TEMPORAL_FHW
+        cnt = _row_counts(kind, F, S, wf, ws)
+        got = np.rint(np.exp(lse[h].numpy().astype(np.float64))).astype(np.int64)
+        assert np.array_equal(got, cnt), f"head {h}: {np.nonzero(got != cnt)[0][:10]}"
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("tperm", [1, 0])
+def test_poisoned_excluded_keys_leave_output_bit_identical(bss, tperm):
+    F, Hs, Ws, d, wf, ws = 8, 16, 24, 128, 2, 40
+    S, N = Hs * Ws, F * Hs * Ws
+    flags = [0, 1]
+    q, k, v = _inputs(2, N, d, seed=78)
+    p = bss.MaskParams(F, Hs, Ws, d, wf, ws, temporal_permuted=tperm, rounding=0)
+    out1, lse1, _ = run_gpu(bss, q, k, v, flags, p)
+    k2, v2 = k.clone(), v.clone()
+    # spatial head 0: frames 1..4 are excluded for queries of frame 7
+    k2[0, S:5 * S] = 1.0e4
+    v2[0, S:5 * S] = -1.0e4
+    # temporal head 1: raster >= 200 of frames >= 1 is excluded for queries with raster <= 40
+    t = torch.arange(N)
+    far = ((t % S) >= 200) & ((t // S) >= 1)
+    k2[1, far] = -1.0e4
+    v2[1, far] = 1.0e4
+    out2, lse2, _ = run_gpu(bss, q, k2, v2, flags, p)
+    rows0 = torch.arange(7 * S, 8 * S)
+    rows1 = torch.nonzero((t % S) <= 40).flatten()
+    assert torch.equal(out1[0, rows0], out2[0, rows0])
+    assert torch.equal(lse1[0, rows0], lse2[0, rows0])
+    assert torch.equal(out1[1, rows1], out2[1, rows1])
+    assert torch.equal(lse1[1, rows1], lse2[1, rows1])
+    assert not torch.equal(out1[0, :S], out2[0, :S])  # frame-0 queries do see frames 1..2
+
+
+def _full_size(bss, wl, tperm, rounding, heads, nrows):
+    dev = torch.device("cuda")
+    Q, K, V = W.qkv_device(wl, dev)
+    flags = wl.head_flags()
+    p = bss.MaskParams(wl.F, wl.Hs, wl.Ws, wl.d, wl.wf, wl.ws, temporal_permuted=tperm, rounding=rounding)
+    O = torch.empty_like(Q)
+    lse = torch.empty(wl.H, wl.N, device=dev)
+    fl = torch.tensor(flags, dtype=torch.uint8, device=dev)
+    ws_ = [torch.empty_like(Q) for _ in range(4)]
+    with bss.build_tile_map(p) as tm:
+        bss.attention_step(Q, K, V, O, tm, fl, *ws_, lse=lse)
+        torch.cuda.synchronize()
+    assert bss.get_device_status() == 0
+    g = oracle.Geometry(wl.F, wl.Hs, wl.Ws, wf=wl.wf, ws=wl.ws, bkv=128)
+    rows = W.sample_rows(wl.N, nrows, seed=wl.index)
+    for h in heads:
+        kind = oracle_kind(flags[h], tperm)
+        qh, kh, vh = (x[h].cpu() for x in (Q, K, V))
+        Oref, lref = oracle.attention(W.bf16_bits(qh), W.bf16_bits(kh), W.bf16_bits(vh), kind, g, rows=rows,
+                                      rounding=bool(rounding))
+        lrow = lse[h].cpu()
+        if flags[h] and tperm:
+            lrow = lrow[[(r % wl.S) * wl.F + r // wl.S for r in rows]]
+        else:
+            lrow = lrow[rows]
+        compare(O[h, rows].float().cpu().numpy(), lrow.numpy(), Oref, lref,
+                f"{wl.name} head {h} kind {kind} rounding {rounding}")
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("rounding", [0, 1])
+def test_full_size_spatial_75k_sampled(bss, rounding):
+    _full_size(bss, W.SPATIAL_75K, 1, rounding, heads=[0, 4, 9], nrows=24)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("tperm", [1, 0])
+def test_full_size_mixed_75k_sampled(bss, tperm):
+    wl = W.MIXED_75K
+    fl = wl.head_flags()
+    heads = [fl.index(0), fl.index(1), len(fl) - 1 - fl[::-1].index(1)]
+    _full_size(bss, wl, tperm, 0, heads=heads, nrows=24)
+
+
+@pytest.mark.gpu
+def test_full_size_1440p_302k_rounded_sampled(bss):
+    wl = W.P1440_302K
+    fl = wl.head_flags()
+    _full_size(bss, wl, 1, 1, heads=[fl.index(0), fl.index(1)], nrows=12)

@@ -102,3 +102,15 @@ def sample_rows(N: int, count: int, seed: int, BQ: int = 128) -> list:
     fixed = {0, 1, N - 1, N - 2, (N // BQ) * BQ - 1 if N > BQ else 0, min(N - 1, (N // BQ) * BQ)}
     rnd = torch.randint(0, N, (max(0, count - len(fixed)),), generator=g).tolist()
     return sorted(set(int(r) for r in list(fixed) + rnd if 0 <= r < N))
+
+
+def qkv_device(w: Workload, device, seed: int | None = None):
+    """Seeded bf16 Q, K, V [H][N][d] drawn directly on a CUDA device (CUDA
+    generator seeded with the workload index): used where the CPU draw of the
+    full-size tensors would dominate a run.  Values differ from ``qkv`` but are
+    equally seeded and reproducible on a given device type."""
+    g = torch.Generator(device=device).manual_seed(w.index if seed is None else seed)
+    out = []
+    for _ in range(3):
+        out.append(torch.randn(w.H, w.N, w.d, generator=g, device=device, dtype=torch.float32).to(torch.bfloat16))
+    return tuple(out)
