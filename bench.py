@@ -1,0 +1,442 @@
+#!/usr/bin/env python
+"""Benchmark of the block-sparse spatio-temporal attention path on GB300.
+
+Step = one pass of the per-layer hot path of the blog "Accelerating
+Spatio-Temporal Attention for Video Diffusion on TPUs" (Figure 8) over one
+batch of synthetic input, all on the GPU:
+  flag-driven permutation of Q, K, V  ->  block-sparse attention (exact mask,
+  full / boundary tiles)  ->  inverse permutation of O
+on 75,600 tokens (21 x 45 x 80 latent patches) x 10 heads x d = 128, bf16,
+5 spatial heads (frame window 3 + first-frame sink) and 5 temporal heads
+(raster window 612 + sink) picked by seeded flags.  The tile map is built once
+before timing (it depends only on the geometry, as on the pages).
+
+value = effective TFLOP/s = 4 * d * (retained query-key pairs, all heads) /
+step time; ms_per_step is the step time.  Extra keys report the attention
+kernel alone, its roofline against the measured bf16 peak, the dense control,
+the tile-aligned (B3) and the no-permutation variants, the permutation
+bandwidth, an end-to-end number through host buffers, and the fp64 oracle on
+the host cores.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "sparse-attn ms & TFLOP/s, 75.6K tok×10h×d128 bf16, % of BF16 TC peak"
+UNIT = "TFLOP/s"
+FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
+ATTN_SOURCES = ["block_sparse_spatio_gb300/csrc/bss_attention.cu", "block_sparse_spatio_gb300/csrc/bss_ptx.cuh"]
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "attn_fwd_mixed75k_dram_traffic.txt")
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="mixed_75600tok_10h_d128")
+    ap.add_argument("--heads", type=int, default=0, help="override head count (profiling runs)")
+    ap.add_argument("--no-extras", action="store_true", help="skip variants, e2e and cpu baseline")
+    ap.add_argument("--cpu-rows-per-head", type=int, default=2048)
+    return ap.parse_args()
+
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("LOCAL_RANK", "0")),
+            int(os.environ.get("WORLD_SIZE", "1")))
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as fh:
+            p = json.load(fh)
+        return {k: float(p[k]) for k in ("bf16_tflops", "bf16_tflops_sustained", "hbm_gbs")}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def source_hash():
+    h = hashlib.sha256()
+    for rel in ATTN_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_from_profile():
+    """DRAM bytes per attention launch from the committed ncu summary, or None
+    when the kernel source changed since the counters were taken."""
+    try:
+        kv = {}
+        with open(TRAFFIC_FILE) as fh:
+            for line in fh:
+                if ":" in line and not line.startswith("#"):
+                    k, v = line.split(":", 1)
+                    kv[k.strip()] = v.strip()
+        if kv.get("source_sha256_16") != source_hash():
+            return None
+        return float(kv["dram_bytes_per_full_launch"])
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------- oracle (host)
+def oracle_sample(w, q, k, v, flags, rows_per_head, seed):
+    """Time the fp64 oracle on seeded query rows of every head; return
+    (seconds, rows evaluated, retained pairs of those rows)."""
+    import oracle
+    import workloads as W
+    g = oracle.Geometry(w.F, w.Hs, w.Ws, wf=w.wf, ws=w.ws, bkv=128)
+    t0 = time.perf_counter()
+    nrows = 0
+    for h in range(q.shape[0]):
+        kind = oracle.TEMPORAL_PERMUTED if flags[h] else oracle.SPATIAL
+        rows = W.sample_rows(w.N, rows_per_head, seed=seed + h)
+        oracle.attention(W.bf16_bits(q[h]), W.bf16_bits(k[h]), W.bf16_bits(v[h]), kind, g, rows=rows)
+        nrows += len(rows)
+    return time.perf_counter() - t0, nrows
+
+
+def run_reference(args):
+    rank, _, world = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    import workloads as W
+    w = W.BY_NAME[args.workload]
+    H = args.heads or w.H
+    flags = w.head_flags()[:H]
+    q, k, v = W.qkv(w, H=H)
+    flops_total = 4.0 * w.d * retained_total(w, flags)
+    rows_total = H * w.N
+    rows_per_head = max(8, args.cpu_rows_per_head // 8)
+    times = []
+    for i in range(args.warmup + args.steps):
+        dt, nrows = oracle_sample(w, q, k, v, flags, rows_per_head, seed=1000 + i)
+        if i >= args.warmup:
+            times.append(dt * rows_total / nrows)   # seconds for the whole workload
+    step_s = statistics.median(times)
+    val = flops_total / step_s / 1e12
+    cores = oracle.num_threads()
+    sample = (f"{rows_per_head} seeded query rows per head x {H} heads per step "
+              f"({100.0 * rows_per_head * H / rows_total:.2f}% of rows), time scaled to all {rows_total} rows")
+    line = {"impl": "reference", "metric": METRIC, "value": val, "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": w.name, "tokens": w.N, "heads": H, "head_dim": w.d, "mask": "exact"},
+            "cpu_baseline": {"value": val, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def retained_total(w, flags):
+    """Exact retained pairs summed over heads (closed forms of the two masks)."""
+    F, S = w.F, w.S
+    sp = S * S * sum(min(f + w.wf, F - 1) - max(f - w.wf, 0) + 1 + (1 if f > w.wf else 0) for f in range(F))
+    tp = 0
+    for s in range(S):
+        b = min(s + w.ws, S - 1) - max(s - w.ws, 0) + 1
+        tp += F * b + (S - b)
+    tp *= F
+    return sum(tp if fl else sp for fl in flags)
+
+
+# --------------------------------------------------------------------------- GPU arm
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+        return
+    import torch
+    import torch.distributed as dist
+
+    import block_sparse_spatio_gb300 as bss
+    import workloads as W
+
+    rank, local_rank, world = dist_env()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    bss.load()
+    peaks, peak_src = load_peaks()
+
+    w = W.BY_NAME[args.workload]
+    H = args.heads or w.H
+    flags = w.head_flags()[:H]
+    # replicas: every rank runs its own batch (different seed), no data exchange
+    Q, K, V = W.qkv_device(w, dev, seed=w.index + 1000 * rank)
+    if H != w.H:
+        Q, K, V = (x[:H].contiguous() for x in (Q, K, V))
+    O = torch.empty_like(Q)
+    Qp, Kp, Vp, Op = (torch.empty_like(Q) for _ in range(4))
+    fl = torch.tensor(flags, dtype=torch.uint8, device=dev)
+    params = bss.MaskParams(w.F, w.Hs, w.Ws, w.d, w.wf, w.ws, temporal_permuted=1, rounding=0)
+    tm = bss.build_tile_map(params)
+    st = (tm.stats(0), tm.stats(1))
+    retained = sum(st[f]["retained_pairs"] for f in flags)
+    flops = 4.0 * w.d * retained
+    stream = torch.cuda.current_stream()
+    attn_events = []
+
+    def step(record=False):
+        bss.permute(Q, Qp, fl, params, False)
+        bss.permute(K, Kp, fl, params, False)
+        bss.permute(V, Vp, fl, params, False)
+        if record:
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+        bss.sparse_attention(Qp, Kp, Vp, Op, tm, fl)
+        if record:
+            e1.record(stream)
+            attn_events.append((e0, e1))
+        bss.permute(Op, O, fl, params, True)
+
+    launches_per_step = 5
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    status = bss.get_device_status()
+    if status != 0:
+        raise RuntimeError(f"device status {bss.status_string(status)} during warm-up")
+
+    sampler = ClockSampler(local_rank)
+    sampler.start()
+    time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(args.steps):
+        step(record=True)
+    t1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clocks = sampler.stop()
+    elapsed_ms = t0.elapsed_time(t1)
+    if world > 1:
+        tt = torch.tensor([elapsed_ms], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(tt.item())
+    status = bss.get_device_status()
+    if status != 0:
+        raise RuntimeError(f"device status {bss.status_string(status)} in the timed region")
+    ms_per_step = elapsed_ms / args.steps
+    attn_ms = statistics.mean(a.elapsed_time(b) for a, b in attn_events)
+    value = flops * world / (ms_per_step * 1e-3) / 1e12
+    attn_tflops = flops / (attn_ms * 1e-3) / 1e12
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": max(3, args.warmup), "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "tokens": w.N, "frames_x_h_x_w": [w.F, w.Hs, w.Ws], "heads": H,
+                   "head_dim": w.d, "flags_temporal": flags, "spatial_frame_window": w.wf,
+                   "temporal_raster_window": w.ws, "mask": "exact (full/boundary tiles, B2)", "tile": [128, 128],
+                   "step": "permute QKV -> sparse attention -> unpermute O",
+                   "l2": f"inputs larger than L2 (Q+K+V = {3 * Q.numel() * 2 / 1e6:.0f} MB)",
+                   "parallelism": "replicas" if world > 1 else "single GPU",
+                   "retained_pairs": retained,
+                   "retained_fraction": retained / (H * w.N * w.N)},
+        "attention": {"ms": attn_ms, "tflops": attn_tflops,
+                      "frac_of_peak": attn_tflops / peaks["bf16_tflops"],
+                      "frac_of_sustained_peak": attn_tflops / peaks["bf16_tflops_sustained"],
+                      "tile_stats": {"spatial": st[0], "temporal": st[1]}},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+    }
+    traffic = traffic_from_profile()
+    if H != w.H and traffic is not None:
+        traffic = traffic * H / w.H
+    line["roofline"] = {"bound": "tensor", "achieved": attn_tflops, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                        "frac": attn_tflops / peaks["bf16_tflops"], "traffic": traffic,
+                        "peak_source": f"{peak_src} bf16 burst (cuBLAS 8192^3)", "kernel": "attn_fwd_kernel<128>"}
+
+    if not args.no_extras and rank == 0:
+        line["variants"] = variants(bss, torch, W, w, H, Q, K, V, dev, peaks, flags)
+        line["e2e"] = e2e(bss, torch, params, tm, flags, Q, K, V, flops, args)
+    if not args.no_extras and rank == 0 and world == 1:
+        line["cpu_baseline"] = cpu_baseline(w, Q, K, V, flags, args, flops)
+    tm.destroy()
+    if world > 1:
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def _time(torch, fn, reps=5, warm=3):
+    for _ in range(warm):
+        fn()
+    torch.cuda.synchronize()
+    s = torch.cuda.current_stream()
+    ev = []
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(s)
+        fn()
+        b.record(s)
+        ev.append((a, b))
+    torch.cuda.synchronize()
+    return statistics.median(a.elapsed_time(b) for a, b in ev)
+
+
+def variants(bss, torch, W, w, H, Q, K, V, dev, peaks, flags):
+    """Attention-kernel timings of the pages' other measurements, same inputs."""
+    out = {}
+    O = torch.empty_like(Q)
+    dense_ms = _time(torch, lambda: bss.dense_attention(Q, K, V, O))
+    dense_flops = 4.0 * w.d * H * w.N * w.N
+    out["dense_control"] = {"ms": dense_ms, "tflops": dense_flops / dense_ms / 1e9,
+                            "frac_of_peak": dense_flops / dense_ms / 1e9 / peaks["bf16_tflops"]}
+    zeros = torch.zeros(H, dtype=torch.uint8, device=dev)
+    for name, rnd in (("spatial_exact_B2", 0), ("spatial_tile_aligned_B3", 1)):
+        p = bss.MaskParams(w.F, w.Hs, w.Ws, w.d, w.wf, w.ws, temporal_permuted=1, rounding=rnd)
+        with bss.build_tile_map(p) as tm:
+            s0 = tm.stats(0)
+            ms = _time(torch, lambda: bss.sparse_attention(Q, K, V, O, tm, zeros))
+            fl_ = 4.0 * w.d * H * s0["retained_pairs"]
+            out[name] = {"ms": ms, "tflops": fl_ / ms / 1e9, "frac_of_peak": fl_ / ms / 1e9 / peaks["bf16_tflops"],
+                         "speedup_vs_dense": dense_ms / ms, "retained_fraction": s0["retained_pairs"] / w.N ** 2,
+                         "tiles": s0}
+    ones = torch.ones(H, dtype=torch.uint8, device=dev)
+    Qp, Kp, Vp, Op = (torch.empty_like(Q) for _ in range(4))
+    p1 = bss.MaskParams(w.F, w.Hs, w.Ws, w.d, w.wf, w.ws, temporal_permuted=1, rounding=0)
+    p0 = bss.MaskParams(w.F, w.Hs, w.Ws, w.d, w.wf, w.ws, temporal_permuted=0, rounding=0)
+    with bss.build_tile_map(p1) as tm1, bss.build_tile_map(p0) as tm0:
+        tp = tm1.stats(1)["retained_pairs"]
+        fl_ = 4.0 * w.d * H * tp
+
+        def with_perm():
+            bss.attention_step(Q, K, V, O, tm1, ones, Qp, Kp, Vp, Op)
+
+        ms_perm = _time(torch, with_perm)
+        ms_attn = _time(torch, lambda: bss.sparse_attention(Qp, Kp, Vp, Op, tm1, ones))
+        ms_noperm = _time(torch, lambda: bss.sparse_attention(Q, K, V, O, tm0, ones))
+        out["temporal_heads"] = {
+            "with_permutation_ms": ms_perm, "attention_only_ms": ms_attn, "in_kernel_indexing_ms": ms_noperm,
+            "tflops_attention": fl_ / ms_attn / 1e9, "tflops_in_kernel_indexing": fl_ / ms_noperm / 1e9,
+            "tiles_permuted": tm1.stats(1), "tiles_in_kernel_indexing": tm0.stats(1)}
+        perm_ms = _time(torch, lambda: bss.permute(Q, Qp, ones, p1, False))
+        nbytes = 2.0 * Q.numel() * 2
+        out["permute"] = {"ms": perm_ms, "gbs": nbytes / perm_ms / 1e6, "frac_of_hbm_peak":
+                          nbytes / perm_ms / 1e6 / peaks["hbm_gbs"]}
+    return out
+
+
+def e2e(bss, torch, params, tm, flags, Qd, Kd, Vd, flops, args):
+    """The same step through the public API from pinned host buffers: H2D of Q, K, V,
+    the path, D2H of O, all inside the timed region."""
+    H, N, d = Qd.shape
+    hq, hk, hv = (torch.empty(H, N, d, dtype=torch.bfloat16, pin_memory=True) for _ in range(3))
+    ho = torch.empty(H, N, d, dtype=torch.bfloat16, pin_memory=True)
+    for x, src in ((hq, Qd), (hk, Kd), (hv, Vd)):
+        x.copy_(src.cpu())
+    dev = Qd.device
+    Q, K, V, O = (torch.empty(H, N, d, dtype=torch.bfloat16, device=dev) for _ in range(4))
+    ws = [torch.empty_like(Q) for _ in range(4)]
+    fl_host = torch.tensor(flags, dtype=torch.uint8).pin_memory()
+    fl = torch.empty(H, dtype=torch.uint8, device=dev)
+
+    def one():
+        Q.copy_(hq, non_blocking=True)
+        K.copy_(hk, non_blocking=True)
+        V.copy_(hv, non_blocking=True)
+        fl.copy_(fl_host, non_blocking=True)
+        bss.attention_step(Q, K, V, O, tm, fl, *ws)
+        ho.copy_(O, non_blocking=True)
+
+    steps = max(3, min(args.steps, 10))
+    ms = _time(torch, one, reps=steps, warm=3)
+    return {"value": flops / (ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": ms,
+            "h2d_bytes_per_step": 3 * H * N * d * 2 + H, "d2h_bytes_per_step": H * N * d * 2}
+
+
+def cpu_baseline(w, Q, K, V, flags, args, flops):
+    import oracle
+    H = Q.shape[0]
+    q, k, v = (x.cpu() for x in (Q, K, V))
+    dt, nrows = oracle_sample(w, q, k, v, flags, args.cpu_rows_per_head, seed=2000)
+    rows_total = H * w.N
+    full_s = dt * rows_total / nrows
+    return {"value": flops / full_s / 1e12, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{args.cpu_rows_per_head} seeded query rows per head x {H} heads "
+                      f"({100.0 * nrows / rows_total:.2f}% of rows, {dt:.1f} s), time scaled to all rows",
+            "seconds_full_workload_extrapolated": full_s}
+
+
+if __name__ == "__main__":
+    main()
