@@ -38,11 +38,11 @@ constexpr int kBQ = 128;
 constexpr int kBKV = 128;
 constexpr int kThreads = 256;
 constexpr int kStages = 2;
-// TMEM columns: two S buffers, O, P (bf16 packed two per column)
+// TMEM columns: two S buffers, O, two P buffers (bf16 packed two per column)
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS0 = 0;
 constexpr uint32_t kColO = 256;
-constexpr uint32_t kColP = 384;
+constexpr uint32_t kColP = 384;  // P buffer b at kColP + 64 * b
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale when max grows by > 256x
 
 struct AttnArgs {
@@ -65,7 +65,7 @@ struct Smem {
     static constexpr uint32_t kK = kTile;
     static constexpr uint32_t kV = kTile * (1 + kStages);
     static constexpr uint32_t kBar = kTile * (1 + 2 * kStages);
-    static constexpr uint32_t kNumBars = 1 + 3 * kStages + 2 + 2 + 1 + 1 + 1;
+    static constexpr uint32_t kNumBars = 1 + 3 * kStages + 2 + 2 + 2 + 2 + 1;
     static constexpr uint32_t kBytes = kBar + kNumBars * 8 + 16;
     static constexpr uint32_t kAlloc = kBytes + 1024;  // slack for 1024-byte alignment
 };
@@ -172,9 +172,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     uint64_t* bar_kv_empty = bars + 1 + 2 * kStages;
     uint64_t* bar_s_full = bars + 1 + 3 * kStages;
     uint64_t* bar_s_free = bar_s_full + 2;
-    uint64_t* bar_p_full = bar_s_free + 2;
-    uint64_t* bar_o_done = bar_p_full + 1;
-    uint64_t* bar_mma_done = bar_o_done + 1;
+    uint64_t* bar_p_full = bar_s_free + 2;   // [2]: P of tile j in buffer j & 1
+    uint64_t* bar_o_done = bar_p_full + 2;   // [2]: PV of tile j committed to j & 1
+    uint64_t* bar_mma_done = bar_o_done + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_mma_done + 1);
 
     const int warp = threadIdx.x >> 5;
@@ -211,8 +211,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             mbar_init(bar_s_full + b, 1);
             mbar_init(bar_s_free + b, 128);
         }
-        mbar_init(bar_p_full, 128);
-        mbar_init(bar_o_done, 1);
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bar_p_full + b, 128);
+            mbar_init(bar_o_done + b, 1);
+        }
         mbar_init(bar_mma_done, 1);
         mbar_fence_init();
     }
@@ -293,16 +295,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                     const int jp = j - 1;
                     const int st = jp % kStages;
                     ok = mbar_wait(bar_v + st, (jp / kStages) & 1, status);
-                    if (ok) ok = mbar_wait(bar_p_full, jp & 1, status);
+                    if (ok) ok = mbar_wait(bar_p_full + (jp & 1), (jp >> 1) & 1, status);
                     if (!ok) break;
                     tc_fence_after();
                     const uint32_t v_base = smem_u32(sV + st * L::kTile);
 #pragma unroll
                     for (int kk = 0; kk < kBKV / 16; ++kk)
-                        umma_ts(tmem + kColO, tmem + kColP + kk * 8, desc_mnmajor_sw128(v_base, kk), idesc_pv,
-                                (jp > 0 || kk > 0) ? 1u : 0u);
+                        umma_ts(tmem + kColO, tmem + kColP + (jp & 1) * 64 + kk * 8, desc_mnmajor_sw128(v_base, kk),
+                                idesc_pv, (jp > 0 || kk > 0) ? 1u : 0u);
                     tc_commit(bar_kv_empty + st);
-                    tc_commit(bar_o_done);
+                    tc_commit(bar_o_done + (jp & 1));
                 }
             }
             tc_commit(bar_mma_done);
@@ -343,48 +345,62 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
 #pragma unroll
                 for (int i = 0; i < 128; ++i) x[i] = ((bits[i >> 5] >> (i & 31)) & 1u) ? x[i] : -INFINITY;
             }
-            float tmax = x[0];
+            // row max with 8 independent chains, then a tree
+            float mx[8];
 #pragma unroll
-            for (int i = 1; i < 128; ++i) tmax = fmaxf(tmax, x[i]);
+            for (int t = 0; t < 8; ++t) mx[t] = x[t];
+#pragma unroll
+            for (int i = 8; i < 128; ++i) mx[i & 7] = fmaxf(mx[i & 7], x[i]);
+            const float tmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                     fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
             const float tmax_s = tmax * c;
             const float m_new = (tmax_s > m + kRescaleThreshold) ? tmax_s : m;
             const float alpha = (m_new == m) ? 1.0f : ex2_approx(m - m_new);
             const float mref = (m_new == -INFINITY) ? 0.0f : m_new;
-            float sum = 0.0f;
+            float sm[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // 8 independent partial sums
             uint32_t pk[64];
 #pragma unroll
             for (int i = 0; i < 64; ++i) {
                 const float p0 = ex2_approx(fmaf(x[2 * i], c, -mref));
                 const float p1 = ex2_approx(fmaf(x[2 * i + 1], c, -mref));
-                sum += p0 + p1;
+                sm[(2 * i) & 7] += p0;
+                sm[(2 * i + 1) & 7] += p1;
                 pk[i] = pack_bf16x2(p0, p1);
             }
-            if (j >= 1) {
-                ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_o_done, (j - 1) & 1, status));
+            const float sum = ((sm[0] + sm[1]) + (sm[2] + sm[3])) + ((sm[4] + sm[5]) + (sm[6] + sm[7]));
+            // O is rescaled only when some row's reference max moved; that needs
+            // every earlier PV to have landed.
+            if (j >= 1 && __any_sync(0xFFFFFFFFu, alpha != 1.0f)) {
+                ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_o_done + ((j - 1) & 1), ((j - 1) >> 1) & 1, status));
                 if (!ok) break;
                 tc_fence_after();
-                if (__any_sync(0xFFFFFFFFu, alpha != 1.0f)) {
 #pragma unroll
-                    for (int cc = 0; cc < D / 32; ++cc) {
-                        uint32_t o[32];
-                        BSS_TMEM_LD32(tmem + lane_base + kColO + cc * 32, o);
-                        tmem_wait_ld();
+                for (int cc = 0; cc < D / 32; ++cc) {
+                    uint32_t o[32];
+                    BSS_TMEM_LD32(tmem + lane_base + kColO + cc * 32, o);
+                    tmem_wait_ld();
 #pragma unroll
-                        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                        BSS_TMEM_ST32(tmem + lane_base + kColO + cc * 32, o);
-                    }
+                    for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                    BSS_TMEM_ST32(tmem + lane_base + kColO + cc * 32, o);
                 }
+            }
+            // P buffer b was last read by the PV of tile j - 2
+            if (j >= 2) {
+                ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_o_done + b, ((j - 2) >> 1) & 1, status));
+                if (!ok) break;
+                tc_fence_after();
             }
             l = l * alpha + sum;
             m = m_new;
-            BSS_TMEM_ST32(tmem + lane_base + kColP + 0, (pk + 0));
-            BSS_TMEM_ST32(tmem + lane_base + kColP + 32, (pk + 32));
+            BSS_TMEM_ST32(tmem + lane_base + kColP + b * 64 + 0, (pk + 0));
+            BSS_TMEM_ST32(tmem + lane_base + kColP + b * 64 + 32, (pk + 32));
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(bar_p_full);
+            mbar_arrive(bar_p_full + b);
         }
         // ---- epilogue: O / l -> bf16 -> swizzled staging (reuses the Q tile) -> TMA store
-        if (ok && n > 0) ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_o_done, (n - 1) & 1, status));
+        if (ok && n > 0)
+            ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_o_done + ((n - 1) & 1), ((n - 1) >> 1) & 1, status));
         if (ok) {
             tc_fence_after();
             const float inv_l = l > 0.0f ? 1.0f / l : 0.0f;
