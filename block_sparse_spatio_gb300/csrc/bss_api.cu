@@ -269,9 +269,9 @@ bss_status bss_sparse_attention(const void* Q, const void* K, const void* V, voi
     if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
         return set_error(BSS_ERR_INVALID_ARG, "tensors must be 16-byte aligned");
     if (H <= 0) return set_error(BSS_ERR_INVALID_ARG, "H must be positive");
-    if (map->BQ != 128 || map->BKV != 128)
-        return set_error(BSS_ERR_UNSUPPORTED, "attention needs a map built with BQ = BKV = 128 (got %d x %d)", map->BQ,
-                         map->BKV);
+    if (map->BQ != attention_block_q() || map->BKV != attention_block_kv())
+        return set_error(BSS_ERR_UNSUPPORTED, "attention needs a map built with BQ = %d, BKV = %d (got %d x %d)",
+                         attention_block_q(), attention_block_kv(), map->BQ, map->BKV);
     if (!std::isfinite(softmax_scale)) return set_error(BSS_ERR_INVALID_ARG, "softmax_scale is not finite");
     int dev = 0;
     cudaGetDevice(&dev);
@@ -330,7 +330,7 @@ bss_status bss_dense_attention(const void* Q, const void* K, const void* V, void
     a.S = N;
     a.S_pad = N;
     a.dense = 1;
-    a.nq = (N + 127) / 128;
+    a.nq = (N + attention_block_q() - 1) / attention_block_q();
     a.code[0] = a.code[1] = MASK_DENSE;
     a.softmax_scale = softmax_scale;
     return launch_attention(a, stream);

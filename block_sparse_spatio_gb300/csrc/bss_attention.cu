@@ -9,24 +9,34 @@
 // mask"), or only the padding predicate on padding tiles of a tile-aligned
 // mask (section "Align the sparse mask with final execution").
 //
-// GB300 design (one CTA per (head, 128-row q tile), 256 threads):
-//   warp 0      TMA producer: Q once, then K and V tiles of the list into a
-//               KV_STAGES-deep ring (128-byte swizzled, 64-column boxes).
-//   warp 1      TMEM allocator and single-thread tcgen05.mma issuer:
-//               S_j = Q K_j^T into one of two TMEM S buffers, then
-//               O += P_{j-1} V_{j-1} with P read from TMEM.
-//   warps 4..7  softmax: one thread per query row (= TMEM lane).  Reads S,
-//               masks boundary / padding tiles, keeps the running max with a
-//               lazy rescale (O and l are rescaled only when the max grows by
-//               more than 2^8), writes bf16 P to TMEM, and finally normalises O
-//               and stores it with a TMA store; LSE is written directly.
-// Every mbarrier wait is bounded; on a timeout the status word is set and all
-// roles unwind to a common exit that frees TMEM.
+// GB300 design.  One CTA per (head, 256-row q tile), 384 threads.  The q tile
+// is two 128-row halves that share every K/V tile brought into shared memory,
+// which halves the L2 -> SM traffic per FLOP compared with 128-row tiles (at
+// 128 rows the kernel ran at the L2 bandwidth limit).
+//   warp 0       TMA producer: Q (both halves) once, then K and V tiles of the
+//                list into separate KV_STAGES-deep rings (128-byte swizzled,
+//                64-column boxes).
+//   warp 1       TMEM allocator and single-thread tcgen05.mma issuer.
+//                TMEM: S_h (128 fp32 columns) and O_h (D columns) per half h;
+//                the bf16 P_h is written over the first 64 columns of S_h.
+//                Issue order  S_1(j) PV_0(j) S_0(j+1) PV_1(j) S_1(j+1) ...
+//                gives each half's softmax one full MMA tile of time.
+//   warps 4..7   softmax of half 0, warps 8..11 softmax of half 1: one thread
+//                per query row (= TMEM lane).  Reads S, masks boundary /
+//                padding tiles, keeps the running max with a lazy rescale (O
+//                and l are rescaled only when the max grows by more than 2^8),
+//                writes bf16 P to TMEM; finally normalises O, stores it with a
+//                TMA store and writes the LSE.
+// tcgen05.mma operations issued by one thread execute in issue order, so an S
+// that overwrites P_h is issued after the PV that reads it.  Every mbarrier
+// wait is bounded; on a timeout the status word is set and all roles unwind to
+// a common exit that frees TMEM.
 #include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <cmath>
 #include <cstdint>
+#include <cstring>
 
 #include "bss_internal.h"
 #include "bss_ptx.cuh"
@@ -34,15 +44,14 @@
 namespace bss {
 namespace {
 
-constexpr int kBQ = 128;
-constexpr int kBKV = 128;
-constexpr int kThreads = 256;
+constexpr int kBQ = 256;        // query rows per CTA (two halves of 128)
+constexpr int kHalf = 128;      // rows per half = MMA M
+constexpr int kBKV = 128;       // key columns per tile = MMA N of S
+constexpr int kThreads = 384;
 constexpr int kStages = 2;
-// TMEM columns: two S buffers, O, two P buffers (bf16 packed two per column)
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kColS0 = 0;
-constexpr uint32_t kColO = 256;
-constexpr uint32_t kColP = 384;  // P buffer b at kColP + 64 * b
+constexpr uint32_t kColS = 0;    // S_h at kColS + 128 h (P_h over its first 64 columns)
+constexpr uint32_t kColO = 256;  // O_h at kColO + 128 h
 constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale when max grows by > 256x
 
 struct AttnArgs {
@@ -60,12 +69,13 @@ struct AttnArgs {
 
 template <int D>
 struct Smem {
-    static constexpr uint32_t kTile = kBQ * D * 2;  // bytes of one 128-row bf16 tile
-    static constexpr uint32_t kQ = 0;
-    static constexpr uint32_t kK = kTile;
-    static constexpr uint32_t kV = kTile * (1 + kStages);
-    static constexpr uint32_t kBar = kTile * (1 + 2 * kStages);
-    static constexpr uint32_t kNumBars = 1 + 3 * kStages + 2 + 2 + 2 + 2 + 1;
+    static constexpr uint32_t kTile = kHalf * D * 2;  // bytes of one 128-row bf16 tile
+    static constexpr uint32_t kQ = 0;                 // two halves
+    static constexpr uint32_t kK = 2 * kTile;
+    static constexpr uint32_t kV = kK + kStages * kTile;
+    static constexpr uint32_t kBar = kV + kStages * kTile;
+    // q, k_full[S], v_full[S], k_empty[S], v_empty[S], s_full[2], p_full[2], o_done[2], mma_done
+    static constexpr uint32_t kNumBars = 1 + 4 * kStages + 2 + 2 + 2 + 1;
     static constexpr uint32_t kBytes = kBar + kNumBars * 8 + 16;
     static constexpr uint32_t kAlloc = kBytes + 1024;  // slack for 1024-byte alignment
 };
@@ -157,8 +167,7 @@ __device__ __forceinline__ uint32_t entry_at(const AttnArgs& a, const int32_t* e
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_constant__ AttnArgs args) {
     using L = Smem<D>;
-    constexpr int kChunks = D / 64;          // 64-column (128-byte) swizzle atoms per row
-    constexpr uint32_t kChunkBytes = kBQ * 128;  // one 64-column box of 128 rows
+    constexpr int kChunks = D / 64;  // 64-column (128-byte) swizzle atoms per row
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -167,13 +176,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     uint8_t* sV = smem + L::kV;
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + L::kBar);
     uint64_t* bar_q = bars;
-    uint64_t* bar_k = bars + 1;
-    uint64_t* bar_v = bars + 1 + kStages;
-    uint64_t* bar_kv_empty = bars + 1 + 2 * kStages;
-    uint64_t* bar_s_full = bars + 1 + 3 * kStages;
-    uint64_t* bar_s_free = bar_s_full + 2;
-    uint64_t* bar_p_full = bar_s_free + 2;   // [2]: P of tile j in buffer j & 1
-    uint64_t* bar_o_done = bar_p_full + 2;   // [2]: PV of tile j committed to j & 1
+    uint64_t* bar_k_full = bars + 1;
+    uint64_t* bar_v_full = bar_k_full + kStages;
+    uint64_t* bar_k_empty = bar_v_full + kStages;
+    uint64_t* bar_v_empty = bar_k_empty + kStages;
+    uint64_t* bar_s_full = bar_v_empty + kStages;  // [2] per half
+    uint64_t* bar_p_full = bar_s_full + 2;         // [2] per half
+    uint64_t* bar_o_done = bar_p_full + 2;         // [2] per half
     uint64_t* bar_mma_done = bar_o_done + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_mma_done + 1);
 
@@ -203,15 +212,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     if (threadIdx.x == 0) {
         mbar_init(bar_q, 1);
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(bar_k + s, 1);
-            mbar_init(bar_v + s, 1);
-            mbar_init(bar_kv_empty + s, 1);
+            mbar_init(bar_k_full + s, 1);
+            mbar_init(bar_v_full + s, 1);
+            mbar_init(bar_k_empty + s, 1);
+            mbar_init(bar_v_empty + s, 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar_s_full + b, 1);
-            mbar_init(bar_s_free + b, 128);
-        }
-        for (int b = 0; b < 2; ++b) {
             mbar_init(bar_p_full + b, 128);
             mbar_init(bar_o_done + b, 1);
         }
@@ -230,16 +237,18 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             tma_prefetch_desc(&args.tm_q);
             tma_prefetch_desc(&args.tm_k);
             tma_prefetch_desc(&args.tm_v);
-            mbar_arrive_expect_tx(bar_q, L::kTile);
+            mbar_arrive_expect_tx(bar_q, 2 * L::kTile);
 #pragma unroll
-            for (int c = 0; c < kChunks; ++c) tma_load_3d(sQ + c * kChunkBytes, &args.tm_q, c * 64, qt * kBQ, h, bar_q);
+            for (int hh = 0; hh < 2; ++hh)
+#pragma unroll
+                for (int c = 0; c < kChunks; ++c)
+                    tma_load_3d(sQ + hh * L::kTile + c * kChunkBytesSw128, &args.tm_q, c * 64, qt * kBQ + hh * kHalf,
+                                h, bar_q);
             bool ok = true;
-            int j = 0;
-            for (; j < n; ++j) {
-                const int st = j % kStages;
-                if (j >= kStages) ok = mbar_wait(bar_kv_empty + st, ((j / kStages) - 1) & 1, status);
-                if (!ok) break;
-                const uint32_t e = entry_at(args, ents, j);
+            int jk = 0, jv = 0;  // K tiles and V tiles issued
+            for (; jv < n; ++jv) {
+                const int st = jv % kStages;
+                const uint32_t e = entry_at(args, ents, jv);
                 const int col0 = static_cast<int>(e & BSS_TILE_INDEX_MASK) * kBKV;
                 const CUtensorMap* mk = &args.tm_k;
                 const CUtensorMap* mv = &args.tm_v;
@@ -252,155 +261,185 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                         row = col0 - args.S_pad;
                     }
                 }
-                mbar_arrive_expect_tx(bar_k + st, L::kTile);
+                if (jv >= kStages) ok = mbar_wait(bar_k_empty + st, ((jv / kStages) - 1) & 1, status);
+                if (!ok) break;
+                mbar_arrive_expect_tx(bar_k_full + st, L::kTile);
 #pragma unroll
                 for (int c = 0; c < kChunks; ++c)
-                    tma_load_3d(sK + st * L::kTile + c * kChunkBytes, mk, c * 64, row, h, bar_k + st);
-                mbar_arrive_expect_tx(bar_v + st, L::kTile);
+                    tma_load_3d(sK + st * L::kTile + c * kChunkBytesSw128, mk, c * 64, row, h, bar_k_full + st);
+                jk = jv + 1;
+                if (jv >= kStages) ok = mbar_wait(bar_v_empty + st, ((jv / kStages) - 1) & 1, status);
+                if (!ok) break;
+                mbar_arrive_expect_tx(bar_v_full + st, L::kTile);
 #pragma unroll
                 for (int c = 0; c < kChunks; ++c)
-                    tma_load_3d(sV + st * L::kTile + c * kChunkBytes, mv, c * 64, row, h, bar_v + st);
+                    tma_load_3d(sV + st * L::kTile + c * kChunkBytesSw128, mv, c * 64, row, h, bar_v_full + st);
             }
             // drain: no copy may still be landing in shared memory at exit
             mbar_wait(bar_q, 0, status);
-            for (int jj = (j - kStages > 0 ? j - kStages : 0); jj < j; ++jj) {
-                const int st = jj % kStages;
-                mbar_wait(bar_k + st, (jj / kStages) & 1, status);
-                mbar_wait(bar_v + st, (jj / kStages) & 1, status);
-            }
+            for (int jj = (jk - kStages > 0 ? jk - kStages : 0); jj < jk; ++jj)
+                mbar_wait(bar_k_full + jj % kStages, (jj / kStages) & 1, status);
+            for (int jj = (jv - kStages > 0 ? jv - kStages : 0); jj < jv; ++jj)
+                mbar_wait(bar_v_full + jj % kStages, (jj / kStages) & 1, status);
         }
     } else if (warp == 1) {
         // =========================== MMA issuer (one thread)
-        if (lane == 0) {
-            constexpr uint32_t idesc_qk = idesc_bf16_f32(kBQ, kBKV, 0);
-            constexpr uint32_t idesc_pv = idesc_bf16_f32(kBQ, D, 1);
-            bool ok = n > 0 ? mbar_wait(bar_q, 0, status) : true;
-            const uint32_t q_base = smem_u32(sQ);
-            for (int j = 0; ok && j <= n; ++j) {
-                if (j < n) {
-                    const int st = j % kStages;
-                    const int b = j & 1;
-                    ok = mbar_wait(bar_k + st, (j / kStages) & 1, status);
-                    if (ok && j >= 2) ok = mbar_wait(bar_s_free + b, ((j >> 1) - 1) & 1, status);
+        if (lane == 0 && n > 0) {
+            constexpr uint32_t idesc_qk = idesc_bf16_f32(kHalf, kBKV, 0);
+            constexpr uint32_t idesc_pv = idesc_bf16_f32(kHalf, D, 1);
+            const uint32_t q_base0 = smem_u32(sQ);
+            const uint32_t q_base1 = smem_u32(sQ + L::kTile);
+            bool ok = mbar_wait(bar_q, 0, status);
+            if (ok) ok = mbar_wait(bar_k_full, 0, status);
+            if (ok) {
+                tc_fence_after();
+                const uint32_t k_base = smem_u32(sK);
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    umma_ss(tmem + kColS, desc_kmajor_sw128(q_base0, kk), desc_kmajor_sw128(k_base, kk), idesc_qk,
+                            kk > 0 ? 1u : 0u);
+                tc_commit(bar_s_full + 0);
+            }
+            for (int j = 0; ok && j < n; ++j) {
+                const int st = j % kStages;
+                const uint32_t k_base = smem_u32(sK + st * L::kTile);
+                const uint32_t v_base = smem_u32(sV + st * L::kTile);
+                // S_1(j): K_j is resident (waited before S_0(j))
+#pragma unroll
+                for (int kk = 0; kk < D / 16; ++kk)
+                    umma_ss(tmem + kColS + 128, desc_kmajor_sw128(q_base1, kk), desc_kmajor_sw128(k_base, kk),
+                            idesc_qk, kk > 0 ? 1u : 0u);
+                tc_commit(bar_s_full + 1);
+                tc_commit(bar_k_empty + st);  // K_j is free once S_0(j) and S_1(j) complete
+                // PV_0(j)
+                ok = mbar_wait(bar_v_full + st, (j / kStages) & 1, status);
+                if (ok) ok = mbar_wait(bar_p_full + 0, j & 1, status);
+                if (!ok) break;
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < kBKV / 16; ++kk)
+                    umma_ts(tmem + kColO, tmem + kColS + kk * 8, desc_mnmajor_sw128(v_base, kk), idesc_pv,
+                            (j > 0 || kk > 0) ? 1u : 0u);
+                tc_commit(bar_o_done + 0);
+                // S_0(j+1)
+                if (j + 1 < n) {
+                    const int st1 = (j + 1) % kStages;
+                    ok = mbar_wait(bar_k_full + st1, ((j + 1) / kStages) & 1, status);
                     if (!ok) break;
                     tc_fence_after();
-                    const uint32_t k_base = smem_u32(sK + st * L::kTile);
+                    const uint32_t k1 = smem_u32(sK + st1 * L::kTile);
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk)
-                        umma_ss(tmem + kColS0 + b * kBKV, desc_kmajor_sw128(q_base, kk),
-                                desc_kmajor_sw128(k_base, kk), idesc_qk, kk > 0 ? 1u : 0u);
-                    tc_commit(bar_s_full + b);
+                        umma_ss(tmem + kColS, desc_kmajor_sw128(q_base0, kk), desc_kmajor_sw128(k1, kk), idesc_qk,
+                                kk > 0 ? 1u : 0u);
+                    tc_commit(bar_s_full + 0);
                 }
-                if (j >= 1) {
-                    const int jp = j - 1;
-                    const int st = jp % kStages;
-                    ok = mbar_wait(bar_v + st, (jp / kStages) & 1, status);
-                    if (ok) ok = mbar_wait(bar_p_full + (jp & 1), (jp >> 1) & 1, status);
-                    if (!ok) break;
-                    tc_fence_after();
-                    const uint32_t v_base = smem_u32(sV + st * L::kTile);
+                // PV_1(j)
+                ok = mbar_wait(bar_p_full + 1, j & 1, status);
+                if (!ok) break;
+                tc_fence_after();
 #pragma unroll
-                    for (int kk = 0; kk < kBKV / 16; ++kk)
-                        umma_ts(tmem + kColO, tmem + kColP + (jp & 1) * 64 + kk * 8, desc_mnmajor_sw128(v_base, kk),
-                                idesc_pv, (jp > 0 || kk > 0) ? 1u : 0u);
-                    tc_commit(bar_kv_empty + st);
-                    tc_commit(bar_o_done + (jp & 1));
-                }
+                for (int kk = 0; kk < kBKV / 16; ++kk)
+                    umma_ts(tmem + kColO + 128, tmem + kColS + 128 + kk * 8, desc_mnmajor_sw128(v_base, kk),
+                            idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
+                tc_commit(bar_o_done + 1);
+                tc_commit(bar_v_empty + st);
             }
             tc_commit(bar_mma_done);
             mbar_wait(bar_mma_done, 0, status);
         }
     } else if (warp >= 4) {
         // =========================== softmax + epilogue (one thread per row)
-        const int r = threadIdx.x - 128;
+        const int hf = (warp - 4) >> 2;  // half
+        const int r = threadIdx.x - 128 - hf * 128;
         const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-        const int q = qt * kBQ + r;
+        const uint32_t t_s = tmem + lane_base + kColS + hf * 128;
+        const uint32_t t_o = tmem + lane_base + kColO + hf * 128;
+        const int q = qt * kBQ + hf * kHalf + r;
         const RowPred rp = row_pred(args, code, q);
         const float c = args.scale_log2;
         float m = -INFINITY;
         float l = 0.0f;
         bool ok = true;
         for (int j = 0; j < n; ++j) {
-            const int b = j & 1;
             const uint32_t e = entry_at(args, ents, j);
             const int cls = static_cast<int>(e >> BSS_CLASS_SHIFT);
             const int c0 = static_cast<int>(e & BSS_TILE_INDEX_MASK) * kBKV;
-            ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_s_full + b, (j >> 1) & 1, status));
+            ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_s_full + hf, j & 1, status));
             if (!ok) break;
             tc_fence_after();
-            uint32_t sr[128];
-            BSS_TMEM_LD32(tmem + lane_base + kColS0 + b * kBKV + 0, (sr + 0));
-            BSS_TMEM_LD32(tmem + lane_base + kColS0 + b * kBKV + 32, (sr + 32));
-            BSS_TMEM_LD32(tmem + lane_base + kColS0 + b * kBKV + 64, (sr + 64));
-            BSS_TMEM_LD32(tmem + lane_base + kColS0 + b * kBKV + 96, (sr + 96));
-            tmem_wait_ld();
-            tc_fence_before();
-            mbar_arrive(bar_s_free + b);
-            float x[128];
-#pragma unroll
-            for (int i = 0; i < 128; ++i) x[i] = __uint_as_float(sr[i]);
-            if (cls != BSS_CLASS_FULL) {
-                uint32_t bits[4];
-                tile_bits(bits, args, code, cls, c0, rp);
-#pragma unroll
-                for (int i = 0; i < 128; ++i) x[i] = ((bits[i >> 5] >> (i & 31)) & 1u) ? x[i] : -INFINITY;
-            }
-            // row max with 8 independent chains, then a tree
+            uint32_t bits[4] = {0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu};
+            if (cls != BSS_CLASS_FULL) tile_bits(bits, args, code, cls, c0, rp);
+            // pass 1: row max over the 128 S columns, 64 at a time, 8 independent chains
             float mx[8];
 #pragma unroll
-            for (int t = 0; t < 8; ++t) mx[t] = x[t];
+            for (int t = 0; t < 8; ++t) mx[t] = -INFINITY;
 #pragma unroll
-            for (int i = 8; i < 128; ++i) mx[i & 7] = fmaxf(mx[i & 7], x[i]);
+            for (int g = 0; g < 2; ++g) {
+                uint32_t sr[64];
+                BSS_TMEM_LD32(t_s + 64 * g, (sr + 0));
+                BSS_TMEM_LD32(t_s + 64 * g + 32, (sr + 32));
+                tmem_wait_ld();
+#pragma unroll
+                for (int i = 0; i < 64; ++i) {
+                    const float v = ((bits[2 * g + (i >> 5)] >> (i & 31)) & 1u) ? __uint_as_float(sr[i]) : -INFINITY;
+                    mx[i & 7] = fmaxf(mx[i & 7], v);
+                }
+            }
             const float tmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
                                      fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
             const float tmax_s = tmax * c;
             const float m_new = (tmax_s > m + kRescaleThreshold) ? tmax_s : m;
             const float alpha = (m_new == m) ? 1.0f : ex2_approx(m - m_new);
             const float mref = (m_new == -INFINITY) ? 0.0f : m_new;
-            float sm[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};  // 8 independent partial sums
-            uint32_t pk[64];
-#pragma unroll
-            for (int i = 0; i < 64; ++i) {
-                const float p0 = ex2_approx(fmaf(x[2 * i], c, -mref));
-                const float p1 = ex2_approx(fmaf(x[2 * i + 1], c, -mref));
-                sm[(2 * i) & 7] += p0;
-                sm[(2 * i + 1) & 7] += p1;
-                pk[i] = pack_bf16x2(p0, p1);
-            }
-            const float sum = ((sm[0] + sm[1]) + (sm[2] + sm[3])) + ((sm[4] + sm[5]) + (sm[6] + sm[7]));
-            // O is rescaled only when some row's reference max moved; that needs
-            // every earlier PV to have landed.
+            // O_h is rescaled only when some row's reference max moved.  PV_h(j-1)
+            // was issued before S_h(j), so it has completed; the wait only orders.
             if (j >= 1 && __any_sync(0xFFFFFFFFu, alpha != 1.0f)) {
-                ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_o_done + ((j - 1) & 1), ((j - 1) >> 1) & 1, status));
+                ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_o_done + hf, (j - 1) & 1, status));
                 if (!ok) break;
                 tc_fence_after();
-#pragma unroll
+#pragma unroll 1
                 for (int cc = 0; cc < D / 32; ++cc) {
                     uint32_t o[32];
-                    BSS_TMEM_LD32(tmem + lane_base + kColO + cc * 32, o);
+                    BSS_TMEM_LD32(t_o + cc * 32, o);
                     tmem_wait_ld();
 #pragma unroll
                     for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                    BSS_TMEM_ST32(tmem + lane_base + kColO + cc * 32, o);
+                    BSS_TMEM_ST32(t_o + cc * 32, o);
                 }
             }
-            // P buffer b was last read by the PV of tile j - 2
-            if (j >= 2) {
-                ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_o_done + b, ((j - 2) >> 1) & 1, status));
-                if (!ok) break;
-                tc_fence_after();
+            // pass 2: P = exp2(s * scale * log2 e - m) as bf16 pairs, written over the
+            // first 64 S columns; 32-column chunk cc lands in columns [16cc, 16cc+16),
+            // which chunks <= cc have already been read from.
+            float sm[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int cc = 0; cc < 4; ++cc) {
+                uint32_t sr[32];
+                BSS_TMEM_LD32(t_s + 32 * cc, sr);
+                tmem_wait_ld();
+                uint32_t pk[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const float x0 = ((bits[cc] >> (2 * i)) & 1u) ? __uint_as_float(sr[2 * i]) : -INFINITY;
+                    const float x1 = ((bits[cc] >> (2 * i + 1)) & 1u) ? __uint_as_float(sr[2 * i + 1]) : -INFINITY;
+                    const float p0 = ex2_approx(fmaf(x0, c, -mref));
+                    const float p1 = ex2_approx(fmaf(x1, c, -mref));
+                    sm[(2 * i) & 7] += p0;
+                    sm[(2 * i + 1) & 7] += p1;
+                    pk[i] = pack_bf16x2(p0, p1);
+                }
+                BSS_TMEM_ST16(t_s + 16 * cc, pk);
             }
+            const float sum = ((sm[0] + sm[1]) + (sm[2] + sm[3])) + ((sm[4] + sm[5]) + (sm[6] + sm[7]));
             l = l * alpha + sum;
             m = m_new;
-            BSS_TMEM_ST32(tmem + lane_base + kColP + b * 64 + 0, (pk + 0));
-            BSS_TMEM_ST32(tmem + lane_base + kColP + b * 64 + 32, (pk + 32));
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(bar_p_full + b);
+            mbar_arrive(bar_p_full + hf);
         }
-        // ---- epilogue: O / l -> bf16 -> swizzled staging (reuses the Q tile) -> TMA store
-        if (ok && n > 0)
-            ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_o_done + ((n - 1) & 1), ((n - 1) >> 1) & 1, status));
+        // ---- epilogue: O / l -> bf16 -> swizzled staging (reuses this half's Q) -> TMA store
+        uint8_t* stage = sQ + hf * L::kTile;
+        if (ok && n > 0) ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_o_done + hf, (n - 1) & 1, status));
         if (ok) {
             tc_fence_after();
             const float inv_l = l > 0.0f ? 1.0f / l : 0.0f;
@@ -408,7 +447,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             for (int cc = 0; cc < D / 32; ++cc) {
                 uint32_t o[32];
                 if (n > 0) {
-                    BSS_TMEM_LD32(tmem + lane_base + kColO + cc * 32, o);
+                    BSS_TMEM_LD32(t_o + cc * 32, o);
                     tmem_wait_ld();
                 } else {
 #pragma unroll
@@ -419,12 +458,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                 for (int i = 0; i < 16; ++i)
                     w[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
                 // columns [32cc, 32cc+32) = 16-byte units 4*(cc%2) .. +3 of 64-column chunk cc/2
-                uint8_t* chunk = sQ + (cc >> 1) * kChunkBytes + r * 128;
+                uint8_t* chunk = stage + (cc >> 1) * kChunkBytesSw128 + r * 128;
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
                     const int unit = (cc & 1) * 4 + u;
-                    uint4 v = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
-                    *reinterpret_cast<uint4*>(chunk + ((unit ^ (r & 7)) << 4)) = v;
+                    *reinterpret_cast<uint4*>(chunk + ((unit ^ (r & 7)) << 4)) =
+                        make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
                 }
             }
             if (args.lse != nullptr && q < args.N) {
@@ -433,10 +472,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             }
             fence_proxy_async_smem();
         }
-        named_barrier_sync(1, 128);
-        if (r == 0 && ok) {
+        named_barrier_sync(1 + hf, 128);
+        const int row0 = qt * kBQ + hf * kHalf;
+        if (r == 0 && ok && row0 < args.N) {
 #pragma unroll
-            for (int cc = 0; cc < kChunks; ++cc) tma_store_3d(&args.tm_o, sQ + cc * kChunkBytes, cc * 64, qt * kBQ, h);
+            for (int cc = 0; cc < kChunks; ++cc)
+                tma_store_3d(&args.tm_o, stage + cc * kChunkBytesSw128, cc * 64, row0, h);
             tma_store_commit();
             tma_store_wait_read_all();
         }
@@ -458,10 +499,10 @@ bss_status launch_d(const AttnLaunch& a, cudaStream_t stream) {
     const uint64_t rs = static_cast<uint64_t>(a.d) * 2;
     const uint64_t hs = rs * static_cast<uint64_t>(a.N);
     bss_status st;
-    if ((st = encode_tmap_3d(&args.tm_q, a.Q, a.d, a.N, a.H, rs, hs, 64, kBQ)) != BSS_OK) return st;
+    if ((st = encode_tmap_3d(&args.tm_q, a.Q, a.d, a.N, a.H, rs, hs, 64, kHalf)) != BSS_OK) return st;
     if ((st = encode_tmap_3d(&args.tm_k, a.K, a.d, a.N, a.H, rs, hs, 64, kBKV)) != BSS_OK) return st;
     if ((st = encode_tmap_3d(&args.tm_v, a.V, a.d, a.N, a.H, rs, hs, 64, kBKV)) != BSS_OK) return st;
-    if ((st = encode_tmap_3d(&args.tm_o, a.O, a.d, a.N, a.H, rs, hs, 64, kBQ)) != BSS_OK) return st;
+    if ((st = encode_tmap_3d(&args.tm_o, a.O, a.d, a.N, a.H, rs, hs, 64, kHalf)) != BSS_OK) return st;
     // frame-0 keys of a (H,W,F)-permuted head: row s of this view is permuted row s*F
     if ((st = encode_tmap_3d(&args.tm_ks, a.K, a.d, a.S, a.H, rs * a.F, hs, 64, kBKV)) != BSS_OK) return st;
     if ((st = encode_tmap_3d(&args.tm_vs, a.V, a.d, a.S, a.H, rs * a.F, hs, 64, kBKV)) != BSS_OK) return st;
@@ -500,6 +541,9 @@ bss_status launch_d(const AttnLaunch& a, cudaStream_t stream) {
 }
 
 }  // namespace
+
+int attention_block_q() { return kBQ; }
+int attention_block_kv() { return kBKV; }
 
 bss_status launch_attention(const AttnLaunch& a, cudaStream_t stream) {
     if (a.d == 128) return launch_d<128>(a, stream);

@@ -59,6 +59,8 @@ struct AttnLaunch {
     float softmax_scale;
 };
 bss_status launch_attention(const AttnLaunch& a, cudaStream_t stream);
+int attention_block_q();   // query rows per attention tile (the map's BQ)
+int attention_block_kv();  // key columns per attention tile (the map's BKV)
 
 // helpers (bss_api.cu)
 bss_status set_error(bss_status st, const char* fmt, ...);

@@ -56,10 +56,13 @@ def run_gpu(bss, q, k, v, flags, params, want_lse=True, dense=False):
 
 
 def oracle_rows(q, k, v, h, kind, g, rows, rounding, dense=False):
+    """Oracle rows; a rounded mask is rounded on the attention kernel's tile grid."""
+    import block_sparse_spatio_gb300 as bss
     b = W.bf16_bits
     if dense:
         kind = oracle.DENSE
-    return oracle.attention(b(q[h]), b(k[h]), b(v[h]), kind, g, rows=rows, rounding=bool(rounding))
+    return oracle.attention(b(q[h]), b(k[h]), b(v[h]), kind, g, rows=rows, rounding=bool(rounding),
+                            BQ=bss.ATTN_BQ, BKV=bss.ATTN_BKV)
 
 
 def compare(out_rows: np.ndarray, lse_rows, Oref: np.ndarray, lref: np.ndarray, what: str):

@@ -129,7 +129,7 @@ def _full_size(bss, wl, tperm, rounding, heads, nrows):
         kind = oracle_kind(flags[h], tperm)
         qh, kh, vh = (x[h].cpu() for x in (Q, K, V))
         Oref, lref = oracle.attention(W.bf16_bits(qh), W.bf16_bits(kh), W.bf16_bits(vh), kind, g, rows=rows,
-                                      rounding=bool(rounding))
+                                      rounding=bool(rounding), BQ=bss.ATTN_BQ, BKV=bss.ATTN_BKV)
         lrow = lse[h].cpu()
         if flags[h] and tperm:
             lrow = lrow[[(r % wl.S) * wl.F + r // wl.S for r in rows]]

@@ -81,7 +81,7 @@ def test_tile_map_full_size_sampled(bss, wl, tperm):
     g = oracle.Geometry(wl.F, wl.Hs, wl.Ws, wf=wl.wf, ws=wl.ws, bkv=128)
     for rounding in (0, 1):
         p = bss.MaskParams(wl.F, wl.Hs, wl.Ws, wl.d, wl.wf, wl.ws, temporal_permuted=tperm, rounding=rounding)
-        with bss.build_tile_map(p) as tm:
+        with bss.build_tile_map(p, 128, 128) as tm:
             nq = tm.dims(0)[0]
             qts = sorted({0, 1, nq // 3, nq // 2, nq - 2, nq - 1})
             st0 = check_map(bss, tm, oracle.SPATIAL, g, 128, 128, rounding, qts)
