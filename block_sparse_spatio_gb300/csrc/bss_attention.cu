@@ -312,8 +312,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                 tc_commit(bar_s_full + 1);
                 tc_commit(bar_k_empty + st);  // K_j is free once S_0(j) and S_1(j) complete
                 // PV_0(j)
-                ok = mbar_wait(bar_v_full + st, (j / kStages) & 1, status);
-                if (ok) ok = mbar_wait(bar_p_full + 0, j & 1, status);
+                ok = mbar_wait_spin(bar_v_full + st, (j / kStages) & 1, status);
+                if (ok) ok = mbar_wait_spin(bar_p_full + 0, j & 1, status);
                 if (!ok) break;
                 tc_fence_after();
 #pragma unroll
@@ -324,7 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                 // S_0(j+1)
                 if (j + 1 < n) {
                     const int st1 = (j + 1) % kStages;
-                    ok = mbar_wait(bar_k_full + st1, ((j + 1) / kStages) & 1, status);
+                    ok = mbar_wait_spin(bar_k_full + st1, ((j + 1) / kStages) & 1, status);
                     if (!ok) break;
                     tc_fence_after();
                     const uint32_t k1 = smem_u32(sK + st1 * L::kTile);
@@ -335,7 +335,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                     tc_commit(bar_s_full + 0);
                 }
                 // PV_1(j)
-                ok = mbar_wait(bar_p_full + 1, j & 1, status);
+                ok = mbar_wait_spin(bar_p_full + 1, j & 1, status);
                 if (!ok) break;
                 tc_fence_after();
 #pragma unroll
@@ -368,71 +368,122 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_s_full + hf, j & 1, status));
             if (!ok) break;
             tc_fence_after();
-            uint32_t bits[4] = {0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu};
-            if (cls != BSS_CLASS_FULL) tile_bits(bits, args, code, cls, c0, rp);
-            // pass 1: row max over the 128 S columns, 64 at a time, 8 independent chains
-            float mx[8];
+            // ---- fast path: a FULL tile, every row of the warp already has a finite
+            // reference max.  One pass: exponentiate against the current reference
+            // while tracking the tile max; the result is kept unless some row's max
+            // grew by more than 2^8 (then the tile is redone on the general path).
+            bool done = false;
+            if (cls == BSS_CLASS_FULL && __all_sync(0xFFFFFFFFu, m != -INFINITY)) {
+                uint32_t pk[64];
+                float cm0 = -INFINITY, cm1 = -INFINITY;
+                uint64_t s2a = 0ull, s2b = 0ull;  // packed partial sums (two chains)
+                const uint64_t c2 = f2_pack(c, c);
+                const uint64_t nm2 = f2_pack(-m, -m);
 #pragma unroll
-            for (int t = 0; t < 8; ++t) mx[t] = -INFINITY;
-#pragma unroll
-            for (int g = 0; g < 2; ++g) {
-                uint32_t sr[64];
-                BSS_TMEM_LD32(t_s + 64 * g, (sr + 0));
-                BSS_TMEM_LD32(t_s + 64 * g + 32, (sr + 32));
-                tmem_wait_ld();
-#pragma unroll
-                for (int i = 0; i < 64; ++i) {
-                    const float v = ((bits[2 * g + (i >> 5)] >> (i & 31)) & 1u) ? __uint_as_float(sr[i]) : -INFINITY;
-                    mx[i & 7] = fmaxf(mx[i & 7], v);
-                }
-            }
-            const float tmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                     fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-            const float tmax_s = tmax * c;
-            const float m_new = (tmax_s > m + kRescaleThreshold) ? tmax_s : m;
-            const float alpha = (m_new == m) ? 1.0f : ex2_approx(m - m_new);
-            const float mref = (m_new == -INFINITY) ? 0.0f : m_new;
-            // O_h is rescaled only when some row's reference max moved.  PV_h(j-1)
-            // was issued before S_h(j), so it has completed; the wait only orders.
-            if (j >= 1 && __any_sync(0xFFFFFFFFu, alpha != 1.0f)) {
-                ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_o_done + hf, (j - 1) & 1, status));
-                if (!ok) break;
-                tc_fence_after();
-#pragma unroll 1
-                for (int cc = 0; cc < D / 32; ++cc) {
-                    uint32_t o[32];
-                    BSS_TMEM_LD32(t_o + cc * 32, o);
+                for (int cc = 0; cc < 4; ++cc) {
+                    uint32_t sr[32];
+                    BSS_TMEM_LD32(t_s + 32 * cc, sr);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                    BSS_TMEM_ST32(t_o + cc * 32, o);
+                    for (int i = 0; i < 16; ++i) {
+                        const float x0 = __uint_as_float(sr[2 * i]), x1 = __uint_as_float(sr[2 * i + 1]);
+                        if (i & 1)
+                            cm1 = fmax3(cm1, x0, x1);
+                        else
+                            cm0 = fmax3(cm0, x0, x1);
+                        float y0, y1;
+                        f2_unpack(f2_fma(f2_pack(x0, x1), c2, nm2), y0, y1);
+                        const float p0 = ex2_approx(y0), p1 = ex2_approx(y1);
+                        const uint64_t pp = f2_pack(p0, p1);
+                        if (i & 1)
+                            s2b = f2_add(s2b, pp);
+                        else
+                            s2a = f2_add(s2a, pp);
+                        pk[16 * cc + i] = pack_bf16x2(p0, p1);
+                    }
+                }
+                const float tmax_s = fmaxf(cm0, cm1) * c;
+                if (!__any_sync(0xFFFFFFFFu, tmax_s > m + kRescaleThreshold)) {
+                    float a0, a1, b0, b1;
+                    f2_unpack(s2a, a0, a1);
+                    f2_unpack(s2b, b0, b1);
+                    l += (a0 + a1) + (b0 + b1);
+                    BSS_TMEM_ST32(t_s + 0, (pk + 0));
+                    BSS_TMEM_ST32(t_s + 32, (pk + 32));
+                    done = true;
                 }
             }
-            // pass 2: P = exp2(s * scale * log2 e - m) as bf16 pairs, written over the
-            // first 64 S columns; 32-column chunk cc lands in columns [16cc, 16cc+16),
-            // which chunks <= cc have already been read from.
-            float sm[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            if (!done) {
+                // ---- general path: masking (boundary / padding tiles), first tile of
+                // a row, or a reference max that must move.  Pass 1 finds the row max,
+                // pass 2 exponentiates and writes P chunk by chunk.
+                uint32_t bits[4] = {0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu};
+                if (cls != BSS_CLASS_FULL) tile_bits(bits, args, code, cls, c0, rp);
+                float mx[8];
 #pragma unroll
-            for (int cc = 0; cc < 4; ++cc) {
-                uint32_t sr[32];
-                BSS_TMEM_LD32(t_s + 32 * cc, sr);
-                tmem_wait_ld();
-                uint32_t pk[16];
+                for (int t = 0; t < 8; ++t) mx[t] = -INFINITY;
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    const float x0 = ((bits[cc] >> (2 * i)) & 1u) ? __uint_as_float(sr[2 * i]) : -INFINITY;
-                    const float x1 = ((bits[cc] >> (2 * i + 1)) & 1u) ? __uint_as_float(sr[2 * i + 1]) : -INFINITY;
-                    const float p0 = ex2_approx(fmaf(x0, c, -mref));
-                    const float p1 = ex2_approx(fmaf(x1, c, -mref));
-                    sm[(2 * i) & 7] += p0;
-                    sm[(2 * i + 1) & 7] += p1;
-                    pk[i] = pack_bf16x2(p0, p1);
+                for (int g = 0; g < 2; ++g) {
+                    uint32_t sr[64];
+                    BSS_TMEM_LD32(t_s + 64 * g, (sr + 0));
+                    BSS_TMEM_LD32(t_s + 64 * g + 32, (sr + 32));
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 64; ++i) {
+                        const float v =
+                            ((bits[2 * g + (i >> 5)] >> (i & 31)) & 1u) ? __uint_as_float(sr[i]) : -INFINITY;
+                        mx[i & 7] = fmaxf(mx[i & 7], v);
+                    }
                 }
-                BSS_TMEM_ST16(t_s + 16 * cc, pk);
+                const float tmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                         fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+                const float tmax_s = tmax * c;
+                const float m_new = (tmax_s > m + kRescaleThreshold) ? tmax_s : m;
+                const float alpha = (m_new == m) ? 1.0f : ex2_approx(m - m_new);
+                const float mref = (m_new == -INFINITY) ? 0.0f : m_new;
+                // O_h is rescaled only when some row's reference max moved.  PV_h(j-1)
+                // was issued before S_h(j), so it has completed; the wait only orders.
+                if (j >= 1 && __any_sync(0xFFFFFFFFu, alpha != 1.0f)) {
+                    ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_o_done + hf, (j - 1) & 1, status));
+                    if (!ok) break;
+                    tc_fence_after();
+#pragma unroll 1
+                    for (int cc = 0; cc < D / 32; ++cc) {
+                        uint32_t o[32];
+                        BSS_TMEM_LD32(t_o + cc * 32, o);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                        BSS_TMEM_ST32(t_o + cc * 32, o);
+                    }
+                }
+                // P = exp2(s * scale * log2 e - m) as bf16 pairs, written over the first
+                // 64 S columns; 32-column chunk cc lands in columns [16cc, 16cc+16),
+                // which chunks <= cc have already been read from.
+                float sm[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                    uint32_t sr[32];
+                    BSS_TMEM_LD32(t_s + 32 * cc, sr);
+                    tmem_wait_ld();
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const float x0 = ((bits[cc] >> (2 * i)) & 1u) ? __uint_as_float(sr[2 * i]) : -INFINITY;
+                        const float x1 =
+                            ((bits[cc] >> (2 * i + 1)) & 1u) ? __uint_as_float(sr[2 * i + 1]) : -INFINITY;
+                        const float p0 = ex2_approx(fmaf(x0, c, -mref));
+                        const float p1 = ex2_approx(fmaf(x1, c, -mref));
+                        sm[(2 * i) & 7] += p0;
+                        sm[(2 * i + 1) & 7] += p1;
+                        pk[i] = pack_bf16x2(p0, p1);
+                    }
+                    BSS_TMEM_ST16(t_s + 16 * cc, pk);
+                }
+                const float sum = ((sm[0] + sm[1]) + (sm[2] + sm[3])) + ((sm[4] + sm[5]) + (sm[6] + sm[7]));
+                l = l * alpha + sum;
+                m = m_new;
             }
-            const float sum = ((sm[0] + sm[1]) + (sm[2] + sm[3])) + ((sm[4] + sm[5]) + (sm[6] + sm[7]));
-            l = l * alpha + sum;
-            m = m_new;
             tmem_wait_st();
             tc_fence_before();
             mbar_arrive(bar_p_full + hf);
