@@ -283,69 +283,80 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                 mbar_wait(bar_v_full + jj % kStages, (jj / kStages) & 1, status);
         }
     } else if (warp == 1) {
-        // =========================== MMA issuer (one thread)
-        if (lane == 0 && n > 0) {
+        // =========================== MMA issuer: the whole warp runs the loop (so
+        // descriptors stay warp-uniform), one elected lane issues and commits.
+        if (n > 0) {
             constexpr uint32_t idesc_qk = idesc_bf16_f32(kHalf, kBKV, 0);
             constexpr uint32_t idesc_pv = idesc_bf16_f32(kHalf, D, 1);
-            const uint32_t q_base0 = smem_u32(sQ);
-            const uint32_t q_base1 = smem_u32(sQ + L::kTile);
-            bool ok = mbar_wait(bar_q, 0, status);
-            if (ok) ok = mbar_wait(bar_k_full, 0, status);
+            const bool leader = elect_one();
+            // base descriptors; K step kk adds (kk / 4) * 16 KiB + (kk % 4) * 32 bytes
+            // (K-major) or kk * 2 KiB (MN-major) to the start-address field (>> 4)
+            const uint64_t dq0 = desc_kmajor_sw128(smem_u32(sQ), 0);
+            const uint64_t dq1 = desc_kmajor_sw128(smem_u32(sQ + L::kTile), 0);
+            const uint64_t dk0 = desc_kmajor_sw128(smem_u32(sK), 0);
+            const uint64_t dv0 = desc_mnmajor_sw128(smem_u32(sV), 0);
+            constexpr uint64_t kStageStep = L::kTile >> 4;
+            auto kstep = [](int kk) -> uint64_t {
+                return static_cast<uint64_t>((kk >> 2) * (kChunkBytesSw128 >> 4) + (kk & 3) * 2);
+            };
+            auto issue_s = [&](uint32_t d_col, uint64_t dq, uint64_t dk) {
+                if (leader) {
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk)
+                        umma_ss(tmem + d_col, dq + kstep(kk), dk + kstep(kk), idesc_qk, kk > 0 ? 1u : 0u);
+                }
+            };
+            auto issue_pv = [&](uint32_t d_col, uint32_t p_col, uint64_t dv, bool acc) {
+                if (leader) {
+#pragma unroll
+                    for (int kk = 0; kk < kBKV / 16; ++kk)
+                        umma_ts(tmem + d_col, tmem + p_col + kk * 8, dv + static_cast<uint64_t>(kk * 128), idesc_pv,
+                                (acc || kk > 0) ? 1u : 0u);
+                }
+            };
+            auto commit = [&](uint64_t* bar) {
+                if (leader) tc_commit(bar);
+            };
+            bool ok = __all_sync(0xFFFFFFFFu, mbar_wait_spin(bar_q, 0, status));
+            if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait_spin(bar_k_full, 0, status));
             if (ok) {
                 tc_fence_after();
-                const uint32_t k_base = smem_u32(sK);
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk)
-                    umma_ss(tmem + kColS, desc_kmajor_sw128(q_base0, kk), desc_kmajor_sw128(k_base, kk), idesc_qk,
-                            kk > 0 ? 1u : 0u);
-                tc_commit(bar_s_full + 0);
+                issue_s(kColS, dq0, dk0);
+                commit(bar_s_full + 0);
             }
             for (int j = 0; ok && j < n; ++j) {
                 const int st = j % kStages;
-                const uint32_t k_base = smem_u32(sK + st * L::kTile);
-                const uint32_t v_base = smem_u32(sV + st * L::kTile);
+                const uint64_t dk = dk0 + st * kStageStep;
+                const uint64_t dv = dv0 + st * kStageStep;
                 // S_1(j): K_j is resident (waited before S_0(j))
-#pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk)
-                    umma_ss(tmem + kColS + 128, desc_kmajor_sw128(q_base1, kk), desc_kmajor_sw128(k_base, kk),
-                            idesc_qk, kk > 0 ? 1u : 0u);
-                tc_commit(bar_s_full + 1);
-                tc_commit(bar_k_empty + st);  // K_j is free once S_0(j) and S_1(j) complete
+                issue_s(kColS + 128, dq1, dk);
+                commit(bar_s_full + 1);
+                commit(bar_k_empty + st);  // K_j is free once S_0(j) and S_1(j) complete
                 // PV_0(j)
-                ok = mbar_wait_spin(bar_v_full + st, (j / kStages) & 1, status);
-                if (ok) ok = mbar_wait_spin(bar_p_full + 0, j & 1, status);
+                ok = __all_sync(0xFFFFFFFFu, mbar_wait_spin(bar_v_full + st, (j / kStages) & 1, status));
+                if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait_spin(bar_p_full + 0, j & 1, status));
                 if (!ok) break;
                 tc_fence_after();
-#pragma unroll
-                for (int kk = 0; kk < kBKV / 16; ++kk)
-                    umma_ts(tmem + kColO, tmem + kColS + kk * 8, desc_mnmajor_sw128(v_base, kk), idesc_pv,
-                            (j > 0 || kk > 0) ? 1u : 0u);
-                tc_commit(bar_o_done + 0);
+                issue_pv(kColO, kColS, dv, j > 0);
+                commit(bar_o_done + 0);
                 // S_0(j+1)
                 if (j + 1 < n) {
                     const int st1 = (j + 1) % kStages;
-                    ok = mbar_wait_spin(bar_k_full + st1, ((j + 1) / kStages) & 1, status);
+                    ok = __all_sync(0xFFFFFFFFu, mbar_wait_spin(bar_k_full + st1, ((j + 1) / kStages) & 1, status));
                     if (!ok) break;
                     tc_fence_after();
-                    const uint32_t k1 = smem_u32(sK + st1 * L::kTile);
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk)
-                        umma_ss(tmem + kColS, desc_kmajor_sw128(q_base0, kk), desc_kmajor_sw128(k1, kk), idesc_qk,
-                                kk > 0 ? 1u : 0u);
-                    tc_commit(bar_s_full + 0);
+                    issue_s(kColS, dq0, dk0 + st1 * kStageStep);
+                    commit(bar_s_full + 0);
                 }
                 // PV_1(j)
-                ok = mbar_wait_spin(bar_p_full + 1, j & 1, status);
+                ok = __all_sync(0xFFFFFFFFu, mbar_wait_spin(bar_p_full + 1, j & 1, status));
                 if (!ok) break;
                 tc_fence_after();
-#pragma unroll
-                for (int kk = 0; kk < kBKV / 16; ++kk)
-                    umma_ts(tmem + kColO + 128, tmem + kColS + 128 + kk * 8, desc_mnmajor_sw128(v_base, kk),
-                            idesc_pv, (j > 0 || kk > 0) ? 1u : 0u);
-                tc_commit(bar_o_done + 1);
-                tc_commit(bar_v_empty + st);
+                issue_pv(kColO + 128, kColS + 128, dv, j > 0);
+                commit(bar_o_done + 1);
+                commit(bar_v_empty + st);
             }
-            tc_commit(bar_mma_done);
+            commit(bar_mma_done);
             mbar_wait(bar_mma_done, 0, status);
         }
     } else if (warp >= 4) {
@@ -423,15 +434,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
 #pragma unroll
                 for (int t = 0; t < 8; ++t) mx[t] = -INFINITY;
 #pragma unroll
-                for (int g = 0; g < 2; ++g) {
-                    uint32_t sr[64];
-                    BSS_TMEM_LD32(t_s + 64 * g, (sr + 0));
-                    BSS_TMEM_LD32(t_s + 64 * g + 32, (sr + 32));
+                for (int cc = 0; cc < 4; ++cc) {
+                    uint32_t sr[32];
+                    BSS_TMEM_LD32(t_s + 32 * cc, sr);
                     tmem_wait_ld();
 #pragma unroll
-                    for (int i = 0; i < 64; ++i) {
-                        const float v =
-                            ((bits[2 * g + (i >> 5)] >> (i & 31)) & 1u) ? __uint_as_float(sr[i]) : -INFINITY;
+                    for (int i = 0; i < 32; ++i) {
+                        const float v = ((bits[cc] >> i) & 1u) ? __uint_as_float(sr[i]) : -INFINITY;
                         mx[i & 7] = fmaxf(mx[i & 7], v);
                     }
                 }
