@@ -74,7 +74,7 @@ class MaskParams:
 EXPORTED = ("bss_build_tile_map", "bss_tile_map_stats", "bss_tile_map_dims", "bss_tile_map_copy_csr",
             "bss_destroy_tile_map", "bss_permute", "bss_sparse_attention", "bss_dense_attention",
             "bss_get_device_status", "bss_status_string", "bss_last_error_message", "bss_version",
-            "bss_diag_mma_tile")
+            "bss_diag_mma_tile", "bss_build_tile_map_csr_noalloc")
 
 
 def load(path: str | None = None):
@@ -114,6 +114,8 @@ def load(path: str | None = None):
     lib.bss_version.restype = i32
     lib.bss_diag_mma_tile.argtypes = [p, p, p, p, p, p, i32, p]
     lib.bss_diag_mma_tile.restype = st
+    lib.bss_build_tile_map_csr_noalloc.argtypes = [MP, i32, i32, i32, p, p, ctypes.c_int64, p, p]
+    lib.bss_build_tile_map_csr_noalloc.restype = st
     _lib = lib
     return lib
 
@@ -277,6 +279,26 @@ def diag_mma_tile(A, B, P, V, S, O, stream=None):
     _check(load().bss_diag_mma_tile(_ptr(A), _ptr(B), _ptr(P), _ptr(V), _ptr(S), _ptr(O), A.shape[1],
                                     _stream(stream)))
     return S, O
+
+
+def noalloc_map_dims(params: MaskParams, kind: int, BQ: int = ATTN_BQ, BKV: int = ATTN_BKV):
+    """(nq, nkv) of the map bss_build_tile_map_csr_noalloc writes for one kind."""
+    N, S = params.N, params.S
+    ncols = (-(-S // BKV) * BKV + N) if (kind == KIND_TEMPORAL and params.temporal_permuted) else N
+    return -(-N // BQ), -(-ncols // BKV)
+
+
+def build_tile_map_csr_noalloc(params: MaskParams, kind: int, row_ptr, entries, stats, BQ: int = ATTN_BQ,
+                               BKV: int = ATTN_BKV, stream=None):
+    """Allocation-free CSR build of one kind into caller-owned device buffers
+    (int32 row_ptr[nq + 1], int32 entries[>= nq * nkv], int64 stats[6])."""
+    import torch
+    _dev_tensor(row_ptr, "row_ptr", torch.int32)
+    _dev_tensor(entries, "entries", torch.int32)
+    _dev_tensor(stats, "stats", torch.int64)
+    _check(load().bss_build_tile_map_csr_noalloc(ctypes.byref(params.c()), kind, BQ, BKV, _ptr(row_ptr),
+                                                  _ptr(entries), entries.numel(), _ptr(stats), _stream(stream)))
+    return row_ptr, entries, stats
 
 
 def attention_step(Q, K, V, O, tile_map: TileMap, head_is_temporal, Qp, Kp, Vp, Op, lse=None, stream=None):

@@ -130,6 +130,8 @@ bss_status encode_tmap_3d(CUtensorMap* map, const void* base, uint64_t inner, ui
     return BSS_OK;
 }
 
+bss_status check_mask_params(const bss_mask_params* p) { return validate_params(p); }
+
 }  // namespace bss
 
 extern "C" {

@@ -39,6 +39,14 @@ struct Geom {
 bss_status build_kind_map(const Geom& g, int32_t code, int32_t rounding, int32_t BQ, int32_t BKV, int32_t nq,
                           KindMap* km, cudaStream_t stream);
 
+// the tile-map kernels on caller-provided buffers (bss_tilemap.cu)
+void tile_map_geometry(const Geom& geo, int32_t code, int32_t BKV, int64_t* ncols, int64_t* nkv);
+bss_status launch_tile_classify(const Geom& geo, int32_t code, int32_t rounding, int32_t BQ, int32_t BKV, int32_t nq,
+                                int32_t nkv, uint8_t* cls, int32_t* row_cnt, unsigned long long* stats,
+                                cudaStream_t stream);
+bss_status launch_tile_compact(int32_t nq, int32_t nkv, const uint8_t* cls, const int32_t* row_ptr, int32_t* entries,
+                               cudaStream_t stream);
+
 // permutation kernel launch (bss_permute.cu)
 bss_status launch_permute(const void* in, void* out, const uint8_t* flags, int32_t H, int32_t F, int32_t S,
                           int32_t d, int32_t inverse, cudaStream_t stream);
@@ -70,6 +78,7 @@ bss_status encode_tmap_3d(CUtensorMap* map, const void* base, uint64_t inner, ui
                           uint64_t row_stride_bytes, uint64_t head_stride_bytes, uint32_t box_inner,
                           uint32_t box_rows);
 int num_sms();
+bss_status check_mask_params(const bss_mask_params* p);  // validation shared by the entry points
 
 }  // namespace bss
 

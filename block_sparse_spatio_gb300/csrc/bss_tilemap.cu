@@ -16,6 +16,7 @@
 
 #include <algorithm>
 #include <cstdint>
+#include <cstring>
 #include <numeric>
 #include <vector>
 
@@ -141,6 +142,50 @@ __global__ void compact_kernel(TmArgs g, const uint8_t* __restrict__ cls, const 
 }
 
 }  // namespace
+
+void tile_map_geometry(const Geom& geo, int32_t code, int32_t BKV, int64_t* ncols, int64_t* nkv) {
+    *ncols = code == MASK_TEMPORAL_VIRT ? static_cast<int64_t>(geo.S_pad) + geo.N : geo.N;
+    *nkv = (*ncols + BKV - 1) / BKV;
+}
+
+bss_status launch_tile_classify(const Geom& geo, int32_t code, int32_t rounding, int32_t BQ, int32_t BKV, int32_t nq,
+                                int32_t nkv, uint8_t* cls, int32_t* row_cnt, unsigned long long* stats,
+                                cudaStream_t stream) {
+    TmArgs g;
+    g.F = geo.F;
+    g.S = geo.S;
+    g.N = geo.N;
+    g.wf = geo.wf;
+    g.ws = geo.ws;
+    g.S_pad = geo.S_pad;
+    g.code = code;
+    g.rounding = rounding;
+    g.BQ = BQ;
+    g.BKV = BKV;
+    g.nq = nq;
+    g.nkv = nkv;
+    const int64_t ntiles = static_cast<int64_t>(nq) * nkv;
+    const int threads = 256;
+    int64_t blocks = (ntiles + threads - 1) / threads;
+    const int64_t cap = static_cast<int64_t>(num_sms()) * 16;
+    if (blocks > cap) blocks = cap;
+    if (blocks < 1) blocks = 1;
+    classify_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(g, cls, row_cnt, stats);
+    return cuda_check(cudaGetLastError(), "classify launch");
+}
+
+bss_status launch_tile_compact(int32_t nq, int32_t nkv, const uint8_t* cls, const int32_t* row_ptr, int32_t* entries,
+                               cudaStream_t stream) {
+    TmArgs g;
+    memset(&g, 0, sizeof(g));
+    g.nq = nq;
+    g.nkv = nkv;
+    const int threads = 256;
+    const int64_t blocks = (static_cast<int64_t>(nq) + (threads / 32) - 1) / (threads / 32);
+    if (blocks <= 0) return BSS_OK;
+    compact_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(g, cls, row_ptr, entries);
+    return cuda_check(cudaGetLastError(), "compact launch");
+}
 
 bss_status build_kind_map(const Geom& geo, int32_t code, int32_t rounding, int32_t BQ, int32_t BKV, int32_t nq,
                           KindMap* km, cudaStream_t stream) {

@@ -168,6 +168,40 @@ bss_status bss_sparse_attention(const void* Q, const void* K, const void* V, voi
 bss_status bss_dense_attention(const void* Q, const void* K, const void* V, void* O, float* lse, int32_t H,
                                int32_t N, int32_t d, float softmax_scale, cudaStream_t stream);
 
+/* Scratch held by bss_build_tile_map_csr_noalloc (bytes): one byte per tile
+ * plus one int32 per q tile (256-byte aligned) must fit in it. */
+#define BSS_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+/* Tile-map build that allocates no device memory.  The blog has no counterpart
+ * to this call: it exists for callers that cannot allocate device memory
+ * themselves -- a framework whose caching allocator owns the GPU's memory and
+ * enforces its own limit, where a stray cudaMalloc can fail or fragment the
+ * pool, or a latency-critical loop where cudaMalloc / cudaFree would
+ * synchronize the device.
+ * Builds the CSR map of ONE mask kind (0 spatial, 1 temporal) into
+ * caller-owned device buffers, with the same contents as the map that
+ * bss_build_tile_map builds for that kind (no longest-first order):
+ *   row_ptr   int32[nq + 1], nq = ceil(N / BQ)
+ *   entries   int32[entries_capacity]; entries_capacity >= nq * nkv, with
+ *             nkv = ceil(ncols / BKV), ncols = N (spatial heads, and temporal
+ *             heads when temporal_permuted = 0) or S_pad + N (permuted temporal
+ *             heads, S_pad = S rounded up to BKV); the first row_ptr[nq] are set
+ *   stats     int64[BSS_STAT_COUNT] (indices BSS_STAT_*)
+ * Its scratch is a file-scope __device__ array of BSS_NOALLOC_SCRATCH_BYTES
+ * that every GPU loading this library holds until the process exits; a map too
+ * large for it returns BSS_ERR_UNSUPPORTED before anything is launched.
+ * Asynchronous on `stream`; calls no cudaMalloc, cudaFree or allocating
+ * library routine.  The first call on a device looks up the array's device
+ * address (cudaGetSymbolAddress), so make that first call before any stream
+ * capture.  Every call uses the same array and it keeps the last call's
+ * contents: calls whose work overlaps on the GPU (other streams or threads)
+ * race and corrupt each other's maps, so serialize them.
+ * Errors: INVALID_ARG (null / misaligned buffer, kind, tile sizes, capacity),
+ * UNSUPPORTED (map larger than the scratch), CUDA. */
+bss_status bss_build_tile_map_csr_noalloc(const bss_mask_params* params, int32_t kind, int32_t BQ, int32_t BKV,
+                                          int32_t* row_ptr, int32_t* entries, int64_t entries_capacity,
+                                          int64_t* stats, cudaStream_t stream);
+
 /* Synchronizes `stream`, returns the current device's status word (BSS_OK or
  * the first device-side error since the last call) and clears it. */
 bss_status bss_get_device_status(cudaStream_t stream);

@@ -124,3 +124,18 @@ def test_product_package_does_not_import_oracle():
                         assert not (node.module or "").startswith("oracle"), fn
             if fn.endswith((".cu", ".cuh", ".h")):
                 assert "oracle" not in open(os.path.join(dirpath, fn)).read().lower(), fn
+
+
+def test_noalloc_rejects_oversized_and_bad_buffers(lib):
+    # host-side checks only: nothing is launched and no device is touched
+    a = ctypes.c_void_p(0x10000)
+    big = bss.MaskParams(F=21, Hs=180, Ws=320, head_dim=128, spatial_frame_window=3,
+                         temporal_raster_window=2450).c()
+    assert lib.bss_build_tile_map_csr_noalloc(ctypes.byref(big), 0, 128, 128, a, a, 1 << 40, a, None) == 2
+    assert b"scratch" in lib.bss_last_error_message()
+    small = _params()
+    assert lib.bss_build_tile_map_csr_noalloc(ctypes.byref(small), 0, 128, 128, None, a, 1 << 20, a, None) == 1
+    assert lib.bss_build_tile_map_csr_noalloc(ctypes.byref(small), 2, 128, 128, a, a, 1 << 20, a, None) == 1
+    assert lib.bss_build_tile_map_csr_noalloc(ctypes.byref(small), 0, 128, 128, a, a, 10, a, None) == 1
+    assert lib.bss_build_tile_map_csr_noalloc(ctypes.byref(small), 0, 128, 128, a, a, 1 << 20,
+                                              ctypes.c_void_p(0x10004), None) == 1
