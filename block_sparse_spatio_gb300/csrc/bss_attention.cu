@@ -74,8 +74,9 @@ struct Smem {
     static constexpr uint32_t kK = 2 * kTile;
     static constexpr uint32_t kV = kK + kStages * kTile;
     static constexpr uint32_t kBar = kV + kStages * kTile;
-    // q, k_full[S], v_full[S], k_empty[S], v_empty[S], s_full[2], p_full[2], o_done[2], mma_done
-    static constexpr uint32_t kNumBars = 1 + 4 * kStages + 2 + 2 + 2 + 1;
+    // q, k_full[S], v_full[S], k_empty[S], v_empty[S], s_full[2][2], p_full[2][2], plo_done[2],
+    // o_done[2], mma_done
+    static constexpr uint32_t kNumBars = 1 + 4 * kStages + 4 + 4 + 2 + 2 + 1;
     static constexpr uint32_t kBytes = kBar + kNumBars * 8 + 16;
     static constexpr uint32_t kAlloc = kBytes + 1024;  // slack for 1024-byte alignment
 };
@@ -180,9 +181,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     uint64_t* bar_v_full = bar_k_full + kStages;
     uint64_t* bar_k_empty = bar_v_full + kStages;
     uint64_t* bar_v_empty = bar_k_empty + kStages;
-    uint64_t* bar_s_full = bar_v_empty + kStages;  // [2] per half
-    uint64_t* bar_p_full = bar_s_full + 2;         // [2] per half
-    uint64_t* bar_o_done = bar_p_full + 2;         // [2] per half
+    uint64_t* bar_s_full = bar_v_empty + kStages;  // [half][column half]: S columns [0,64) / [64,128) landed
+    uint64_t* bar_p_full = bar_s_full + 4;         // [half][column half]: P of those columns written
+    uint64_t* bar_plo_done = bar_p_full + 4;       // [half]: PV over the first 64 keys of the tile done
+    uint64_t* bar_o_done = bar_plo_done + 2;       // [half]: last PV done
     uint64_t* bar_mma_done = bar_o_done + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_mma_done + 1);
 
@@ -217,9 +219,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             mbar_init(bar_k_empty + s, 1);
             mbar_init(bar_v_empty + s, 1);
         }
-        for (int b = 0; b < 2; ++b) {
+        for (int b = 0; b < 4; ++b) {
             mbar_init(bar_s_full + b, 1);
             mbar_init(bar_p_full + b, 128);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(bar_plo_done + b, 1);
             mbar_init(bar_o_done + b, 1);
         }
         mbar_init(bar_mma_done, 1);
@@ -285,78 +290,113 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     } else if (warp == 1) {
         // =========================== MMA issuer: the whole warp runs the loop (so
         // descriptors stay warp-uniform), one elected lane issues and commits.
+        // S of each half is issued as two N = 64 column halves and PV as two K = 64
+        // key halves, so a softmax can start on the first 64 columns while the
+        // rest of S is computed, and PV over the first 64 keys can start while the
+        // softmax still works on the other 64.
         if (n > 0) {
-            constexpr uint32_t idesc_qk = idesc_bf16_f32(kHalf, kBKV, 0);
+            constexpr uint32_t idesc_s = idesc_bf16_f32(kHalf, kBKV / 2, 0);
             constexpr uint32_t idesc_pv = idesc_bf16_f32(kHalf, D, 1);
             const bool leader = elect_one();
             // base descriptors; K step kk adds (kk / 4) * 16 KiB + (kk % 4) * 32 bytes
-            // (K-major) or kk * 2 KiB (MN-major) to the start-address field (>> 4)
+            // (K-major) or kk * 2 KiB (MN-major) to the start-address field (>> 4);
+            // key rows 64..127 of a K tile start 8 KiB into each 64-column chunk
             const uint64_t dq0 = desc_kmajor_sw128(smem_u32(sQ), 0);
             const uint64_t dq1 = desc_kmajor_sw128(smem_u32(sQ + L::kTile), 0);
             const uint64_t dk0 = desc_kmajor_sw128(smem_u32(sK), 0);
             const uint64_t dv0 = desc_mnmajor_sw128(smem_u32(sV), 0);
             constexpr uint64_t kStageStep = L::kTile >> 4;
+            constexpr uint64_t kRowHalfStep = (64 * 128) >> 4;
             auto kstep = [](int kk) -> uint64_t {
                 return static_cast<uint64_t>((kk >> 2) * (kChunkBytesSw128 >> 4) + (kk & 3) * 2);
             };
-            auto issue_s = [&](uint32_t d_col, uint64_t dq, uint64_t dk) {
+            // S_h columns [64 g, 64 g + 64) = Q_h K[rows 64 g ..]^T
+            auto issue_s = [&](int hh, int g, uint64_t dk) {
                 if (leader) {
+                    const uint64_t dq = hh ? dq1 : dq0;
+                    const uint64_t dkg = dk + (g ? kRowHalfStep : 0);
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk)
-                        umma_ss(tmem + d_col, dq + kstep(kk), dk + kstep(kk), idesc_qk, kk > 0 ? 1u : 0u);
+                        umma_ss(tmem + kColS + 128 * hh + 64 * g, dq + kstep(kk), dkg + kstep(kk), idesc_s,
+                                kk > 0 ? 1u : 0u);
                 }
             };
-            auto issue_pv = [&](uint32_t d_col, uint32_t p_col, uint64_t dv, bool acc) {
+            // O_h += P_h[:, keys 64 g ..] V[keys 64 g .., :]
+            auto issue_pv = [&](int hh, int g, uint64_t dv, bool first) {
                 if (leader) {
 #pragma unroll
-                    for (int kk = 0; kk < kBKV / 16; ++kk)
-                        umma_ts(tmem + d_col, tmem + p_col + kk * 8, dv + static_cast<uint64_t>(kk * 128), idesc_pv,
-                                (acc || kk > 0) ? 1u : 0u);
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const int k8 = 4 * g + kk;
+                        umma_ts(tmem + kColO + 128 * hh, tmem + kColS + 128 * hh + k8 * 8,
+                                dv + static_cast<uint64_t>(k8 * 128), idesc_pv, (first && k8 == 0) ? 0u : 1u);
+                    }
                 }
             };
             auto commit = [&](uint64_t* bar) {
                 if (leader) tc_commit(bar);
             };
-            bool ok = __all_sync(0xFFFFFFFFu, mbar_wait_spin(bar_q, 0, status));
-            if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait_spin(bar_k_full, 0, status));
+            auto wait = [&](uint64_t* bar, uint32_t parity) {
+                return __all_sync(0xFFFFFFFFu, mbar_wait_spin(bar, parity, status));
+            };
+            bool ok = wait(bar_q, 0);
+            if (ok) ok = wait(bar_k_full, 0);
             if (ok) {
                 tc_fence_after();
-                issue_s(kColS, dq0, dk0);
+                issue_s(0, 0, dk0);
                 commit(bar_s_full + 0);
+                issue_s(0, 1, dk0);
+                commit(bar_s_full + 1);
             }
             for (int j = 0; ok && j < n; ++j) {
                 const int st = j % kStages;
+                const uint32_t ph = j & 1;
                 const uint64_t dk = dk0 + st * kStageStep;
                 const uint64_t dv = dv0 + st * kStageStep;
                 // S_1(j): K_j is resident (waited before S_0(j))
-                issue_s(kColS + 128, dq1, dk);
-                commit(bar_s_full + 1);
+                issue_s(1, 0, dk);
+                commit(bar_s_full + 2);
+                issue_s(1, 1, dk);
+                commit(bar_s_full + 3);
                 commit(bar_k_empty + st);  // K_j is free once S_0(j) and S_1(j) complete
                 // PV_0(j)
-                ok = __all_sync(0xFFFFFFFFu, mbar_wait_spin(bar_v_full + st, (j / kStages) & 1, status));
-                if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait_spin(bar_p_full + 0, j & 1, status));
+                ok = wait(bar_v_full + st, (j / kStages) & 1);
+                if (ok) ok = wait(bar_p_full + 0, ph);
                 if (!ok) break;
                 tc_fence_after();
-                issue_pv(kColO, kColS, dv, j > 0);
-                commit(bar_o_done + 0);
-                // S_0(j+1)
+                issue_pv(0, 0, dv, j == 0);
+                commit(bar_plo_done + 0);
+                ok = wait(bar_p_full + 1, ph);
+                if (!ok) break;
+                tc_fence_after();
+                issue_pv(0, 1, dv, j == 0);
+                if (j == n - 1) commit(bar_o_done + 0);
+                // S_0(j+1) (it overwrites P_0(j), read by the PVs issued above)
                 if (j + 1 < n) {
                     const int st1 = (j + 1) % kStages;
-                    ok = __all_sync(0xFFFFFFFFu, mbar_wait_spin(bar_k_full + st1, ((j + 1) / kStages) & 1, status));
+                    ok = wait(bar_k_full + st1, ((j + 1) / kStages) & 1);
                     if (!ok) break;
                     tc_fence_after();
-                    issue_s(kColS, dq0, dk0 + st1 * kStageStep);
+                    const uint64_t dk1 = dk0 + st1 * kStageStep;
+                    issue_s(0, 0, dk1);
                     commit(bar_s_full + 0);
+                    issue_s(0, 1, dk1);
+                    commit(bar_s_full + 1);
                 }
                 // PV_1(j)
-                ok = __all_sync(0xFFFFFFFFu, mbar_wait_spin(bar_p_full + 1, j & 1, status));
+                ok = wait(bar_p_full + 2, ph);
                 if (!ok) break;
                 tc_fence_after();
-                issue_pv(kColO + 128, kColS + 128, dv, j > 0);
-                commit(bar_o_done + 1);
+                issue_pv(1, 0, dv, j == 0);
+                commit(bar_plo_done + 1);
+                ok = wait(bar_p_full + 3, ph);
+                if (!ok) break;
+                tc_fence_after();
+                issue_pv(1, 1, dv, j == 0);
                 commit(bar_v_empty + st);
+                if (j == n - 1) commit(bar_o_done + 1);
             }
             commit(bar_mma_done);
+            __syncwarp();
             mbar_wait(bar_mma_done, 0, status);
         }
     } else if (warp >= 4) {
@@ -372,31 +412,33 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         float m = -INFINITY;
         float l = 0.0f;
         bool ok = true;
-        for (int j = 0; j < n; ++j) {
+        for (int j = 0; j < n && ok; ++j) {
             const uint32_t e = entry_at(args, ents, j);
             const int cls = static_cast<int>(e >> BSS_CLASS_SHIFT);
             const int c0 = static_cast<int>(e & BSS_TILE_INDEX_MASK) * kBKV;
-            ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_s_full + hf, j & 1, status));
-            if (!ok) break;
-            tc_fence_after();
-            // ---- fast path: a FULL tile, every row of the warp already has a finite
-            // reference max.  One pass: exponentiate against the current reference
-            // while tracking the tile max; the result is kept unless some row's max
-            // grew by more than 2^8 (then the tile is redone on the general path).
-            bool done = false;
-            if (cls == BSS_CLASS_FULL && __all_sync(0xFFFFFFFFu, m != -INFINITY)) {
-                uint32_t pk[64];
-                float cm0 = -INFINITY, cm1 = -INFINITY;
-                uint64_t s2a = 0ull, s2b = 0ull;  // packed partial sums (two chains)
-                const uint64_t c2 = f2_pack(c, c);
-                const uint64_t nm2 = f2_pack(-m, -m);
-#pragma unroll
-                for (int cc = 0; cc < 4; ++cc) {
-                    uint32_t sr[32];
-                    BSS_TMEM_LD32(t_s + 32 * cc, sr);
+#pragma unroll 1
+            for (int g = 0; g < 2; ++g) {  // the two 64-column halves of the tile
+                ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_s_full + 2 * hf + g, j & 1, status));
+                if (!ok) break;
+                tc_fence_after();
+                const uint32_t t_sg = t_s + 64 * g;        // S columns of this half
+                const uint32_t t_pg = t_s + 32 * g;        // where its bf16 P goes
+                // ---- fast path: FULL tile, every row of the warp has a finite reference
+                // max.  Exponentiate against the current reference while tracking the
+                // max; keep the result unless some row's max grew by more than 2^8.
+                bool done = false;
+                if (cls == BSS_CLASS_FULL && __all_sync(0xFFFFFFFFu, m != -INFINITY)) {
+                    uint32_t sr[64];
+                    BSS_TMEM_LD32(t_sg + 0, (sr + 0));
+                    BSS_TMEM_LD32(t_sg + 32, (sr + 32));
                     tmem_wait_ld();
+                    uint32_t pk[32];
+                    float cm0 = -INFINITY, cm1 = -INFINITY;
+                    uint64_t s2a = 0ull, s2b = 0ull;  // packed partial sums (two chains)
+                    const uint64_t c2 = f2_pack(c, c);
+                    const uint64_t nm2 = f2_pack(-m, -m);
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
+                    for (int i = 0; i < 32; ++i) {
                         const float x0 = __uint_as_float(sr[2 * i]), x1 = __uint_as_float(sr[2 * i + 1]);
                         if (i & 1)
                             cm1 = fmax3(cm1, x0, x1);
@@ -410,96 +452,99 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                             s2b = f2_add(s2b, pp);
                         else
                             s2a = f2_add(s2a, pp);
-                        pk[16 * cc + i] = pack_bf16x2(p0, p1);
-                    }
-                }
-                const float tmax_s = fmaxf(cm0, cm1) * c;
-                if (!__any_sync(0xFFFFFFFFu, tmax_s > m + kRescaleThreshold)) {
-                    float a0, a1, b0, b1;
-                    f2_unpack(s2a, a0, a1);
-                    f2_unpack(s2b, b0, b1);
-                    l += (a0 + a1) + (b0 + b1);
-                    BSS_TMEM_ST32(t_s + 0, (pk + 0));
-                    BSS_TMEM_ST32(t_s + 32, (pk + 32));
-                    done = true;
-                }
-            }
-            if (!done) {
-                // ---- general path: masking (boundary / padding tiles), first tile of
-                // a row, or a reference max that must move.  Pass 1 finds the row max,
-                // pass 2 exponentiates and writes P chunk by chunk.
-                uint32_t bits[4] = {0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu};
-                if (cls != BSS_CLASS_FULL) tile_bits(bits, args, code, cls, c0, rp);
-                float mx[8];
-#pragma unroll
-                for (int t = 0; t < 8; ++t) mx[t] = -INFINITY;
-#pragma unroll
-                for (int cc = 0; cc < 4; ++cc) {
-                    uint32_t sr[32];
-                    BSS_TMEM_LD32(t_s + 32 * cc, sr);
-                    tmem_wait_ld();
-#pragma unroll
-                    for (int i = 0; i < 32; ++i) {
-                        const float v = ((bits[cc] >> i) & 1u) ? __uint_as_float(sr[i]) : -INFINITY;
-                        mx[i & 7] = fmaxf(mx[i & 7], v);
-                    }
-                }
-                const float tmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                         fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-                const float tmax_s = tmax * c;
-                const float m_new = (tmax_s > m + kRescaleThreshold) ? tmax_s : m;
-                const float alpha = (m_new == m) ? 1.0f : ex2_approx(m - m_new);
-                const float mref = (m_new == -INFINITY) ? 0.0f : m_new;
-                // O_h is rescaled only when some row's reference max moved.  PV_h(j-1)
-                // was issued before S_h(j), so it has completed; the wait only orders.
-                if (j >= 1 && __any_sync(0xFFFFFFFFu, alpha != 1.0f)) {
-                    ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_o_done + hf, (j - 1) & 1, status));
-                    if (!ok) break;
-                    tc_fence_after();
-#pragma unroll 1
-                    for (int cc = 0; cc < D / 32; ++cc) {
-                        uint32_t o[32];
-                        BSS_TMEM_LD32(t_o + cc * 32, o);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                        BSS_TMEM_ST32(t_o + cc * 32, o);
-                    }
-                }
-                // P = exp2(s * scale * log2 e - m) as bf16 pairs, written over the first
-                // 64 S columns; 32-column chunk cc lands in columns [16cc, 16cc+16),
-                // which chunks <= cc have already been read from.
-                float sm[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                for (int cc = 0; cc < 4; ++cc) {
-                    uint32_t sr[32];
-                    BSS_TMEM_LD32(t_s + 32 * cc, sr);
-                    tmem_wait_ld();
-                    uint32_t pk[16];
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const float x0 = ((bits[cc] >> (2 * i)) & 1u) ? __uint_as_float(sr[2 * i]) : -INFINITY;
-                        const float x1 =
-                            ((bits[cc] >> (2 * i + 1)) & 1u) ? __uint_as_float(sr[2 * i + 1]) : -INFINITY;
-                        const float p0 = ex2_approx(fmaf(x0, c, -mref));
-                        const float p1 = ex2_approx(fmaf(x1, c, -mref));
-                        sm[(2 * i) & 7] += p0;
-                        sm[(2 * i + 1) & 7] += p1;
                         pk[i] = pack_bf16x2(p0, p1);
                     }
-                    BSS_TMEM_ST16(t_s + 16 * cc, pk);
+                    const float tmax_s = fmaxf(cm0, cm1) * c;
+                    if (!__any_sync(0xFFFFFFFFu, tmax_s > m + kRescaleThreshold)) {
+                        float a0, a1, b0, b1;
+                        f2_unpack(s2a, a0, a1);
+                        f2_unpack(s2b, b0, b1);
+                        l += (a0 + a1) + (b0 + b1);
+                        BSS_TMEM_ST32(t_pg, pk);
+                        done = true;
+                    }
                 }
-                const float sum = ((sm[0] + sm[1]) + (sm[2] + sm[3])) + ((sm[4] + sm[5]) + (sm[6] + sm[7]));
-                l = l * alpha + sum;
-                m = m_new;
+                if (!done) {
+                    // ---- general path: masking (boundary / padding tiles), a row's first
+                    // tile, or a reference max that must move.  Pass 1: max of these 64
+                    // columns; pass 2: exponentiate and write P.
+                    uint32_t bits[4] = {0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu};
+                    if (cls != BSS_CLASS_FULL) tile_bits(bits, args, code, cls, c0, rp);
+                    float mx[8];
+#pragma unroll
+                    for (int t = 0; t < 8; ++t) mx[t] = -INFINITY;
+#pragma unroll
+                    for (int cc = 0; cc < 2; ++cc) {
+                        uint32_t sr[32];
+                        BSS_TMEM_LD32(t_sg + 32 * cc, sr);
+                        tmem_wait_ld();
+                        const uint32_t bw = bits[2 * g + cc];
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) {
+                            const float v = ((bw >> i) & 1u) ? __uint_as_float(sr[i]) : -INFINITY;
+                            mx[i & 7] = fmaxf(mx[i & 7], v);
+                        }
+                    }
+                    const float tmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                             fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+                    const float tmax_s = tmax * c;
+                    const float m_new = (tmax_s > m + kRescaleThreshold) ? tmax_s : m;
+                    const float alpha = (m_new == m) ? 1.0f : ex2_approx(m - m_new);
+                    const float mref = (m_new == -INFINITY) ? 0.0f : m_new;
+                    // O_h holds every PV issued before this S: for the first column half
+                    // that is PV_h(j-1) (issued before S_h(j), so complete); for the
+                    // second it also includes PV over this tile's first 64 keys.
+                    if ((j > 0 || g > 0) && __any_sync(0xFFFFFFFFu, alpha != 1.0f)) {
+                        if (g == 1) {
+                            ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_plo_done + hf, j & 1, status));
+                            if (!ok) break;
+                        }
+                        tc_fence_after();
+#pragma unroll 1
+                        for (int cc = 0; cc < D / 32; ++cc) {
+                            uint32_t o[32];
+                            BSS_TMEM_LD32(t_o + cc * 32, o);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                            BSS_TMEM_ST32(t_o + cc * 32, o);
+                        }
+                    }
+                    float sm[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                    for (int cc = 0; cc < 2; ++cc) {
+                        uint32_t sr[32];
+                        BSS_TMEM_LD32(t_sg + 32 * cc, sr);
+                        tmem_wait_ld();
+                        const uint32_t bw = bits[2 * g + cc];
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) {
+                            const float x0 = ((bw >> (2 * i)) & 1u) ? __uint_as_float(sr[2 * i]) : -INFINITY;
+                            const float x1 =
+                                ((bw >> (2 * i + 1)) & 1u) ? __uint_as_float(sr[2 * i + 1]) : -INFINITY;
+                            const float p0 = ex2_approx(fmaf(x0, c, -mref));
+                            const float p1 = ex2_approx(fmaf(x1, c, -mref));
+                            sm[(2 * i) & 7] += p0;
+                            sm[(2 * i + 1) & 7] += p1;
+                            pk[i] = pack_bf16x2(p0, p1);
+                        }
+                        // chunk cc of this half lands in P columns [16cc, 16cc + 16) of the
+                        // half's 32, which lie in S columns already read
+                        BSS_TMEM_ST16(t_pg + 16 * cc, pk);
+                    }
+                    const float sum = ((sm[0] + sm[1]) + (sm[2] + sm[3])) + ((sm[4] + sm[5]) + (sm[6] + sm[7]));
+                    l = l * alpha + sum;
+                    m = m_new;
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                mbar_arrive(bar_p_full + 2 * hf + g);
             }
-            tmem_wait_st();
-            tc_fence_before();
-            mbar_arrive(bar_p_full + hf);
         }
         // ---- epilogue: O / l -> bf16 -> swizzled staging (reuses this half's Q) -> TMA store
         uint8_t* stage = sQ + hf * L::kTile;
-        if (ok && n > 0) ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_o_done + hf, (n - 1) & 1, status));
+        if (ok && n > 0) ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_o_done + hf, 0, status));
         if (ok) {
             tc_fence_after();
             const float inv_l = l > 0.0f ? 1.0f / l : 0.0f;
