@@ -181,7 +181,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     uint64_t* bar_v_full = bar_k_full + kStages;
     uint64_t* bar_k_empty = bar_v_full + kStages;
     uint64_t* bar_v_empty = bar_k_empty + kStages;
-    uint64_t* bar_s_full = bar_v_empty + kStages;  // [half][column half]: S columns [0,64) / [64,128) landed
+    uint64_t* bar_s_full = bar_v_empty + kStages;  // [2 * half]: S_h landed (entries 2 h + 1 unused)
     uint64_t* bar_p_full = bar_s_full + 4;         // [half][column half]: P of those columns written
     uint64_t* bar_plo_done = bar_p_full + 4;       // [half]: PV over the first 64 keys of the tile done
     uint64_t* bar_o_done = bar_plo_done + 2;       // [half]: last PV done
@@ -290,35 +290,31 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     } else if (warp == 1) {
         // =========================== MMA issuer: the whole warp runs the loop (so
         // descriptors stay warp-uniform), one elected lane issues and commits.
-        // S of each half is issued as two N = 64 column halves and PV as two K = 64
-        // key halves, so a softmax can start on the first 64 columns while the
-        // rest of S is computed, and PV over the first 64 keys can start while the
-        // softmax still works on the other 64.
+        // PV of each half is issued as two K = 64 key halves, so PV over the first
+        // 64 keys starts while the softmax still works on the other 64.  (S stays
+        // one N = 128 group: N = 64 halves would read Q from shared memory twice as
+        // often per FLOP and run shared-memory bound.)
         if (n > 0) {
-            constexpr uint32_t idesc_s = idesc_bf16_f32(kHalf, kBKV / 2, 0);
+            constexpr uint32_t idesc_s = idesc_bf16_f32(kHalf, kBKV, 0);
             constexpr uint32_t idesc_pv = idesc_bf16_f32(kHalf, D, 1);
             const bool leader = elect_one();
             // base descriptors; K step kk adds (kk / 4) * 16 KiB + (kk % 4) * 32 bytes
-            // (K-major) or kk * 2 KiB (MN-major) to the start-address field (>> 4);
-            // key rows 64..127 of a K tile start 8 KiB into each 64-column chunk
+            // (K-major) or kk * 2 KiB (MN-major) to the start-address field (>> 4)
             const uint64_t dq0 = desc_kmajor_sw128(smem_u32(sQ), 0);
             const uint64_t dq1 = desc_kmajor_sw128(smem_u32(sQ + L::kTile), 0);
             const uint64_t dk0 = desc_kmajor_sw128(smem_u32(sK), 0);
             const uint64_t dv0 = desc_mnmajor_sw128(smem_u32(sV), 0);
             constexpr uint64_t kStageStep = L::kTile >> 4;
-            constexpr uint64_t kRowHalfStep = (64 * 128) >> 4;
             auto kstep = [](int kk) -> uint64_t {
                 return static_cast<uint64_t>((kk >> 2) * (kChunkBytesSw128 >> 4) + (kk & 3) * 2);
             };
-            // S_h columns [64 g, 64 g + 64) = Q_h K[rows 64 g ..]^T
-            auto issue_s = [&](int hh, int g, uint64_t dk) {
+            // S_h = Q_h K^T
+            auto issue_s = [&](int hh, uint64_t dk) {
                 if (leader) {
                     const uint64_t dq = hh ? dq1 : dq0;
-                    const uint64_t dkg = dk + (g ? kRowHalfStep : 0);
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk)
-                        umma_ss(tmem + kColS + 128 * hh + 64 * g, dq + kstep(kk), dkg + kstep(kk), idesc_s,
-                                kk > 0 ? 1u : 0u);
+                        umma_ss(tmem + kColS + 128 * hh, dq + kstep(kk), dk + kstep(kk), idesc_s, kk > 0 ? 1u : 0u);
                 }
             };
             // O_h += P_h[:, keys 64 g ..] V[keys 64 g .., :]
@@ -342,10 +338,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             if (ok) ok = wait(bar_k_full, 0);
             if (ok) {
                 tc_fence_after();
-                issue_s(0, 0, dk0);
+                issue_s(0, dk0);
                 commit(bar_s_full + 0);
-                issue_s(0, 1, dk0);
-                commit(bar_s_full + 1);
             }
             for (int j = 0; ok && j < n; ++j) {
                 const int st = j % kStages;
@@ -353,10 +347,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                 const uint64_t dk = dk0 + st * kStageStep;
                 const uint64_t dv = dv0 + st * kStageStep;
                 // S_1(j): K_j is resident (waited before S_0(j))
-                issue_s(1, 0, dk);
+                issue_s(1, dk);
                 commit(bar_s_full + 2);
-                issue_s(1, 1, dk);
-                commit(bar_s_full + 3);
                 commit(bar_k_empty + st);  // K_j is free once S_0(j) and S_1(j) complete
                 // PV_0(j)
                 ok = wait(bar_v_full + st, (j / kStages) & 1);
@@ -377,10 +369,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                     if (!ok) break;
                     tc_fence_after();
                     const uint64_t dk1 = dk0 + st1 * kStageStep;
-                    issue_s(0, 0, dk1);
+                    issue_s(0, dk1);
                     commit(bar_s_full + 0);
-                    issue_s(0, 1, dk1);
-                    commit(bar_s_full + 1);
                 }
                 // PV_1(j)
                 ok = wait(bar_p_full + 2, ph);
@@ -418,9 +408,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             const int c0 = static_cast<int>(e & BSS_TILE_INDEX_MASK) * kBKV;
 #pragma unroll 1
             for (int g = 0; g < 2; ++g) {  // the two 64-column halves of the tile
-                ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_s_full + 2 * hf + g, j & 1, status));
-                if (!ok) break;
-                tc_fence_after();
+                if (g == 0) {
+                    ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_s_full + 2 * hf, j & 1, status));
+                    if (!ok) break;
+                    tc_fence_after();
+                }
                 const uint32_t t_sg = t_s + 64 * g;        // S columns of this half
                 const uint32_t t_pg = t_s + 32 * g;        // where its bf16 P goes
                 // ---- fast path: FULL tile, every row of the warp has a finite reference
@@ -491,9 +483,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                     const float m_new = (tmax_s > m + kRescaleThreshold) ? tmax_s : m;
                     const float alpha = (m_new == m) ? 1.0f : ex2_approx(m - m_new);
                     const float mref = (m_new == -INFINITY) ? 0.0f : m_new;
-                    // O_h holds every PV issued before this S: for the first column half
-                    // that is PV_h(j-1) (issued before S_h(j), so complete); for the
-                    // second it also includes PV over this tile's first 64 keys.
+                    // O_h holds every PV issued before S_h(j) -- complete, since S_h(j)
+                    // completed -- and, for the second column half, PV over this tile's
+                    // first 64 keys, which is waited for.
                     if ((j > 0 || g > 0) && __any_sync(0xFFFFFFFFu, alpha != 1.0f)) {
                         if (g == 1) {
                             ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_plo_done + hf, j & 1, status));
