@@ -9,13 +9,15 @@
 // mask"), or only the padding predicate on padding tiles of a tile-aligned
 // mask (section "Align the sparse mask with final execution").
 //
-// GB300 design.  One CTA per (head, 256-row q tile), 384 threads.  The q tile
-// is two 128-row halves that share every K/V tile brought into shared memory,
-// which halves the L2 -> SM traffic per FLOP compared with 128-row tiles (at
-// 128 rows the kernel ran at the L2 bandwidth limit).
-//   warp 0       TMA producer: Q (both halves) once, then K and V tiles of the
-//                list into separate KV_STAGES-deep rings (128-byte swizzled,
-//                64-column boxes).
+// GB300 design.  A cluster of two CTAs per (head, 512-row q tile); each CTA
+// owns 256 rows as two 128-row halves.  The four halves share every K/V tile:
+// CTA 0 loads each K tile and CTA 1 each V tile, both multicast into the two
+// CTAs' shared memory, so one L2 read of K/V feeds 512 query rows (the L2 ->
+// SM bandwidth is what limits smaller q tiles).  384 threads per CTA:
+//   warp 0       TMA producer: own Q (both halves) once, then its share of the
+//                K / V tiles of the list into separate KV_STAGES-deep rings
+//                (128-byte swizzled, 64-column boxes).  A ring slot is reused
+//                only after both CTAs released it.
 //   warp 1       TMEM allocator and single-thread tcgen05.mma issuer.
 //                TMEM: S_h (128 fp32 columns) and O_h (D columns) per half h;
 //                the bf16 P_h is written over the first 64 columns of S_h.
@@ -44,7 +46,8 @@
 namespace bss {
 namespace {
 
-constexpr int kBQ = 256;        // query rows per CTA (two halves of 128)
+constexpr int kBQ = 512;        // query rows per cluster (two CTAs x two halves of 128)
+constexpr int kCtaRows = 256;   // query rows per CTA
 constexpr int kHalf = 128;      // rows per half = MMA M
 constexpr int kBKV = 128;       // key columns per tile = MMA N of S
 constexpr int kThreads = 384;
@@ -74,9 +77,8 @@ struct Smem {
     static constexpr uint32_t kK = 2 * kTile;
     static constexpr uint32_t kV = kK + kStages * kTile;
     static constexpr uint32_t kBar = kV + kStages * kTile;
-    // q, k_full[S], v_full[S], k_empty[S], v_empty[S], s_full[2][2], p_full[2][2], plo_done[2],
-    // o_done[2], mma_done
-    static constexpr uint32_t kNumBars = 1 + 4 * kStages + 4 + 4 + 2 + 2 + 1;
+    // q, k_full[S], v_full[S], k_empty[S], v_empty[S], s_full[2], p_full[2], o_done[2], mma_done
+    static constexpr uint32_t kNumBars = 1 + 4 * kStages + 2 + 2 + 2 + 1;
     static constexpr uint32_t kBytes = kBar + kNumBars * 8 + 16;
     static constexpr uint32_t kAlloc = kBytes + 1024;  // slack for 1024-byte alignment
 };
@@ -181,10 +183,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     uint64_t* bar_v_full = bar_k_full + kStages;
     uint64_t* bar_k_empty = bar_v_full + kStages;
     uint64_t* bar_v_empty = bar_k_empty + kStages;
-    uint64_t* bar_s_full = bar_v_empty + kStages;  // [2 * half]: S_h landed (entries 2 h + 1 unused)
-    uint64_t* bar_p_full = bar_s_full + 4;         // [half][column half]: P of those columns written
-    uint64_t* bar_plo_done = bar_p_full + 4;       // [half]: PV over the first 64 keys of the tile done
-    uint64_t* bar_o_done = bar_plo_done + 2;       // [half]: last PV done
+    uint64_t* bar_s_full = bar_v_empty + kStages;  // [2] per half
+    uint64_t* bar_p_full = bar_s_full + 2;         // [2] per half
+    uint64_t* bar_o_done = bar_p_full + 2;         // [2] per half
     uint64_t* bar_mma_done = bar_o_done + 2;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_mma_done + 1);
 
@@ -192,8 +193,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     const int lane = threadIdx.x & 31;
     int* status = args.status;
 
-    // ---- work item: (head, q tile); heads in order, q tiles longest first
-    const int item = blockIdx.x;
+    // ---- work item of the cluster: (head, q tile); heads in order, q tiles longest first
+    const uint32_t crank = cluster_ctarank();
+    const int item = blockIdx.x >> 1;
     const int h = item / args.nq;
     const int local = item - h * args.nq;
     int kind = 0;
@@ -216,15 +218,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         for (int s = 0; s < kStages; ++s) {
             mbar_init(bar_k_full + s, 1);
             mbar_init(bar_v_full + s, 1);
-            mbar_init(bar_k_empty + s, 1);
-            mbar_init(bar_v_empty + s, 1);
-        }
-        for (int b = 0; b < 4; ++b) {
-            mbar_init(bar_s_full + b, 1);
-            mbar_init(bar_p_full + b, 128);
+            mbar_init(bar_k_empty + s, 2);  // released by the MMA warps of both CTAs
+            mbar_init(bar_v_empty + s, 2);
         }
         for (int b = 0; b < 2; ++b) {
-            mbar_init(bar_plo_done + b, 1);
+            mbar_init(bar_s_full + b, 1);
+            mbar_init(bar_p_full + b, 128);
             mbar_init(bar_o_done + b, 1);
         }
         mbar_init(bar_mma_done, 1);
@@ -233,8 +232,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
     tc_fence_before();
     __syncthreads();
+    // the peer CTA multicasts into this CTA's shared memory and barriers: both
+    // CTAs' barriers must be initialised first
+    cluster_sync();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    const int row_base = qt * kBQ + static_cast<int>(crank) * kCtaRows;
 
     if (warp == 0) {
         // =========================== TMA producer
@@ -247,7 +250,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             for (int hh = 0; hh < 2; ++hh)
 #pragma unroll
                 for (int c = 0; c < kChunks; ++c)
-                    tma_load_3d(sQ + hh * L::kTile + c * kChunkBytesSw128, &args.tm_q, c * 64, qt * kBQ + hh * kHalf,
+                    tma_load_3d(sQ + hh * L::kTile + c * kChunkBytesSw128, &args.tm_q, c * 64, row_base + hh * kHalf,
                                 h, bar_q);
             bool ok = true;
             int jk = 0, jv = 0;  // K tiles and V tiles issued
@@ -269,16 +272,22 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                 if (jv >= kStages) ok = mbar_wait(bar_k_empty + st, ((jv / kStages) - 1) & 1, status);
                 if (!ok) break;
                 mbar_arrive_expect_tx(bar_k_full + st, L::kTile);
+                if (crank == 0) {
 #pragma unroll
-                for (int c = 0; c < kChunks; ++c)
-                    tma_load_3d(sK + st * L::kTile + c * kChunkBytesSw128, mk, c * 64, row, h, bar_k_full + st);
+                    for (int c = 0; c < kChunks; ++c)
+                        tma_load_3d_multicast(sK + st * L::kTile + c * kChunkBytesSw128, mk, c * 64, row, h,
+                                              bar_k_full + st, 0x3);
+                }
                 jk = jv + 1;
                 if (jv >= kStages) ok = mbar_wait(bar_v_empty + st, ((jv / kStages) - 1) & 1, status);
                 if (!ok) break;
                 mbar_arrive_expect_tx(bar_v_full + st, L::kTile);
+                if (crank == 1) {
 #pragma unroll
-                for (int c = 0; c < kChunks; ++c)
-                    tma_load_3d(sV + st * L::kTile + c * kChunkBytesSw128, mv, c * 64, row, h, bar_v_full + st);
+                    for (int c = 0; c < kChunks; ++c)
+                        tma_load_3d_multicast(sV + st * L::kTile + c * kChunkBytesSw128, mv, c * 64, row, h,
+                                              bar_v_full + st, 0x3);
+                }
             }
             // drain: no copy may still be landing in shared memory at exit
             mbar_wait(bar_q, 0, status);
@@ -286,16 +295,18 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                 mbar_wait(bar_k_full + jj % kStages, (jj / kStages) & 1, status);
             for (int jj = (jv - kStages > 0 ? jv - kStages : 0); jj < jv; ++jj)
                 mbar_wait(bar_v_full + jj % kStages, (jj / kStages) & 1, status);
+            // tail: wait until both CTAs released the last slots, so no release
+            // from the peer can arrive at this CTA after it exits
+            for (int jj = (jk - kStages > 0 ? jk - kStages : 0); jj < jk; ++jj)
+                mbar_wait(bar_k_empty + jj % kStages, (jj / kStages) & 1, status);
+            for (int jj = (jv - kStages > 0 ? jv - kStages : 0); jj < jv; ++jj)
+                mbar_wait(bar_v_empty + jj % kStages, (jj / kStages) & 1, status);
         }
     } else if (warp == 1) {
         // =========================== MMA issuer: the whole warp runs the loop (so
         // descriptors stay warp-uniform), one elected lane issues and commits.
-        // PV of each half is issued as two K = 64 key halves, so PV over the first
-        // 64 keys starts while the softmax still works on the other 64.  (S stays
-        // one N = 128 group: N = 64 halves would read Q from shared memory twice as
-        // often per FLOP and run shared-memory bound.)
         if (n > 0) {
-            constexpr uint32_t idesc_s = idesc_bf16_f32(kHalf, kBKV, 0);
+            constexpr uint32_t idesc_qk = idesc_bf16_f32(kHalf, kBKV, 0);
             constexpr uint32_t idesc_pv = idesc_bf16_f32(kHalf, D, 1);
             const bool leader = elect_one();
             // base descriptors; K step kk adds (kk / 4) * 16 KiB + (kk % 4) * 32 bytes
@@ -308,85 +319,64 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             auto kstep = [](int kk) -> uint64_t {
                 return static_cast<uint64_t>((kk >> 2) * (kChunkBytesSw128 >> 4) + (kk & 3) * 2);
             };
-            // S_h = Q_h K^T
-            auto issue_s = [&](int hh, uint64_t dk) {
+            auto issue_s = [&](uint32_t d_col, uint64_t dq, uint64_t dk) {
                 if (leader) {
-                    const uint64_t dq = hh ? dq1 : dq0;
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk)
-                        umma_ss(tmem + kColS + 128 * hh, dq + kstep(kk), dk + kstep(kk), idesc_s, kk > 0 ? 1u : 0u);
+                        umma_ss(tmem + d_col, dq + kstep(kk), dk + kstep(kk), idesc_qk, kk > 0 ? 1u : 0u);
                 }
             };
-            // O_h += P_h[:, keys 64 g ..] V[keys 64 g .., :]
-            auto issue_pv = [&](int hh, int g, uint64_t dv, bool first) {
+            auto issue_pv = [&](uint32_t d_col, uint32_t p_col, uint64_t dv, bool acc) {
                 if (leader) {
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        const int k8 = 4 * g + kk;
-                        umma_ts(tmem + kColO + 128 * hh, tmem + kColS + 128 * hh + k8 * 8,
-                                dv + static_cast<uint64_t>(k8 * 128), idesc_pv, (first && k8 == 0) ? 0u : 1u);
-                    }
+                    for (int kk = 0; kk < kBKV / 16; ++kk)
+                        umma_ts(tmem + d_col, tmem + p_col + kk * 8, dv + static_cast<uint64_t>(kk * 128), idesc_pv,
+                                (acc || kk > 0) ? 1u : 0u);
                 }
             };
             auto commit = [&](uint64_t* bar) {
                 if (leader) tc_commit(bar);
             };
-            auto wait = [&](uint64_t* bar, uint32_t parity) {
-                return __all_sync(0xFFFFFFFFu, mbar_wait_spin(bar, parity, status));
-            };
-            bool ok = wait(bar_q, 0);
-            if (ok) ok = wait(bar_k_full, 0);
+            bool ok = __all_sync(0xFFFFFFFFu, mbar_wait_spin(bar_q, 0, status));
+            if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait_spin(bar_k_full, 0, status));
             if (ok) {
                 tc_fence_after();
-                issue_s(0, dk0);
+                issue_s(kColS, dq0, dk0);
                 commit(bar_s_full + 0);
             }
             for (int j = 0; ok && j < n; ++j) {
                 const int st = j % kStages;
-                const uint32_t ph = j & 1;
                 const uint64_t dk = dk0 + st * kStageStep;
                 const uint64_t dv = dv0 + st * kStageStep;
                 // S_1(j): K_j is resident (waited before S_0(j))
-                issue_s(1, dk);
-                commit(bar_s_full + 2);
-                commit(bar_k_empty + st);  // K_j is free once S_0(j) and S_1(j) complete
+                issue_s(kColS + 128, dq1, dk);
+                commit(bar_s_full + 1);
+                if (leader) tc_commit_multicast(bar_k_empty + st, 0x3);  // K_j free in both CTAs' view
                 // PV_0(j)
-                ok = wait(bar_v_full + st, (j / kStages) & 1);
-                if (ok) ok = wait(bar_p_full + 0, ph);
+                ok = __all_sync(0xFFFFFFFFu, mbar_wait_spin(bar_v_full + st, (j / kStages) & 1, status));
+                if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait_spin(bar_p_full + 0, j & 1, status));
                 if (!ok) break;
                 tc_fence_after();
-                issue_pv(0, 0, dv, j == 0);
-                commit(bar_plo_done + 0);
-                ok = wait(bar_p_full + 1, ph);
-                if (!ok) break;
-                tc_fence_after();
-                issue_pv(0, 1, dv, j == 0);
-                if (j == n - 1) commit(bar_o_done + 0);
-                // S_0(j+1) (it overwrites P_0(j), read by the PVs issued above)
+                issue_pv(kColO, kColS, dv, j > 0);
+                commit(bar_o_done + 0);
+                // S_0(j+1)
                 if (j + 1 < n) {
                     const int st1 = (j + 1) % kStages;
-                    ok = wait(bar_k_full + st1, ((j + 1) / kStages) & 1);
+                    ok = __all_sync(0xFFFFFFFFu, mbar_wait_spin(bar_k_full + st1, ((j + 1) / kStages) & 1, status));
                     if (!ok) break;
                     tc_fence_after();
-                    const uint64_t dk1 = dk0 + st1 * kStageStep;
-                    issue_s(0, dk1);
+                    issue_s(kColS, dq0, dk0 + st1 * kStageStep);
                     commit(bar_s_full + 0);
                 }
                 // PV_1(j)
-                ok = wait(bar_p_full + 2, ph);
+                ok = __all_sync(0xFFFFFFFFu, mbar_wait_spin(bar_p_full + 1, j & 1, status));
                 if (!ok) break;
                 tc_fence_after();
-                issue_pv(1, 0, dv, j == 0);
-                commit(bar_plo_done + 1);
-                ok = wait(bar_p_full + 3, ph);
-                if (!ok) break;
-                tc_fence_after();
-                issue_pv(1, 1, dv, j == 0);
-                commit(bar_v_empty + st);
-                if (j == n - 1) commit(bar_o_done + 1);
+                issue_pv(kColO + 128, kColS + 128, dv, j > 0);
+                commit(bar_o_done + 1);
+                if (leader) tc_commit_multicast(bar_v_empty + st, 0x3);
             }
             commit(bar_mma_done);
-            __syncwarp();
             mbar_wait(bar_mma_done, 0, status);
         }
     } else if (warp >= 4) {
@@ -396,41 +386,37 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
         const uint32_t t_s = tmem + lane_base + kColS + hf * 128;
         const uint32_t t_o = tmem + lane_base + kColO + hf * 128;
-        const int q = qt * kBQ + hf * kHalf + r;
+        const int q = row_base + hf * kHalf + r;
         const RowPred rp = row_pred(args, code, q);
         const float c = args.scale_log2;
         float m = -INFINITY;
         float l = 0.0f;
         bool ok = true;
-        for (int j = 0; j < n && ok; ++j) {
+        for (int j = 0; j < n; ++j) {
             const uint32_t e = entry_at(args, ents, j);
             const int cls = static_cast<int>(e >> BSS_CLASS_SHIFT);
             const int c0 = static_cast<int>(e & BSS_TILE_INDEX_MASK) * kBKV;
-#pragma unroll 1
-            for (int g = 0; g < 2; ++g) {  // the two 64-column halves of the tile
-                if (g == 0) {
-                    ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_s_full + 2 * hf, j & 1, status));
-                    if (!ok) break;
-                    tc_fence_after();
-                }
-                const uint32_t t_sg = t_s + 64 * g;        // S columns of this half
-                const uint32_t t_pg = t_s + 32 * g;        // where its bf16 P goes
-                // ---- fast path: FULL tile, every row of the warp has a finite reference
-                // max.  Exponentiate against the current reference while tracking the
-                // max; keep the result unless some row's max grew by more than 2^8.
-                bool done = false;
-                if (cls == BSS_CLASS_FULL && __all_sync(0xFFFFFFFFu, m != -INFINITY)) {
-                    uint32_t sr[64];
-                    BSS_TMEM_LD32(t_sg + 0, (sr + 0));
-                    BSS_TMEM_LD32(t_sg + 32, (sr + 32));
-                    tmem_wait_ld();
-                    uint32_t pk[32];
-                    float cm0 = -INFINITY, cm1 = -INFINITY;
-                    uint64_t s2a = 0ull, s2b = 0ull;  // packed partial sums (two chains)
-                    const uint64_t c2 = f2_pack(c, c);
-                    const uint64_t nm2 = f2_pack(-m, -m);
+            ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_s_full + hf, j & 1, status));
+            if (!ok) break;
+            tc_fence_after();
+            // ---- fast path: a FULL tile, every row of the warp already has a finite
+            // reference max.  One pass: exponentiate against the current reference
+            // while tracking the tile max; the result is kept unless some row's max
+            // grew by more than 2^8 (then the tile is redone on the general path).
+            bool done = false;
+            if (cls == BSS_CLASS_FULL && __all_sync(0xFFFFFFFFu, m != -INFINITY)) {
+                uint32_t pk[64];
+                float cm0 = -INFINITY, cm1 = -INFINITY;
+                uint64_t s2a = 0ull, s2b = 0ull;  // packed partial sums (two chains)
+                const uint64_t c2 = f2_pack(c, c);
+                const uint64_t nm2 = f2_pack(-m, -m);
 #pragma unroll
-                    for (int i = 0; i < 32; ++i) {
+                for (int cc = 0; cc < 4; ++cc) {
+                    uint32_t sr[32];
+                    BSS_TMEM_LD32(t_s + 32 * cc, sr);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
                         const float x0 = __uint_as_float(sr[2 * i]), x1 = __uint_as_float(sr[2 * i + 1]);
                         if (i & 1)
                             cm1 = fmax3(cm1, x0, x1);
@@ -444,99 +430,96 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                             s2b = f2_add(s2b, pp);
                         else
                             s2a = f2_add(s2a, pp);
+                        pk[16 * cc + i] = pack_bf16x2(p0, p1);
+                    }
+                }
+                const float tmax_s = fmaxf(cm0, cm1) * c;
+                if (!__any_sync(0xFFFFFFFFu, tmax_s > m + kRescaleThreshold)) {
+                    float a0, a1, b0, b1;
+                    f2_unpack(s2a, a0, a1);
+                    f2_unpack(s2b, b0, b1);
+                    l += (a0 + a1) + (b0 + b1);
+                    BSS_TMEM_ST32(t_s + 0, (pk + 0));
+                    BSS_TMEM_ST32(t_s + 32, (pk + 32));
+                    done = true;
+                }
+            }
+            if (!done) {
+                // ---- general path: masking (boundary / padding tiles), first tile of
+                // a row, or a reference max that must move.  Pass 1 finds the row max,
+                // pass 2 exponentiates and writes P chunk by chunk.
+                uint32_t bits[4] = {0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu};
+                if (cls != BSS_CLASS_FULL) tile_bits(bits, args, code, cls, c0, rp);
+                float mx[8];
+#pragma unroll
+                for (int t = 0; t < 8; ++t) mx[t] = -INFINITY;
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                    uint32_t sr[32];
+                    BSS_TMEM_LD32(t_s + 32 * cc, sr);
+                    tmem_wait_ld();
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) {
+                        const float v = ((bits[cc] >> i) & 1u) ? __uint_as_float(sr[i]) : -INFINITY;
+                        mx[i & 7] = fmaxf(mx[i & 7], v);
+                    }
+                }
+                const float tmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                         fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+                const float tmax_s = tmax * c;
+                const float m_new = (tmax_s > m + kRescaleThreshold) ? tmax_s : m;
+                const float alpha = (m_new == m) ? 1.0f : ex2_approx(m - m_new);
+                const float mref = (m_new == -INFINITY) ? 0.0f : m_new;
+                // O_h is rescaled only when some row's reference max moved.  PV_h(j-1)
+                // was issued before S_h(j), so it has completed; the wait only orders.
+                if (j >= 1 && __any_sync(0xFFFFFFFFu, alpha != 1.0f)) {
+                    ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_o_done + hf, (j - 1) & 1, status));
+                    if (!ok) break;
+                    tc_fence_after();
+#pragma unroll 1
+                    for (int cc = 0; cc < D / 32; ++cc) {
+                        uint32_t o[32];
+                        BSS_TMEM_LD32(t_o + cc * 32, o);
+                        tmem_wait_ld();
+#pragma unroll
+                        for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+                        BSS_TMEM_ST32(t_o + cc * 32, o);
+                    }
+                }
+                // P = exp2(s * scale * log2 e - m) as bf16 pairs, written over the first
+                // 64 S columns; 32-column chunk cc lands in columns [16cc, 16cc+16),
+                // which chunks <= cc have already been read from.
+                float sm[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) {
+                    uint32_t sr[32];
+                    BSS_TMEM_LD32(t_s + 32 * cc, sr);
+                    tmem_wait_ld();
+                    uint32_t pk[16];
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        const float x0 = ((bits[cc] >> (2 * i)) & 1u) ? __uint_as_float(sr[2 * i]) : -INFINITY;
+                        const float x1 =
+                            ((bits[cc] >> (2 * i + 1)) & 1u) ? __uint_as_float(sr[2 * i + 1]) : -INFINITY;
+                        const float p0 = ex2_approx(fmaf(x0, c, -mref));
+                        const float p1 = ex2_approx(fmaf(x1, c, -mref));
+                        sm[(2 * i) & 7] += p0;
+                        sm[(2 * i + 1) & 7] += p1;
                         pk[i] = pack_bf16x2(p0, p1);
                     }
-                    const float tmax_s = fmaxf(cm0, cm1) * c;
-                    if (!__any_sync(0xFFFFFFFFu, tmax_s > m + kRescaleThreshold)) {
-                        float a0, a1, b0, b1;
-                        f2_unpack(s2a, a0, a1);
-                        f2_unpack(s2b, b0, b1);
-                        l += (a0 + a1) + (b0 + b1);
-                        BSS_TMEM_ST32(t_pg, pk);
-                        done = true;
-                    }
+                    BSS_TMEM_ST16(t_s + 16 * cc, pk);
                 }
-                if (!done) {
-                    // ---- general path: masking (boundary / padding tiles), a row's first
-                    // tile, or a reference max that must move.  Pass 1: max of these 64
-                    // columns; pass 2: exponentiate and write P.
-                    uint32_t bits[4] = {0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu};
-                    if (cls != BSS_CLASS_FULL) tile_bits(bits, args, code, cls, c0, rp);
-                    float mx[8];
-#pragma unroll
-                    for (int t = 0; t < 8; ++t) mx[t] = -INFINITY;
-#pragma unroll
-                    for (int cc = 0; cc < 2; ++cc) {
-                        uint32_t sr[32];
-                        BSS_TMEM_LD32(t_sg + 32 * cc, sr);
-                        tmem_wait_ld();
-                        const uint32_t bw = bits[2 * g + cc];
-#pragma unroll
-                        for (int i = 0; i < 32; ++i) {
-                            const float v = ((bw >> i) & 1u) ? __uint_as_float(sr[i]) : -INFINITY;
-                            mx[i & 7] = fmaxf(mx[i & 7], v);
-                        }
-                    }
-                    const float tmax = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                             fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-                    const float tmax_s = tmax * c;
-                    const float m_new = (tmax_s > m + kRescaleThreshold) ? tmax_s : m;
-                    const float alpha = (m_new == m) ? 1.0f : ex2_approx(m - m_new);
-                    const float mref = (m_new == -INFINITY) ? 0.0f : m_new;
-                    // O_h holds every PV issued before S_h(j) -- complete, since S_h(j)
-                    // completed -- and, for the second column half, PV over this tile's
-                    // first 64 keys, which is waited for.
-                    if ((j > 0 || g > 0) && __any_sync(0xFFFFFFFFu, alpha != 1.0f)) {
-                        if (g == 1) {
-                            ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_plo_done + hf, j & 1, status));
-                            if (!ok) break;
-                        }
-                        tc_fence_after();
-#pragma unroll 1
-                        for (int cc = 0; cc < D / 32; ++cc) {
-                            uint32_t o[32];
-                            BSS_TMEM_LD32(t_o + cc * 32, o);
-                            tmem_wait_ld();
-#pragma unroll
-                            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-                            BSS_TMEM_ST32(t_o + cc * 32, o);
-                        }
-                    }
-                    float sm[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-                    for (int cc = 0; cc < 2; ++cc) {
-                        uint32_t sr[32];
-                        BSS_TMEM_LD32(t_sg + 32 * cc, sr);
-                        tmem_wait_ld();
-                        const uint32_t bw = bits[2 * g + cc];
-                        uint32_t pk[16];
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            const float x0 = ((bw >> (2 * i)) & 1u) ? __uint_as_float(sr[2 * i]) : -INFINITY;
-                            const float x1 =
-                                ((bw >> (2 * i + 1)) & 1u) ? __uint_as_float(sr[2 * i + 1]) : -INFINITY;
-                            const float p0 = ex2_approx(fmaf(x0, c, -mref));
-                            const float p1 = ex2_approx(fmaf(x1, c, -mref));
-                            sm[(2 * i) & 7] += p0;
-                            sm[(2 * i + 1) & 7] += p1;
-                            pk[i] = pack_bf16x2(p0, p1);
-                        }
-                        // chunk cc of this half lands in P columns [16cc, 16cc + 16) of the
-                        // half's 32, which lie in S columns already read
-                        BSS_TMEM_ST16(t_pg + 16 * cc, pk);
-                    }
-                    const float sum = ((sm[0] + sm[1]) + (sm[2] + sm[3])) + ((sm[4] + sm[5]) + (sm[6] + sm[7]));
-                    l = l * alpha + sum;
-                    m = m_new;
-                }
-                tmem_wait_st();
-                tc_fence_before();
-                mbar_arrive(bar_p_full + 2 * hf + g);
+                const float sum = ((sm[0] + sm[1]) + (sm[2] + sm[3])) + ((sm[4] + sm[5]) + (sm[6] + sm[7]));
+                l = l * alpha + sum;
+                m = m_new;
             }
+            tmem_wait_st();
+            tc_fence_before();
+            mbar_arrive(bar_p_full + hf);
         }
         // ---- epilogue: O / l -> bf16 -> swizzled staging (reuses this half's Q) -> TMA store
         uint8_t* stage = sQ + hf * L::kTile;
-        if (ok && n > 0) ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_o_done + hf, 0, status));
+        if (ok && n > 0) ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_o_done + hf, (n - 1) & 1, status));
         if (ok) {
             tc_fence_after();
             const float inv_l = l > 0.0f ? 1.0f / l : 0.0f;
@@ -570,7 +553,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             fence_proxy_async_smem();
         }
         named_barrier_sync(1 + hf, 128);
-        const int row0 = qt * kBQ + hf * kHalf;
+        const int row0 = row_base + hf * kHalf;
         if (r == 0 && ok && row0 < args.N) {
 #pragma unroll
             for (int cc = 0; cc < kChunks; ++cc)
@@ -582,6 +565,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
 
     tc_fence_before();
     __syncthreads();
+    cluster_sync();
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();
@@ -633,7 +617,22 @@ bss_status launch_d(const AttnLaunch& a, cudaStream_t stream) {
     const int64_t items = static_cast<int64_t>(a.H) * a.nq;
     if (items <= 0) return BSS_OK;
     if (items > 0x7FFFFFFF) return set_error(BSS_ERR_UNSUPPORTED, "too many work items");
-    attn_fwd_kernel<D><<<static_cast<unsigned>(items), kThreads, smem, stream>>>(args);
+    if (items > 0x3FFFFFFF) return set_error(BSS_ERR_UNSUPPORTED, "too many work items");
+    cudaLaunchConfig_t cfg;
+    memset(&cfg, 0, sizeof(cfg));
+    cfg.gridDim = dim3(static_cast<unsigned>(2 * items), 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaLaunchKernelEx(&cfg, attn_fwd_kernel<D>, args);
+    if (e != cudaSuccess) return cuda_check(e, "attention launch");
     return cuda_check(cudaGetLastError(), "attention launch");
 }
 
