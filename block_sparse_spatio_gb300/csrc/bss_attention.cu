@@ -316,23 +316,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             const uint64_t dk0 = desc_kmajor_sw128(smem_u32(sK), 0);
             const uint64_t dv0 = desc_mnmajor_sw128(smem_u32(sV), 0);
             constexpr uint64_t kStageStep = L::kTile >> 4;
-            auto kstep = [](int kk) -> uint64_t {
-                return static_cast<uint64_t>((kk >> 2) * (kChunkBytesSw128 >> 4) + (kk & 3) * 2);
-            };
             auto issue_s = [&](uint32_t d_col, uint64_t dq, uint64_t dk) {
                 if (leader) {
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk)
-                        umma_ss(tmem + d_col, dq + kstep(kk), dk + kstep(kk), idesc_qk, kk > 0 ? 1u : 0u);
+                    if (D == 128)
+                        umma_ss_k128(tmem + d_col, dq, dk, idesc_qk, 0u);
+                    else
+                        umma_ss_k64(tmem + d_col, dq, dk, idesc_qk, 0u);
                 }
             };
             auto issue_pv = [&](uint32_t d_col, uint32_t p_col, uint64_t dv, bool acc) {
-                if (leader) {
-#pragma unroll
-                    for (int kk = 0; kk < kBKV / 16; ++kk)
-                        umma_ts(tmem + d_col, tmem + p_col + kk * 8, dv + static_cast<uint64_t>(kk * 128), idesc_pv,
-                                (acc || kk > 0) ? 1u : 0u);
-                }
+                if (leader) umma_ts_k128(tmem + d_col, tmem + p_col, dv, idesc_pv, acc ? 1u : 0u);
             };
             auto commit = [&](uint64_t* bar) {
                 if (leader) tc_commit(bar);
@@ -351,14 +344,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                 // S_1(j): K_j is resident (waited before S_0(j))
                 issue_s(kColS + 128, dq1, dk);
                 commit(bar_s_full + 1);
-                if (leader) tc_commit_multicast(bar_k_empty + st, 0x3);  // K_j free in both CTAs' view
                 // PV_0(j)
                 ok = __all_sync(0xFFFFFFFFu, mbar_wait_spin(bar_v_full + st, (j / kStages) & 1, status));
                 if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait_spin(bar_p_full + 0, j & 1, status));
                 if (!ok) break;
                 tc_fence_after();
                 issue_pv(kColO, kColS, dv, j > 0);
-                commit(bar_o_done + 0);
+                if (j == n - 1) commit(bar_o_done + 0);
                 // S_0(j+1)
                 if (j + 1 < n) {
                     const int st1 = (j + 1) % kStages;
@@ -373,8 +365,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                 if (!ok) break;
                 tc_fence_after();
                 issue_pv(kColO + 128, kColS + 128, dv, j > 0);
-                commit(bar_o_done + 1);
-                if (leader) tc_commit_multicast(bar_v_empty + st, 0x3);
+                if (j == n - 1) commit(bar_o_done + 1);
             }
             commit(bar_mma_done);
             mbar_wait(bar_mma_done, 0, status);
@@ -399,6 +390,15 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_s_full + hf, j & 1, status));
             if (!ok) break;
             tc_fence_after();
+            // S_1(j) complete means S_0(j) is too (issued earlier): K_j is free in
+            // this CTA; it also means PV_0(j-1) and PV_1(j-1) completed, so V_{j-1}
+            // is free.  One thread tells both CTAs' producers.
+            if (hf == 1 && r == 0) {
+                for (uint32_t cta = 0; cta < 2; ++cta) {
+                    mbar_arrive_cluster(bar_k_empty + (j % kStages), cta);
+                    if (j >= 1) mbar_arrive_cluster(bar_v_empty + ((j - 1) % kStages), cta);
+                }
+            }
             // ---- fast path: a FULL tile, every row of the warp already has a finite
             // reference max.  One pass: exponentiate against the current reference
             // while tracking the tile max; the result is kept unless some row's max
@@ -471,11 +471,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                 const float alpha = (m_new == m) ? 1.0f : ex2_approx(m - m_new);
                 const float mref = (m_new == -INFINITY) ? 0.0f : m_new;
                 // O_h is rescaled only when some row's reference max moved.  PV_h(j-1)
-                // was issued before S_h(j), so it has completed; the wait only orders.
+                // was issued before S_h(j), whose completion this thread observed.
                 if (j >= 1 && __any_sync(0xFFFFFFFFu, alpha != 1.0f)) {
-                    ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_o_done + hf, (j - 1) & 1, status));
-                    if (!ok) break;
-                    tc_fence_after();
 #pragma unroll 1
                     for (int cc = 0; cc < D / 32; ++cc) {
                         uint32_t o[32];
@@ -519,7 +516,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         }
         // ---- epilogue: O / l -> bf16 -> swizzled staging (reuses this half's Q) -> TMA store
         uint8_t* stage = sQ + hf * L::kTile;
-        if (ok && n > 0) ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_o_done + hf, (n - 1) & 1, status));
+        if (ok && n > 0) ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_o_done + hf, 0, status));
+        if (hf == 1 && r == 0 && n > 0) {  // the last PVs completed: V_{n-1} is free
+            for (uint32_t cta = 0; cta < 2; ++cta) mbar_arrive_cluster(bar_v_empty + ((n - 1) % kStages), cta);
+        }
         if (ok) {
             tc_fence_after();
             const float inv_l = l > 0.0f ? 1.0f / l : 0.0f;
