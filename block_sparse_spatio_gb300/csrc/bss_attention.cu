@@ -18,11 +18,11 @@
 //                K / V tiles of the list into separate KV_STAGES-deep rings
 //                (128-byte swizzled, 64-column boxes).  A ring slot is reused
 //                only after both CTAs released it.
-//   warp 1       TMEM allocator and single-thread tcgen05.mma issuer.
-//                TMEM: S_h (128 fp32 columns) and O_h (D columns) per half h;
-//                the bf16 P_h is written over the first 64 columns of S_h.
-//                Issue order  S_1(j) PV_0(j) S_0(j+1) PV_1(j) S_1(j+1) ...
-//                gives each half's softmax one full MMA tile of time.
+//   warps 1, 2   tcgen05.mma issuers, one per half (warp 1 also allocates
+//                TMEM).  TMEM: S_h (128 fp32 columns) and O_h (D columns) per
+//                half h; the bf16 P_h is written over the first 64 columns of S_h.
+//                Each half is its own in-order stream S_h(0) PV_h(0) S_h(1) ...;
+//                the tensor pipe interleaves the two streams.
 //   warps 4..7   softmax of half 0, warps 8..11 softmax of half 1: one thread
 //                per query row (= TMEM lane).  Reads S, masks boundary /
 //                padding tiles, keeps the running max with a lazy rescale (O
@@ -78,7 +78,7 @@ struct Smem {
     static constexpr uint32_t kV = kK + kStages * kTile;
     static constexpr uint32_t kBar = kV + kStages * kTile;
     // q, k_full[S], v_full[S], k_empty[S], v_empty[S], s_full[2], p_full[2], o_done[2], mma_done
-    static constexpr uint32_t kNumBars = 1 + 4 * kStages + 2 + 2 + 2 + 1;
+    static constexpr uint32_t kNumBars = 1 + 4 * kStages + 2 + 2 + 2 + 2;
     static constexpr uint32_t kBytes = kBar + kNumBars * 8 + 16;
     static constexpr uint32_t kAlloc = kBytes + 1024;  // slack for 1024-byte alignment
 };
@@ -187,7 +187,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     uint64_t* bar_p_full = bar_s_full + 2;         // [2] per half
     uint64_t* bar_o_done = bar_p_full + 2;         // [2] per half
     uint64_t* bar_mma_done = bar_o_done + 2;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_mma_done + 1);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_mma_done + 2);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -218,8 +218,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         for (int s = 0; s < kStages; ++s) {
             mbar_init(bar_k_full + s, 1);
             mbar_init(bar_v_full + s, 1);
-            mbar_init(bar_k_empty + s, 2);  // released by the MMA warps of both CTAs
-            mbar_init(bar_v_empty + s, 2);
+            mbar_init(bar_k_empty + s, 4);  // released by both MMA warps of both CTAs
+            mbar_init(bar_v_empty + s, 4);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar_s_full + b, 1);
@@ -227,6 +227,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             mbar_init(bar_o_done + b, 1);
         }
         mbar_init(bar_mma_done, 1);
+        mbar_init(bar_mma_done + 1, 1);
         mbar_fence_init();
     }
     if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
@@ -302,73 +303,59 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             for (int jj = (jv - kStages > 0 ? jv - kStages : 0); jj < jv; ++jj)
                 mbar_wait(bar_v_empty + jj % kStages, (jj / kStages) & 1, status);
         }
-    } else if (warp == 1) {
-        // =========================== MMA issuer: the whole warp runs the loop (so
-        // descriptors stay warp-uniform), one elected lane issues and commits.
+    } else if (warp == 1 || warp == 2) {
+        // =========================== MMA issuers: warp 1 drives half 0, warp 2 half 1.
+        // Each warp runs its loop warp-uniformly (descriptors stay uniform) and one
+        // elected lane issues and commits.  Per half the stream is
+        // S_h(0) PV_h(0) S_h(1) PV_h(1) ...; MMAs of one thread execute in issue
+        // order, so S_h(j+1) (which overwrites P_h(j)) follows PV_h(j), and the
+        // tensor pipe interleaves the two halves' streams.
+        const int hh = warp - 1;
         if (n > 0) {
             constexpr uint32_t idesc_qk = idesc_bf16_f32(kHalf, kBKV, 0);
             constexpr uint32_t idesc_pv = idesc_bf16_f32(kHalf, D, 1);
             const bool leader = elect_one();
-            // base descriptors; K step kk adds (kk / 4) * 16 KiB + (kk % 4) * 32 bytes
-            // (K-major) or kk * 2 KiB (MN-major) to the start-address field (>> 4)
-            const uint64_t dq0 = desc_kmajor_sw128(smem_u32(sQ), 0);
-            const uint64_t dq1 = desc_kmajor_sw128(smem_u32(sQ + L::kTile), 0);
+            const uint64_t dq = desc_kmajor_sw128(smem_u32(sQ + hh * L::kTile), 0);
             const uint64_t dk0 = desc_kmajor_sw128(smem_u32(sK), 0);
             const uint64_t dv0 = desc_mnmajor_sw128(smem_u32(sV), 0);
             constexpr uint64_t kStageStep = L::kTile >> 4;
-            auto issue_s = [&](uint32_t d_col, uint64_t dq, uint64_t dk) {
-                if (leader) {
-                    if (D == 128)
-                        umma_ss_k128(tmem + d_col, dq, dk, idesc_qk, 0u);
-                    else
-                        umma_ss_k64(tmem + d_col, dq, dk, idesc_qk, 0u);
-                }
+            const uint32_t t_s = tmem + kColS + 128 * hh;
+            const uint32_t t_o = tmem + kColO + 128 * hh;
+            auto wait = [&](uint64_t* bar, uint32_t parity) {
+                return __all_sync(0xFFFFFFFFu, mbar_wait_spin(bar, parity, status));
             };
-            auto issue_pv = [&](uint32_t d_col, uint32_t p_col, uint64_t dv, bool acc) {
-                if (leader) umma_ts_k128(tmem + d_col, tmem + p_col, dv, idesc_pv, acc ? 1u : 0u);
-            };
-            auto commit = [&](uint64_t* bar) {
-                if (leader) tc_commit(bar);
-            };
-            bool ok = __all_sync(0xFFFFFFFFu, mbar_wait_spin(bar_q, 0, status));
-            if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait_spin(bar_k_full, 0, status));
-            if (ok) {
-                tc_fence_after();
-                issue_s(kColS, dq0, dk0);
-                commit(bar_s_full + 0);
-            }
+            bool ok = wait(bar_q, 0);
             for (int j = 0; ok && j < n; ++j) {
                 const int st = j % kStages;
+                const uint32_t ph = (j / kStages) & 1;
                 const uint64_t dk = dk0 + st * kStageStep;
                 const uint64_t dv = dv0 + st * kStageStep;
-                // S_1(j): K_j is resident (waited before S_0(j))
-                issue_s(kColS + 128, dq1, dk);
-                commit(bar_s_full + 1);
-                // PV_0(j)
-                ok = __all_sync(0xFFFFFFFFu, mbar_wait_spin(bar_v_full + st, (j / kStages) & 1, status));
-                if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait_spin(bar_p_full + 0, j & 1, status));
+                // S_h(j) = Q_h K_j^T
+                ok = wait(bar_k_full + st, ph);
                 if (!ok) break;
                 tc_fence_after();
-                issue_pv(kColO, kColS, dv, j > 0);
-                if (j == n - 1) commit(bar_o_done + 0);
-                // S_0(j+1)
-                if (j + 1 < n) {
-                    const int st1 = (j + 1) % kStages;
-                    ok = __all_sync(0xFFFFFFFFu, mbar_wait_spin(bar_k_full + st1, ((j + 1) / kStages) & 1, status));
-                    if (!ok) break;
-                    tc_fence_after();
-                    issue_s(kColS, dq0, dk0 + st1 * kStageStep);
-                    commit(bar_s_full + 0);
+                if (leader) {
+                    if (D == 128)
+                        umma_ss_k128(t_s, dq, dk, idesc_qk, 0u);
+                    else
+                        umma_ss_k64(t_s, dq, dk, idesc_qk, 0u);
+                    tc_commit(bar_s_full + hh);
+                    tc_commit_multicast(bar_k_empty + st, 0x3);  // this half is done with K_j
                 }
-                // PV_1(j)
-                ok = __all_sync(0xFFFFFFFFu, mbar_wait_spin(bar_p_full + 1, j & 1, status));
+                // O_h += P_h(j) V_j
+                ok = wait(bar_v_full + st, ph);
+                if (ok) ok = wait(bar_p_full + hh, j & 1);
                 if (!ok) break;
                 tc_fence_after();
-                issue_pv(kColO + 128, kColS + 128, dv, j > 0);
-                if (j == n - 1) commit(bar_o_done + 1);
+                if (leader) {
+                    umma_ts_k128(t_o, t_s, dv, idesc_pv, j > 0 ? 1u : 0u);
+                    tc_commit_multicast(bar_v_empty + st, 0x3);  // this half is done with V_j
+                    if (j == n - 1) tc_commit(bar_o_done + hh);
+                }
             }
-            commit(bar_mma_done);
-            mbar_wait(bar_mma_done, 0, status);
+            if (leader) tc_commit(bar_mma_done + hh);
+            __syncwarp();
+            mbar_wait(bar_mma_done + hh, 0, status);
         }
     } else if (warp >= 4) {
         // =========================== softmax + epilogue (one thread per row)
@@ -390,15 +377,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_s_full + hf, j & 1, status));
             if (!ok) break;
             tc_fence_after();
-            // S_1(j) complete means S_0(j) is too (issued earlier): K_j is free in
-            // this CTA; it also means PV_0(j-1) and PV_1(j-1) completed, so V_{j-1}
-            // is free.  One thread tells both CTAs' producers.
-            if (hf == 1 && r == 0) {
-                for (uint32_t cta = 0; cta < 2; ++cta) {
-                    mbar_arrive_cluster(bar_k_empty + (j % kStages), cta);
-                    if (j >= 1) mbar_arrive_cluster(bar_v_empty + ((j - 1) % kStages), cta);
-                }
-            }
             // ---- fast path: a FULL tile, every row of the warp already has a finite
             // reference max.  One pass: exponentiate against the current reference
             // while tracking the tile max; the result is kept unless some row's max
@@ -471,7 +449,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                 const float alpha = (m_new == m) ? 1.0f : ex2_approx(m - m_new);
                 const float mref = (m_new == -INFINITY) ? 0.0f : m_new;
                 // O_h is rescaled only when some row's reference max moved.  PV_h(j-1)
-                // was issued before S_h(j), whose completion this thread observed.
+                // was issued before S_h(j) by the same thread, so it completed before
+                // the S_h(j) completion this thread observed.
                 if (j >= 1 && __any_sync(0xFFFFFFFFu, alpha != 1.0f)) {
 #pragma unroll 1
                     for (int cc = 0; cc < D / 32; ++cc) {
@@ -517,9 +496,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         // ---- epilogue: O / l -> bf16 -> swizzled staging (reuses this half's Q) -> TMA store
         uint8_t* stage = sQ + hf * L::kTile;
         if (ok && n > 0) ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_o_done + hf, 0, status));
-        if (hf == 1 && r == 0 && n > 0) {  // the last PVs completed: V_{n-1} is free
-            for (uint32_t cta = 0; cta < 2; ++cta) mbar_arrive_cluster(bar_v_empty + ((n - 1) % kStages), cta);
-        }
         if (ok) {
             tc_fence_after();
             const float inv_l = l > 0.0f ? 1.0f / l : 0.0f;
