@@ -9,20 +9,18 @@
 // mask"), or only the padding predicate on padding tiles of a tile-aligned
 // mask (section "Align the sparse mask with final execution").
 //
-// GB300 design.  A cluster of two CTAs per (head, 512-row q tile); each CTA
-// owns 256 rows as two 128-row halves.  The four halves share every K/V tile:
-// CTA 0 loads each K tile and CTA 1 each V tile, both multicast into the two
-// CTAs' shared memory, so one L2 read of K/V feeds 512 query rows (the L2 ->
-// SM bandwidth is what limits smaller q tiles).  384 threads per CTA:
-//   warp 0       TMA producer: own Q (both halves) once, then its share of the
-//                K / V tiles of the list into separate KV_STAGES-deep rings
-//                (128-byte swizzled, 64-column boxes).  A ring slot is reused
-//                only after both CTAs released it.
-//   warps 1, 2   tcgen05.mma issuers, one per half (warp 1 also allocates
-//                TMEM).  TMEM: S_h (128 fp32 columns) and O_h (D columns) per
-//                half h; the bf16 P_h is written over the first 64 columns of S_h.
-//                Each half is its own in-order stream S_h(0) PV_h(0) S_h(1) ...;
-//                the tensor pipe interleaves the two streams.
+// GB300 design.  One CTA per (head, 256-row q tile), 384 threads.  The q tile
+// is two 128-row halves that share every K/V tile brought into shared memory,
+// which halves the L2 -> SM traffic per FLOP compared with 128-row tiles (at
+// 128 rows the kernel ran at the L2 bandwidth limit).
+//   warp 0       TMA producer: Q (both halves) once, then K and V tiles of the
+//                list into separate KV_STAGES-deep rings (128-byte swizzled,
+//                64-column boxes).
+//   warp 1       TMEM allocator and single-thread tcgen05.mma issuer.
+//                TMEM: S_h (128 fp32 columns) and O_h (D columns) per half h;
+//                the bf16 P_h is written over the first 64 columns of S_h.
+//                Issue order  S_1(j) PV_0(j) S_0(j+1) PV_1(j) S_1(j+1) ...
+//                gives each half's softmax one full MMA tile of time.
 //   warps 4..7   softmax of half 0, warps 8..11 softmax of half 1: one thread
 //                per query row (= TMEM lane).  Reads S, masks boundary /
 //                padding tiles, keeps the running max with a lazy rescale (O
@@ -39,6 +37,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <type_traits>
 
 #include "bss_internal.h"
 #include "bss_ptx.cuh"
@@ -46,8 +45,7 @@
 namespace bss {
 namespace {
 
-constexpr int kBQ = 512;        // query rows per cluster (two CTAs x two halves of 128)
-constexpr int kCtaRows = 256;   // query rows per CTA
+constexpr int kBQ = 256;        // query rows per CTA (two halves of 128)
 constexpr int kHalf = 128;      // rows per half = MMA M
 constexpr int kBKV = 128;       // key columns per tile = MMA N of S
 constexpr int kThreads = 384;
@@ -78,7 +76,7 @@ struct Smem {
     static constexpr uint32_t kV = kK + kStages * kTile;
     static constexpr uint32_t kBar = kV + kStages * kTile;
     // q, k_full[S], v_full[S], k_empty[S], v_empty[S], s_full[2], p_full[2], o_done[2], mma_done
-    static constexpr uint32_t kNumBars = 1 + 4 * kStages + 2 + 2 + 2 + 2;
+    static constexpr uint32_t kNumBars = 1 + 4 * kStages + 2 + 2 + 2 + 1;
     static constexpr uint32_t kBytes = kBar + kNumBars * 8 + 16;
     static constexpr uint32_t kAlloc = kBytes + 1024;  // slack for 1024-byte alignment
 };
@@ -187,15 +185,14 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     uint64_t* bar_p_full = bar_s_full + 2;         // [2] per half
     uint64_t* bar_o_done = bar_p_full + 2;         // [2] per half
     uint64_t* bar_mma_done = bar_o_done + 2;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_mma_done + 2);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_mma_done + 1);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     int* status = args.status;
 
-    // ---- work item of the cluster: (head, q tile); heads in order, q tiles longest first
-    const uint32_t crank = cluster_ctarank();
-    const int item = blockIdx.x >> 1;
+    // ---- work item: (head, q tile); heads in order, q tiles longest first
+    const int item = blockIdx.x;
     const int h = item / args.nq;
     const int local = item - h * args.nq;
     int kind = 0;
@@ -218,8 +215,8 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         for (int s = 0; s < kStages; ++s) {
             mbar_init(bar_k_full + s, 1);
             mbar_init(bar_v_full + s, 1);
-            mbar_init(bar_k_empty + s, 4);  // released by both MMA warps of both CTAs
-            mbar_init(bar_v_empty + s, 4);
+            mbar_init(bar_k_empty + s, 1);
+            mbar_init(bar_v_empty + s, 1);
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(bar_s_full + b, 1);
@@ -227,18 +224,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             mbar_init(bar_o_done + b, 1);
         }
         mbar_init(bar_mma_done, 1);
-        mbar_init(bar_mma_done + 1, 1);
         mbar_fence_init();
     }
     if (warp == 1) tmem_alloc(tmem_slot, kTmemCols);
     tc_fence_before();
     __syncthreads();
-    // the peer CTA multicasts into this CTA's shared memory and barriers: both
-    // CTAs' barriers must be initialised first
-    cluster_sync();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const int row_base = qt * kBQ + static_cast<int>(crank) * kCtaRows;
 
     if (warp == 0) {
         // =========================== TMA producer
@@ -251,7 +243,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             for (int hh = 0; hh < 2; ++hh)
 #pragma unroll
                 for (int c = 0; c < kChunks; ++c)
-                    tma_load_3d(sQ + hh * L::kTile + c * kChunkBytesSw128, &args.tm_q, c * 64, row_base + hh * kHalf,
+                    tma_load_3d(sQ + hh * L::kTile + c * kChunkBytesSw128, &args.tm_q, c * 64, qt * kBQ + hh * kHalf,
                                 h, bar_q);
             bool ok = true;
             int jk = 0, jv = 0;  // K tiles and V tiles issued
@@ -273,22 +265,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                 if (jv >= kStages) ok = mbar_wait(bar_k_empty + st, ((jv / kStages) - 1) & 1, status);
                 if (!ok) break;
                 mbar_arrive_expect_tx(bar_k_full + st, L::kTile);
-                if (crank == 0) {
 #pragma unroll
-                    for (int c = 0; c < kChunks; ++c)
-                        tma_load_3d_multicast(sK + st * L::kTile + c * kChunkBytesSw128, mk, c * 64, row, h,
-                                              bar_k_full + st, 0x3);
-                }
+                for (int c = 0; c < kChunks; ++c)
+                    tma_load_3d(sK + st * L::kTile + c * kChunkBytesSw128, mk, c * 64, row, h, bar_k_full + st);
                 jk = jv + 1;
                 if (jv >= kStages) ok = mbar_wait(bar_v_empty + st, ((jv / kStages) - 1) & 1, status);
                 if (!ok) break;
                 mbar_arrive_expect_tx(bar_v_full + st, L::kTile);
-                if (crank == 1) {
 #pragma unroll
-                    for (int c = 0; c < kChunks; ++c)
-                        tma_load_3d_multicast(sV + st * L::kTile + c * kChunkBytesSw128, mv, c * 64, row, h,
-                                              bar_v_full + st, 0x3);
-                }
+                for (int c = 0; c < kChunks; ++c)
+                    tma_load_3d(sV + st * L::kTile + c * kChunkBytesSw128, mv, c * 64, row, h, bar_v_full + st);
             }
             // drain: no copy may still be landing in shared memory at exit
             mbar_wait(bar_q, 0, status);
@@ -296,66 +282,83 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                 mbar_wait(bar_k_full + jj % kStages, (jj / kStages) & 1, status);
             for (int jj = (jv - kStages > 0 ? jv - kStages : 0); jj < jv; ++jj)
                 mbar_wait(bar_v_full + jj % kStages, (jj / kStages) & 1, status);
-            // tail: wait until both CTAs released the last slots, so no release
-            // from the peer can arrive at this CTA after it exits
-            for (int jj = (jk - kStages > 0 ? jk - kStages : 0); jj < jk; ++jj)
-                mbar_wait(bar_k_empty + jj % kStages, (jj / kStages) & 1, status);
-            for (int jj = (jv - kStages > 0 ? jv - kStages : 0); jj < jv; ++jj)
-                mbar_wait(bar_v_empty + jj % kStages, (jj / kStages) & 1, status);
         }
-    } else if (warp == 1 || warp == 2) {
-        // =========================== MMA issuers: warp 1 drives half 0, warp 2 half 1.
-        // Each warp runs its loop warp-uniformly (descriptors stay uniform) and one
-        // elected lane issues and commits.  Per half the stream is
-        // S_h(0) PV_h(0) S_h(1) PV_h(1) ...; MMAs of one thread execute in issue
-        // order, so S_h(j+1) (which overwrites P_h(j)) follows PV_h(j), and the
-        // tensor pipe interleaves the two halves' streams.
-        const int hh = warp - 1;
+    } else if (warp == 1) {
+        // =========================== MMA issuer: the whole warp runs the loop (so
+        // descriptors stay warp-uniform), one elected lane issues and commits.
         if (n > 0) {
             constexpr uint32_t idesc_qk = idesc_bf16_f32(kHalf, kBKV, 0);
             constexpr uint32_t idesc_pv = idesc_bf16_f32(kHalf, D, 1);
             const bool leader = elect_one();
-            const uint64_t dq = desc_kmajor_sw128(smem_u32(sQ + hh * L::kTile), 0);
+            // base descriptors; K step kk adds (kk / 4) * 16 KiB + (kk % 4) * 32 bytes
+            // (K-major) or kk * 2 KiB (MN-major) to the start-address field (>> 4)
+            const uint64_t dq0 = desc_kmajor_sw128(smem_u32(sQ), 0);
+            const uint64_t dq1 = desc_kmajor_sw128(smem_u32(sQ + L::kTile), 0);
             const uint64_t dk0 = desc_kmajor_sw128(smem_u32(sK), 0);
             const uint64_t dv0 = desc_mnmajor_sw128(smem_u32(sV), 0);
             constexpr uint64_t kStageStep = L::kTile >> 4;
-            const uint32_t t_s = tmem + kColS + 128 * hh;
-            const uint32_t t_o = tmem + kColO + 128 * hh;
-            auto wait = [&](uint64_t* bar, uint32_t parity) {
-                return __all_sync(0xFFFFFFFFu, mbar_wait_spin(bar, parity, status));
+            auto kstep = [](int kk) -> uint64_t {
+                return static_cast<uint64_t>((kk >> 2) * (kChunkBytesSw128 >> 4) + (kk & 3) * 2);
             };
-            bool ok = wait(bar_q, 0);
+            auto issue_s = [&](uint32_t d_col, uint64_t dq, uint64_t dk) {
+                if (leader) {
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk)
+                        umma_ss(tmem + d_col, dq + kstep(kk), dk + kstep(kk), idesc_qk, kk > 0 ? 1u : 0u);
+                }
+            };
+            auto issue_pv = [&](uint32_t d_col, uint32_t p_col, uint64_t dv, bool acc) {
+                if (leader) {
+#pragma unroll
+                    for (int kk = 0; kk < kBKV / 16; ++kk)
+                        umma_ts(tmem + d_col, tmem + p_col + kk * 8, dv + static_cast<uint64_t>(kk * 128), idesc_pv,
+                                (acc || kk > 0) ? 1u : 0u);
+                }
+            };
+            auto commit = [&](uint64_t* bar) {
+                if (leader) tc_commit(bar);
+            };
+            bool ok = __all_sync(0xFFFFFFFFu, mbar_wait_spin(bar_q, 0, status));
+            if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait_spin(bar_k_full, 0, status));
+            if (ok) {
+                tc_fence_after();
+                issue_s(kColS, dq0, dk0);
+                commit(bar_s_full + 0);
+            }
             for (int j = 0; ok && j < n; ++j) {
                 const int st = j % kStages;
-                const uint32_t ph = (j / kStages) & 1;
                 const uint64_t dk = dk0 + st * kStageStep;
                 const uint64_t dv = dv0 + st * kStageStep;
-                // S_h(j) = Q_h K_j^T
-                ok = wait(bar_k_full + st, ph);
+                // S_1(j): K_j is resident (waited before S_0(j))
+                issue_s(kColS + 128, dq1, dk);
+                commit(bar_s_full + 1);
+                commit(bar_k_empty + st);  // K_j is free once S_0(j) and S_1(j) complete
+                // PV_0(j)
+                ok = __all_sync(0xFFFFFFFFu, mbar_wait_spin(bar_v_full + st, (j / kStages) & 1, status));
+                if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait_spin(bar_p_full + 0, j & 1, status));
                 if (!ok) break;
                 tc_fence_after();
-                if (leader) {
-                    if (D == 128)
-                        umma_ss_k128(t_s, dq, dk, idesc_qk, 0u);
-                    else
-                        umma_ss_k64(t_s, dq, dk, idesc_qk, 0u);
-                    tc_commit(bar_s_full + hh);
-                    tc_commit_multicast(bar_k_empty + st, 0x3);  // this half is done with K_j
+                issue_pv(kColO, kColS, dv, j > 0);
+                commit(bar_o_done + 0);
+                // S_0(j+1)
+                if (j + 1 < n) {
+                    const int st1 = (j + 1) % kStages;
+                    ok = __all_sync(0xFFFFFFFFu, mbar_wait_spin(bar_k_full + st1, ((j + 1) / kStages) & 1, status));
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_s(kColS, dq0, dk0 + st1 * kStageStep);
+                    commit(bar_s_full + 0);
                 }
-                // O_h += P_h(j) V_j
-                ok = wait(bar_v_full + st, ph);
-                if (ok) ok = wait(bar_p_full + hh, j & 1);
+                // PV_1(j)
+                ok = __all_sync(0xFFFFFFFFu, mbar_wait_spin(bar_p_full + 1, j & 1, status));
                 if (!ok) break;
                 tc_fence_after();
-                if (leader) {
-                    umma_ts_k128(t_o, t_s, dv, idesc_pv, j > 0 ? 1u : 0u);
-                    tc_commit_multicast(bar_v_empty + st, 0x3);  // this half is done with V_j
-                    if (j == n - 1) tc_commit(bar_o_done + hh);
-                }
+                issue_pv(kColO + 128, kColS + 128, dv, j > 0);
+                commit(bar_o_done + 1);
+                commit(bar_v_empty + st);
             }
-            if (leader) tc_commit(bar_mma_done + hh);
-            __syncwarp();
-            mbar_wait(bar_mma_done + hh, 0, status);
+            commit(bar_mma_done);
+            mbar_wait(bar_mma_done, 0, status);
         }
     } else if (warp >= 4) {
         // =========================== softmax + epilogue (one thread per row)
@@ -364,7 +367,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
         const uint32_t t_s = tmem + lane_base + kColS + hf * 128;
         const uint32_t t_o = tmem + lane_base + kColO + hf * 128;
-        const int q = row_base + hf * kHalf + r;
+        const int q = qt * kBQ + hf * kHalf + r;
         const RowPred rp = row_pred(args, code, q);
         const float c = args.scale_log2;
         float m = -INFINITY;
@@ -377,12 +380,16 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_s_full + hf, j & 1, status));
             if (!ok) break;
             tc_fence_after();
-            // ---- fast path: a FULL tile, every row of the warp already has a finite
-            // reference max.  One pass: exponentiate against the current reference
-            // while tracking the tile max; the result is kept unless some row's max
+            // ---- fast path: every row of the warp already has a finite reference
+            // max.  One pass: exponentiate against the current reference while
+            // tracking the tile max (FULL tiles without any mask, boundary / padding
+            // tiles through their bitmask); the result is kept unless some row's max
             // grew by more than 2^8 (then the tile is redone on the general path).
             bool done = false;
-            if (cls == BSS_CLASS_FULL && __all_sync(0xFFFFFFFFu, m != -INFINITY)) {
+            // one pass over the four 32-column chunks; MASKED applies the tile's
+            // retained-column bitmask (boundary / padding tiles)
+            auto single_pass = [&](auto masked_tag, const uint32_t (&bits)[4]) -> bool {
+                constexpr bool MASKED = decltype(masked_tag)::value;
                 uint32_t pk[64];
                 float cm0 = -INFINITY, cm1 = -INFINITY;
                 uint64_t s2a = 0ull, s2b = 0ull;  // packed partial sums (two chains)
@@ -395,7 +402,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                     tmem_wait_ld();
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
-                        const float x0 = __uint_as_float(sr[2 * i]), x1 = __uint_as_float(sr[2 * i + 1]);
+                        float x0 = __uint_as_float(sr[2 * i]), x1 = __uint_as_float(sr[2 * i + 1]);
+                        if (MASKED) {
+                            x0 = ((bits[cc] >> (2 * i)) & 1u) ? x0 : -INFINITY;
+                            x1 = ((bits[cc] >> (2 * i + 1)) & 1u) ? x1 : -INFINITY;
+                        }
                         if (i & 1)
                             cm1 = fmax3(cm1, x0, x1);
                         else
@@ -412,14 +423,23 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                     }
                 }
                 const float tmax_s = fmaxf(cm0, cm1) * c;
-                if (!__any_sync(0xFFFFFFFFu, tmax_s > m + kRescaleThreshold)) {
-                    float a0, a1, b0, b1;
-                    f2_unpack(s2a, a0, a1);
-                    f2_unpack(s2b, b0, b1);
-                    l += (a0 + a1) + (b0 + b1);
-                    BSS_TMEM_ST32(t_s + 0, (pk + 0));
-                    BSS_TMEM_ST32(t_s + 32, (pk + 32));
-                    done = true;
+                if (__any_sync(0xFFFFFFFFu, tmax_s > m + kRescaleThreshold)) return false;
+                float a0, a1, b0, b1;
+                f2_unpack(s2a, a0, a1);
+                f2_unpack(s2b, b0, b1);
+                l += (a0 + a1) + (b0 + b1);
+                BSS_TMEM_ST32(t_s + 0, (pk + 0));
+                BSS_TMEM_ST32(t_s + 32, (pk + 32));
+                return true;
+            };
+            if (__all_sync(0xFFFFFFFFu, m != -INFINITY)) {
+                if (cls == BSS_CLASS_FULL) {
+                    const uint32_t none[4] = {0u, 0u, 0u, 0u};
+                    done = single_pass(std::integral_constant<bool, false>(), none);
+                } else {
+                    uint32_t bits[4];
+                    tile_bits(bits, args, code, cls, c0, rp);
+                    done = single_pass(std::integral_constant<bool, true>(), bits);
                 }
             }
             if (!done) {
@@ -449,9 +469,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                 const float alpha = (m_new == m) ? 1.0f : ex2_approx(m - m_new);
                 const float mref = (m_new == -INFINITY) ? 0.0f : m_new;
                 // O_h is rescaled only when some row's reference max moved.  PV_h(j-1)
-                // was issued before S_h(j) by the same thread, so it completed before
-                // the S_h(j) completion this thread observed.
+                // was issued before S_h(j), so it has completed; the wait only orders.
                 if (j >= 1 && __any_sync(0xFFFFFFFFu, alpha != 1.0f)) {
+                    ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_o_done + hf, (j - 1) & 1, status));
+                    if (!ok) break;
+                    tc_fence_after();
 #pragma unroll 1
                     for (int cc = 0; cc < D / 32; ++cc) {
                         uint32_t o[32];
@@ -495,7 +517,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         }
         // ---- epilogue: O / l -> bf16 -> swizzled staging (reuses this half's Q) -> TMA store
         uint8_t* stage = sQ + hf * L::kTile;
-        if (ok && n > 0) ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_o_done + hf, 0, status));
+        if (ok && n > 0) ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_o_done + hf, (n - 1) & 1, status));
         if (ok) {
             tc_fence_after();
             const float inv_l = l > 0.0f ? 1.0f / l : 0.0f;
@@ -529,7 +551,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             fence_proxy_async_smem();
         }
         named_barrier_sync(1 + hf, 128);
-        const int row0 = row_base + hf * kHalf;
+        const int row0 = qt * kBQ + hf * kHalf;
         if (r == 0 && ok && row0 < args.N) {
 #pragma unroll
             for (int cc = 0; cc < kChunks; ++cc)
@@ -541,7 +563,6 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
 
     tc_fence_before();
     __syncthreads();
-    cluster_sync();
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();
@@ -593,22 +614,7 @@ bss_status launch_d(const AttnLaunch& a, cudaStream_t stream) {
     const int64_t items = static_cast<int64_t>(a.H) * a.nq;
     if (items <= 0) return BSS_OK;
     if (items > 0x7FFFFFFF) return set_error(BSS_ERR_UNSUPPORTED, "too many work items");
-    if (items > 0x3FFFFFFF) return set_error(BSS_ERR_UNSUPPORTED, "too many work items");
-    cudaLaunchConfig_t cfg;
-    memset(&cfg, 0, sizeof(cfg));
-    cfg.gridDim = dim3(static_cast<unsigned>(2 * items), 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    e = cudaLaunchKernelEx(&cfg, attn_fwd_kernel<D>, args);
-    if (e != cudaSuccess) return cuda_check(e, "attention launch");
+    attn_fwd_kernel<D><<<static_cast<unsigned>(items), kThreads, smem, stream>>>(args);
     return cuda_check(cudaGetLastError(), "attention launch");
 }
 
