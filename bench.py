@@ -363,7 +363,7 @@ def variants(bss, torch, W, w, H, Q, K, V, dev, peaks, flags):
     out["dense_control"] = {"ms": dense_ms, "tflops": dense_flops / dense_ms / 1e9,
                             "frac_of_peak": dense_flops / dense_ms / 1e9 / peaks["bf16_tflops"]}
     zeros = torch.zeros(H, dtype=torch.uint8, device=dev)
-    for name, rnd in (("spatial_exact_B2", 0), ("spatial_tile_aligned_B3", 1)):
+    for name, rnd in (("spatial_naive_B1", 2), ("spatial_exact_B2", 0), ("spatial_tile_aligned_B3", 1)):
         p = bss.MaskParams(w.F, w.Hs, w.Ws, w.d, w.wf, w.ws, temporal_permuted=1, rounding=rnd)
         with bss.build_tile_map(p) as tm:
             s0 = tm.stats(0)

@@ -52,7 +52,7 @@ bss_status validate_params(const bss_mask_params* p) {
     if (p->sink_frames != 1) return set_error(BSS_ERR_UNSUPPORTED, "sink_frames must be 1 (got %d)", p->sink_frames);
     if (p->temporal_permuted != 0 && p->temporal_permuted != 1)
         return set_error(BSS_ERR_INVALID_ARG, "temporal_permuted must be 0 or 1");
-    if (p->rounding != 0 && p->rounding != 1) return set_error(BSS_ERR_INVALID_ARG, "rounding must be 0 or 1");
+    if (p->rounding < 0 || p->rounding > 2) return set_error(BSS_ERR_INVALID_ARG, "rounding must be 0, 1 or 2");
     return BSS_OK;
 }
 

@@ -33,43 +33,45 @@ __device__ __forceinline__ void st_stream(uint4* p, const uint4& v) {
                  : "memory");
 }
 
+// blockIdx.y = head.  Each thread moves one 16-byte piece of UNROLL destination
+// rows per iteration; the source row index (one 32-bit division per row) is the
+// only arithmetic, so the kernel streams at the memory rate.
 template <int VEC_PER_ROW, int UNROLL>
 __global__ void __launch_bounds__(256) permute_kernel(const uint4* __restrict__ in, uint4* __restrict__ out,
-                                                      const uint8_t* __restrict__ flags, int64_t H, int64_t F,
-                                                      int64_t S, int inverse) {
-    const int64_t N = F * S;
-    const int64_t total = H * N * VEC_PER_ROW;
-    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-    int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    for (; i < total; i += stride * UNROLL) {
+                                                      const uint8_t* __restrict__ flags, uint32_t N, uint32_t F,
+                                                      uint32_t S, int inverse) {
+    const uint32_t h = blockIdx.y;
+    const bool perm = flags != nullptr && flags[h] != 0;
+    const uint4* src_h = in + static_cast<size_t>(h) * N * VEC_PER_ROW;
+    uint4* dst_h = out + static_cast<size_t>(h) * N * VEC_PER_ROW;
+    const uint32_t piece = threadIdx.x % VEC_PER_ROW;
+    const uint32_t rows_per_block = blockDim.x / VEC_PER_ROW;
+    const uint32_t row_stride = gridDim.x * rows_per_block;
+    for (uint32_t row0 = blockIdx.x * rows_per_block + threadIdx.x / VEC_PER_ROW; row0 < N;
+         row0 += row_stride * UNROLL) {
         uint4 v[UNROLL];
-        int64_t dst[UNROLL];
+        uint32_t dst[UNROLL];
 #pragma unroll
         for (int u = 0; u < UNROLL; ++u) {
-            const int64_t idx = i + u * stride;
-            dst[u] = -1;
-            if (idx < total) {
-                const int64_t row = idx / VEC_PER_ROW;
-                const int64_t piece = idx - row * VEC_PER_ROW;
-                const int64_t h = row / N;
-                const int64_t x = row - h * N;  // destination token
-                int64_t src = x;
-                if (flags != nullptr && flags[h]) {
+            const uint32_t x = row0 + u * row_stride;  // destination row
+            dst[u] = x;
+            if (x < N) {
+                uint32_t src = x;
+                if (perm) {
                     if (!inverse) {  // destination x = s*F + f  <-  source f*S + s
-                        const int64_t s = x / F, f = x - s * F;
-                        src = f * S + s;
+                        const uint32_t sp = x / F, f = x - sp * F;
+                        src = f * S + sp;
                     } else {  // destination x = f*S + s  <-  source s*F + f
-                        const int64_t f = x / S, s = x - f * S;
-                        src = s * F + f;
+                        const uint32_t f = x / S, sp = x - f * S;
+                        src = sp * F + f;
                     }
                 }
-                v[u] = ld_stream(in + (h * N + src) * VEC_PER_ROW + piece);
-                dst[u] = idx;
+                v[u] = ld_stream(src_h + static_cast<size_t>(src) * VEC_PER_ROW + piece);
             }
         }
 #pragma unroll
         for (int u = 0; u < UNROLL; ++u)
-            if (dst[u] >= 0) st_stream(out + dst[u], v[u]);
+            if (dst[u] < N) st_stream(dst_h + static_cast<size_t>(dst[u]) * VEC_PER_ROW + piece, v[u]);
     }
 }
 
@@ -78,18 +80,26 @@ __global__ void __launch_bounds__(256) permute_kernel(const uint4* __restrict__ 
 bss_status launch_permute(const void* in, void* out, const uint8_t* flags, int32_t H, int32_t F, int32_t S,
                           int32_t d, int32_t inverse, cudaStream_t stream) {
     const int64_t N = static_cast<int64_t>(F) * S;
+    if (N == 0 || H == 0) return BSS_OK;
+    if (N > 0xFFFFFFFFll / 16) return set_error(BSS_ERR_UNSUPPORTED, "too many tokens per head");
+    if (H > 65535) return set_error(BSS_ERR_UNSUPPORTED, "too many heads (at most 65535)");
     const int threads = 256;
-    const int64_t blocks = static_cast<int64_t>(num_sms()) * 8;
-    const int64_t total_vec = static_cast<int64_t>(H) * N * (d * 2 / 16);
-    if (total_vec == 0) return BSS_OK;
-    const int64_t need = (total_vec + threads - 1) / threads;
-    const unsigned grid = static_cast<unsigned>(need < blocks ? need : blocks);
+    const int vec = d * 2 / 16;
+    constexpr int kUnroll = 4;
+    const int64_t rows_per_block = threads / vec;
+    int64_t bx = (N + rows_per_block * kUnroll - 1) / (rows_per_block * kUnroll);
+    const int64_t cap = (static_cast<int64_t>(num_sms()) * 8 + H - 1) / H;
+    if (bx > cap) bx = cap;
+    if (bx < 1) bx = 1;
+    const dim3 grid(static_cast<unsigned>(bx), static_cast<unsigned>(H), 1);
     const uint4* src = static_cast<const uint4*>(in);
     uint4* dst = static_cast<uint4*>(out);
     if (d == 128) {
-        permute_kernel<16, 4><<<grid, threads, 0, stream>>>(src, dst, flags, H, F, S, inverse);
+        permute_kernel<16, kUnroll><<<grid, threads, 0, stream>>>(src, dst, flags, static_cast<uint32_t>(N), F, S,
+                                                                 inverse);
     } else if (d == 64) {
-        permute_kernel<8, 4><<<grid, threads, 0, stream>>>(src, dst, flags, H, F, S, inverse);
+        permute_kernel<8, kUnroll><<<grid, threads, 0, stream>>>(src, dst, flags, static_cast<uint32_t>(N), F, S,
+                                                                inverse);
     } else {
         return set_error(BSS_ERR_UNSUPPORTED, "head_dim %d not supported (64 or 128)", d);
     }

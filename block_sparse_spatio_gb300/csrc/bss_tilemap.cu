@@ -6,7 +6,8 @@
 // physical sparsity"; with tile-aligned rounding a tile is kept or dropped as
 // a whole and only padding is masked, section "Align the sparse mask with
 // final execution" (this library keeps a tile iff at least half of its real
-// pairs are retained).
+// pairs are retained).  Mode 2 reproduces the blog's naive traversal (B1):
+// tiles are skipped or visited, and every visited tile evaluates the mask.
 //
 // Counting uses the closed-form interval structure of each query row's
 // retained set (at most three intervals, or one per frame for the striped
@@ -95,8 +96,11 @@ __global__ void classify_kernel(TmArgs g, uint8_t* __restrict__ cls, int32_t* __
         const int64_t rc = real_cols(g, c0, c1);
         uint8_t k;
         int64_t retained;
-        if (!g.rounding) {
+        if (g.rounding == 0) {
             k = c == 0 ? CLS_SKIP : ((rc == g.BKV && c == rr * g.BKV) ? CLS_FULL : CLS_BOUNDARY);
+            retained = c;
+        } else if (g.rounding == 2) {  // every visited tile evaluates the exact mask
+            k = c == 0 ? CLS_SKIP : CLS_BOUNDARY;
             retained = c;
         } else {
             const int64_t area = rr * rc;

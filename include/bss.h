@@ -84,10 +84,14 @@ enum {
  *                      rows; 0: temporal heads stay in (F,H,W) order and the
  *                      kernel evaluates the striped predicate (the blog's
  *                      "handling temporal access inside the kernel").
- *   rounding           0: exact mask (full / boundary / skip tiles);
+ *   rounding           0: exact mask (full / boundary / skip tiles; the
+ *                      blog's B2);
  *                      1: tile-aligned mask, a tile is kept iff at least half
  *                      of its real pairs are retained, then only padding
- *                      columns are masked. */
+ *                      columns are masked (B3);
+ *                      2: exact mask evaluated in every visited tile (the
+ *                      blog's naive traversal B1, kept for comparison: every
+ *                      non-skipped tile is classed BOUNDARY). */
 typedef struct {
     int32_t F, Hs, Ws;
     int32_t head_dim;

@@ -133,8 +133,9 @@ def num_cols(kind: int, g: Geometry) -> int:
     return int(_load().orc_num_cols(kind, ctypes.byref(gc)))
 
 
-def classify(kind: int, g: Geometry, BQ: int, BKV: int, rounding: bool, qt0: int = 0, qt1: int | None = None):
-    """Per-tile retained real-pair counts and classes for q-tile rows [qt0, qt1)."""
+def classify(kind: int, g: Geometry, BQ: int, BKV: int, rounding, qt0: int = 0, qt1: int | None = None):
+    """Per-tile retained real-pair counts and classes for q-tile rows [qt0, qt1).
+    rounding: 0 exact, 1 tile-aligned, 2 exact mask in every visited tile."""
     g = g.with_bkv(BKV)
     nq = -(-g.N // BQ)
     if qt1 is None:
@@ -143,7 +144,7 @@ def classify(kind: int, g: Geometry, BQ: int, BKV: int, rounding: bool, qt0: int
     counts = np.zeros((qt1 - qt0, nkv), dtype=np.int64)
     cls = np.zeros((qt1 - qt0, nkv), dtype=np.int8)
     gc = g.c()
-    _load().orc_classify(kind, ctypes.byref(gc), BQ, BKV, int(bool(rounding)), qt0, qt1,
+    _load().orc_classify(kind, ctypes.byref(gc), BQ, BKV, int(rounding), qt0, qt1,
                          counts.ctypes.data, cls.ctypes.data)
     return counts, cls
 
@@ -176,7 +177,7 @@ def tile_map(kind: int, g: Geometry, BQ: int, BKV: int, rounding: bool, qt0: int
     q0 = qt0 if qt0 else 0
     real_rows = np.array([min(BQ, max(0, gg.N - (q0 + i) * BQ)) for i in range(rows)], dtype=np.int64)
     kept = cls != SKIP
-    if rounding:
+    if rounding == 1:
         retained_pairs = int((kept * np.outer(real_rows, real_cols)).sum())
     else:
         retained_pairs = int(counts.sum())
@@ -198,7 +199,7 @@ def _layout_kind(kind: int, g: Geometry):
 
 
 def attention(Q: np.ndarray, K: np.ndarray, V: np.ndarray, kind: int, g: Geometry, rows=None,
-              rounding: bool = False, BQ: int = 128, BKV: int = 128, scale: float | None = None):
+              rounding=0, BQ: int = 128, BKV: int = 128, scale: float | None = None):
     """fp64 masked attention of ONE head.
 
     Q, K, V: [N][d] uint16 (bf16 bits) in the ORIGINAL (F,H,W) token order.
@@ -228,7 +229,7 @@ def attention(Q: np.ndarray, K: np.ndarray, V: np.ndarray, kind: int, g: Geometr
         Qp, Kp, Vp, lrows = Q, K, V, rows
     kept_ptr = None
     kept = None
-    if rounding:
+    if rounding == 1:  # only the tile-aligned mask changes the retained set
         nq = -(-N // BQ)
         nkv = -(-num_cols(kind, g) // BKV)
         kept = np.zeros((nq, nkv), dtype=np.int8)

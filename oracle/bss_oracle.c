@@ -154,7 +154,9 @@ int64_t orc_num_cols(int kind, const orc_geom *g) {
  *                  -> FULL; otherwise BOUNDARY.
  *        rounded   kept iff real_area > 0 and 2c >= real_area (reading of the
  *                  "balanced" rounding: at least half the tile is retained);
- *                  kept tiles with a padding column -> PAD, else FULL. */
+ *                  kept tiles with a padding column -> PAD, else FULL.
+ *        naive     (mode 2, the blog's B1 naive traversal) c == 0 -> SKIP;
+ *                  every visited tile -> BOUNDARY. */
 void orc_classify(int kind, const orc_geom *g, int64_t BQ, int64_t BKV, int rounding,
                   int64_t qt0, int64_t qt1, int64_t *counts, int8_t *cls) {
     int64_t ncols = orc_num_cols(kind, g);
@@ -169,7 +171,9 @@ void orc_classify(int kind, const orc_geom *g, int64_t BQ, int64_t BKV, int roun
         for (int64_t q = I * BQ; q < (I + 1) * BQ; ++q)
             for (int64_t k = J * BKV; k < (J + 1) * BKV; ++k) c += orc_retained(kind, g, q, k);
         int8_t cl;
-        if (!rounding) {
+        if (rounding == 2) {
+            cl = c == 0 ? ORC_SKIP : ORC_BOUNDARY;
+        } else if (!rounding) {
             if (c == 0) cl = ORC_SKIP;
             else if (real_cols == BKV && c == real_rows * BKV) cl = ORC_FULL;
             else cl = ORC_BOUNDARY;

@@ -52,7 +52,7 @@ def _params(**kw):
 
 @pytest.mark.parametrize("kw,code", [
     (dict(F=0), 1), (dict(Hs=-1), 1), (dict(head_dim=96), 2), (dict(spatial_frame_window=-1), 1),
-    (dict(sink_frames=2), 2), (dict(rounding=3), 1), (dict(temporal_permuted=2), 1),
+    (dict(sink_frames=2), 2), (dict(rounding=3), 1), (dict(rounding=-1), 1), (dict(temporal_permuted=2), 1),
 ])
 def test_build_tile_map_rejects_bad_params(lib, kw, code):
     h = ctypes.c_void_p()

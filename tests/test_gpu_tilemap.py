@@ -38,7 +38,7 @@ def check_map(bss, tm, kind_code, g, BQ, BKV, rounding, qtiles=None):
 
 @pytest.mark.gpu
 @pytest.mark.parametrize("geo", GEOMS, ids=[x[0] for x in GEOMS])
-@pytest.mark.parametrize("rounding", [0, 1])
+@pytest.mark.parametrize("rounding", [0, 1, 2])
 @pytest.mark.parametrize("tperm", [1, 0])
 def test_tile_map_bit_exact_small(bss, geo, rounding, tperm):
     name, F, Hs, Ws, wf, ws, d, BQ, BKV = geo

@@ -96,7 +96,9 @@ def tile_classes(M, col_real, BQ, BKV, rounding):
     real_cols = cr.reshape(nkv, BKV).sum(1)
     area = np.outer(real_rows, real_cols)
     cls = np.full((nq, nkv), oracle.SKIP, np.int8)
-    if rounding:
+    if rounding == 2:  # naive traversal: every visited tile masks
+        cls[counts > 0] = oracle.BOUNDARY
+    elif rounding:
         kept = (area > 0) & (2 * counts >= area)
         cls[kept] = oracle.FULL
         cls[kept & (real_cols[None, :] < BKV)] = oracle.PAD
@@ -197,7 +199,7 @@ def test_temporal_virtual_space_counts_each_key_once(g):
 
 @pytest.mark.parametrize("g", GEOMS, ids=[g[0] for g in GEOMS])
 @pytest.mark.parametrize("kind", KINDS)
-@pytest.mark.parametrize("rounding", [0, 1])
+@pytest.mark.parametrize("rounding", [0, 1, 2])
 def test_classify_matches_numpy_tiling(g, kind, rounding):
     name, F, Hs, Ws, wf, ws, BQ, BKV = g
     M, col_tok, col_real, pt = layout_mask(kind, F, Hs, Ws, wf, ws, BKV)
