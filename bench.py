@@ -390,6 +390,12 @@ def variants(bss, torch, W, w, H, Q, K, V, dev, peaks, flags):
             "with_permutation_ms": ms_perm, "attention_only_ms": ms_attn, "in_kernel_indexing_ms": ms_noperm,
             "tflops_attention": fl_ / ms_attn / 1e9, "tflops_in_kernel_indexing": fl_ / ms_noperm / 1e9,
             "tiles_permuted": tm1.stats(1), "tiles_in_kernel_indexing": tm0.stats(1)}
+        rows = torch.tensor(W.sample_rows(w.N, 64, seed=w.index), dtype=torch.int32, device=dev)
+        rflags = torch.empty(H, dtype=torch.uint8, device=dev)
+        rerr = torch.empty(H, 2, dtype=torch.float32, device=dev)
+        route_ms = _time(torch, lambda: bss.route_heads(Q, K, V, p1, rows, rflags, rerr))
+        out["routing"] = {"ms": route_ms, "sampled_rows": int(rows.numel()),
+                          "flags": rflags.cpu().tolist(), "note": "dense/spatial/temporal outputs of the sampled rows"}
         perm_ms = _time(torch, lambda: bss.permute(Q, Qp, ones, p1, False))
         nbytes = 2.0 * Q.numel() * 2
         out["permute"] = {"ms": perm_ms, "gbs": nbytes / perm_ms / 1e6, "frac_of_hbm_peak":

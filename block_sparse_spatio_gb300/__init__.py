@@ -74,7 +74,7 @@ class MaskParams:
 EXPORTED = ("bss_build_tile_map", "bss_tile_map_stats", "bss_tile_map_dims", "bss_tile_map_copy_csr",
             "bss_destroy_tile_map", "bss_permute", "bss_sparse_attention", "bss_dense_attention",
             "bss_get_device_status", "bss_status_string", "bss_last_error_message", "bss_version",
-            "bss_diag_mma_tile", "bss_build_tile_map_csr_noalloc")
+            "bss_diag_mma_tile", "bss_build_tile_map_csr_noalloc", "bss_route_heads")
 
 
 def load(path: str | None = None):
@@ -116,6 +116,8 @@ def load(path: str | None = None):
     lib.bss_diag_mma_tile.restype = st
     lib.bss_build_tile_map_csr_noalloc.argtypes = [MP, i32, i32, i32, p, p, ctypes.c_int64, p, p]
     lib.bss_build_tile_map_csr_noalloc.restype = st
+    lib.bss_route_heads.argtypes = [p, p, p, i32, MP, p, i32, p, p, p]
+    lib.bss_route_heads.restype = st
     _lib = lib
     return lib
 
@@ -299,6 +301,21 @@ def build_tile_map_csr_noalloc(params: MaskParams, kind: int, row_ptr, entries, 
     _check(load().bss_build_tile_map_csr_noalloc(ctypes.byref(params.c()), kind, BQ, BKV, _ptr(row_ptr),
                                                   _ptr(entries), entries.numel(), _ptr(stats), _stream(stream)))
     return row_ptr, entries, stats
+
+
+def route_heads(Q, K, V, params: MaskParams, rows, head_is_temporal, errors, stream=None):
+    """Per-head routing from sampled query rows (int32 device tensor of (F,H,W)
+    token indices): writes head_is_temporal (uint8[H]) and errors (float32[H][2]:
+    spatial and temporal deviation from the dense output)."""
+    import torch
+    for t, n in ((Q, "Q"), (K, "K"), (V, "V")):
+        _dev_tensor(t, n, torch.bfloat16)
+    _dev_tensor(rows, "rows", torch.int32)
+    _dev_tensor(head_is_temporal, "head_is_temporal", torch.uint8)
+    _dev_tensor(errors, "errors", torch.float32)
+    _check(load().bss_route_heads(_ptr(Q), _ptr(K), _ptr(V), Q.shape[0], ctypes.byref(params.c()), _ptr(rows),
+                                  rows.numel(), _ptr(head_is_temporal), _ptr(errors), _stream(stream)))
+    return head_is_temporal, errors
 
 
 def attention_step(Q, K, V, O, tile_map: TileMap, head_is_temporal, Qp, Kp, Vp, Op, lse=None, stream=None):

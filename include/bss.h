@@ -172,6 +172,27 @@ bss_status bss_sparse_attention(const void* Q, const void* K, const void* V, voi
 bss_status bss_dense_attention(const void* Q, const void* K, const void* V, void* O, float* lse, int32_t H,
                                int32_t N, int32_t d, float softmax_scale, cudaStream_t stream);
 
+/* Per-head routing from sampled queries (section "Speeding up attention":
+ * Sparse VideoGen samples a few queries, computes their outputs under dense,
+ * spatial and temporal attention and routes each head to the sparse mask whose
+ * output deviates least from the dense one; Figure 8: one flag per head).
+ * Reading: deviation = squared L2 distance to the dense output summed over the
+ * sampled rows and channels; a head is temporal iff its temporal deviation is
+ * strictly smaller.  Exact fp32 softmaxes, masks in (F,H,W) order.
+ *   Q, K, V           device [H][N][d] bf16 in (F,H,W) order, 16-byte aligned.
+ *   rows              device int32[R]: sampled query tokens (F,H,W index), the
+ *                     same rows for every head; a row outside [0, N) is skipped
+ *                     and recorded as BSS_ERR_INVALID_ARG in the status word.
+ *   head_is_temporal  device uint8[H] output (1 = temporal).
+ *   errors            device float[2 * H] output: per head the spatial and the
+ *                     temporal deviation (accumulated with atomics: exact ties
+ *                     may resolve either way).
+ * Asynchronous on `stream`; allocates nothing.  Errors: INVALID_ARG,
+ * UNSUPPORTED, CUDA. */
+bss_status bss_route_heads(const void* Q, const void* K, const void* V, int32_t H, const bss_mask_params* params,
+                           const int32_t* rows, int32_t R, uint8_t* head_is_temporal, float* errors,
+                           cudaStream_t stream);
+
 /* Scratch held by bss_build_tile_map_csr_noalloc (bytes): one byte per tile
  * plus one int32 per q tile (256-byte aligned) must fit in it. */
 #define BSS_NOALLOC_SCRATCH_BYTES (8u << 20)

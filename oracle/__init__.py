@@ -244,3 +244,22 @@ def attention(Q: np.ndarray, K: np.ndarray, V: np.ndarray, kind: int, g: Geometr
                       float(scale), kept_ptr, BQ, BKV, lrows.ctypes.data, rows.size,
                       O.ctypes.data, lse.ctypes.data)
     return O, lse
+
+
+def route(Q: np.ndarray, K: np.ndarray, V: np.ndarray, g: Geometry, rows):
+    """Per-head routing from sampled queries, fp64 (blog section "Speeding up
+    attention": compare each sampled query's spatial and temporal outputs with
+    its dense output and pick the mask that deviates least).  Deviation = squared
+    L2 distance to the dense output summed over rows and channels; temporal iff
+    strictly smaller.  Q, K, V: [H][N][d] uint16 (bf16 bits), (F,H,W) order.
+    Returns (flags uint8[H], errors float64[H][2])."""
+    H = Q.shape[0]
+    errors = np.zeros((H, 2), dtype=np.float64)
+    for h in range(H):
+        Od, _ = attention(Q[h], K[h], V[h], DENSE, g, rows=rows)
+        Os, _ = attention(Q[h], K[h], V[h], SPATIAL, g, rows=rows)
+        Ot, _ = attention(Q[h], K[h], V[h], TEMPORAL_FHW, g, rows=rows)
+        errors[h, 0] = float(((Os - Od) ** 2).sum())
+        errors[h, 1] = float(((Ot - Od) ** 2).sum())
+    flags = (errors[:, 1] < errors[:, 0]).astype(np.uint8)
+    return flags, errors

@@ -1,0 +1,49 @@
+"""GPU per-head routing against the fp64 oracle (deviations and flags)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+from test_oracle import _structured_heads
+
+
+def _run(bss, q, k, v, p, rows):
+    dev = torch.device("cuda")
+    Q, K, V = (x.to(dev) for x in (q, k, v))
+    R = torch.tensor(rows, dtype=torch.int32, device=dev)
+    flags = torch.empty(q.shape[0], dtype=torch.uint8, device=dev)
+    err = torch.empty(q.shape[0], 2, dtype=torch.float32, device=dev)
+    bss.route_heads(Q, K, V, p, R, flags, err)
+    torch.cuda.synchronize()
+    assert bss.get_device_status() == 0
+    return flags.cpu().numpy(), err.cpu().numpy()
+
+
+@pytest.mark.gpu
+def test_route_structured_heads(bss):
+    F, Hs, Ws, d = 6, 6, 8, 64
+    q, k, v = _structured_heads(F, Hs, Ws, d, 3)
+    p = bss.MaskParams(F, Hs, Ws, d, 1, 2)
+    rows = list(range(0, F * Hs * Ws, 7))
+    flags, err = _run(bss, q, k, v, p, rows)
+    oflags, oerr = oracle.route(W.bf16_bits(q), W.bf16_bits(k), W.bf16_bits(v),
+                                oracle.Geometry(F, Hs, Ws, wf=1, ws=2), rows)
+    assert flags.tolist() == oflags.tolist() == [0, 1]
+    np.testing.assert_allclose(err, oerr, rtol=2e-3, atol=1e-6)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("wl", [W.SMALL, W.MIXED_75K], ids=lambda w: w.name)
+def test_route_random_heads_match_oracle(bss, wl):
+    dev = torch.device("cuda")
+    H = 4
+    q, k, v = W.qkv(wl, H=H, seed=11)
+    rows = W.sample_rows(wl.N, 24, seed=5)
+    p = bss.MaskParams(wl.F, wl.Hs, wl.Ws, wl.d, wl.wf, wl.ws)
+    flags, err = _run(bss, q, k, v, p, rows)
+    oflags, oerr = oracle.route(W.bf16_bits(q), W.bf16_bits(k), W.bf16_bits(v),
+                                oracle.Geometry(wl.F, wl.Hs, wl.Ws, wf=wl.wf, ws=wl.ws), rows)
+    np.testing.assert_allclose(err, oerr, rtol=5e-3, atol=1e-7)
+    clear = np.abs(oerr[:, 0] - oerr[:, 1]) > 1e-2 * np.maximum(oerr[:, 0], oerr[:, 1])
+    assert np.array_equal(flags[clear], oflags[clear])

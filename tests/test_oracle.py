@@ -415,3 +415,49 @@ def test_small_tile_stats_regression():
         _, _, st = oracle.tile_map(kind, gg, 128, 128, rounding)
         st.pop("ncols")
         assert st == gold[key], key
+
+
+# ----------------------------------------------------------------------------
+# routing (blog section "Speeding up attention")
+# ----------------------------------------------------------------------------
+def _structured_heads(F, Hs, Ws, d, seed):
+    """Two heads of constructed data: head 0 attends within its own frame (every
+    key of frame f points along a frame-specific direction shared by that
+    frame's queries), head 1 attends to its own raster position across frames
+    (keys at raster s share a direction with queries at s)."""
+    g = torch.Generator().manual_seed(seed)
+    S, N = Hs * Ws, F * Hs * Ws
+    f = torch.arange(N) // S
+    s = torch.arange(N) % S
+    noise = 0.05
+    fdir = torch.randn(F, d, generator=g)
+    sdir = torch.randn(S, d, generator=g)
+    Q = torch.empty(2, N, d)
+    K = torch.empty(2, N, d)
+    Q[0] = 3.0 * fdir[f] + noise * torch.randn(N, d, generator=g)
+    K[0] = fdir[f] + noise * torch.randn(N, d, generator=g)
+    Q[1] = 3.0 * sdir[s] + noise * torch.randn(N, d, generator=g)
+    K[1] = sdir[s] + noise * torch.randn(N, d, generator=g)
+    V = torch.randn(2, N, d, generator=g)
+    return Q.bfloat16(), K.bfloat16(), V.bfloat16()
+
+
+def test_route_picks_the_mask_that_matches_the_attention_structure():
+    F, Hs, Ws, d = 6, 6, 8, 64
+    q, k, v = _structured_heads(F, Hs, Ws, d, 3)
+    gg = geom(F, Hs, Ws, 1, 2, 64)
+    rows = list(range(0, F * Hs * Ws, 7))
+    flags, err = oracle.route(bits(q), bits(k), bits(v), gg, rows)
+    assert flags.tolist() == [0, 1]
+    assert err[0, 0] < err[0, 1] and err[1, 1] < err[1, 0]
+
+
+def test_route_windows_covering_everything_give_zero_deviation():
+    F, Hs, Ws, d = 5, 7, 9, 64
+    S, N = Hs * Ws, F * Hs * Ws
+    q, k, v = W.qkv(W.SMALL, H=1, N=N, d=d, seed=4)
+    rows = [0, 17, N - 1]
+    _, err = oracle.route(bits(q), bits(k), bits(v), geom(F, Hs, Ws, 1, S - 1, 64), rows)
+    assert err[0, 1] == 0.0 and err[0, 0] > 0.0       # temporal mask = dense
+    flags, err = oracle.route(bits(q), bits(k), bits(v), geom(F, Hs, Ws, F - 1, 3, 64), rows)
+    assert err[0, 0] == 0.0 and err[0, 1] > 0.0 and flags[0] == 0  # spatial mask = dense
