@@ -12,11 +12,12 @@
 // iff its temporal deviation is strictly smaller (ties stay spatial).  Masks are
 // evaluated in (F,H,W) order (routing runs before the permutation).
 //
-// Kernel: one CTA of 128 threads per (head, block of kRows sampled rows).  Pass
+// Kernel: one CTA of 512 threads per (head, block of kRows sampled rows).  Pass
 // 1 finds each row's maximum logit under the three masks; pass 2 forms the
-// exponentials of a 128-key chunk (one key per thread) in shared memory and
-// accumulates the three outputs per channel (one channel per thread), reading
-// each V row of the chunk coalesced.  fp32 throughout, exact two-pass softmax.
+// exponentials of a 512-key chunk (one key per thread) in shared memory and
+// accumulates the three outputs per channel (128 channels x 4 key groups),
+// reading each V row of the chunk coalesced.  fp32 throughout, exact two-pass
+// softmax.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -28,8 +29,9 @@
 namespace bss {
 namespace {
 
-constexpr int kRows = 4;      // sampled rows per CTA
-constexpr int kThreads = 128;  // keys per chunk in pass 1/2, channels in the accumulation
+constexpr int kRows = 4;       // sampled rows per CTA
+constexpr int kThreads = 512;  // keys per chunk in passes 1 and 2
+constexpr int kGroups = 4;     // key groups per channel in the accumulation (kThreads / 128)
 
 struct RouteArgs {
     const __nv_bfloat16* Q;
@@ -169,10 +171,11 @@ __global__ void __launch_bounds__(kThreads) route_kernel(const RouteArgs a) {
                 for (int m = 0; m < 3; ++m) ps[m][r][t] = 0.0f;
         }
         __syncthreads();
-        if (t < D) {
+        const int ch = t % 128, grp = t / 128;
+        if (ch < D) {
             const int kn = a.N - k0 < kThreads ? a.N - k0 : kThreads;
-            for (int j = 0; j < kn; ++j) {
-                const float v = __bfloat162float(a.V[head + static_cast<size_t>(k0 + j) * D + t]);
+            for (int j = grp; j < kn; j += kGroups) {
+                const float v = __bfloat162float(a.V[head + static_cast<size_t>(k0 + j) * D + ch]);
 #pragma unroll
                 for (int m = 0; m < 3; ++m)
 #pragma unroll
@@ -182,6 +185,19 @@ __global__ void __launch_bounds__(kThreads) route_kernel(const RouteArgs a) {
         __syncthreads();
     }
     block_reduce<3 * kRows, false>(l, red);
+    // combine the key groups' partial outputs per channel
+    __shared__ float og[kGroups][3 * kRows][128];
+    {
+        const int ch = t % 128, grp = t / 128;
+#pragma unroll
+        for (int i = 0; i < 3 * kRows; ++i) og[grp][i][ch] = o[i];
+        __syncthreads();
+        if (grp == 0) {
+#pragma unroll
+            for (int i = 0; i < 3 * kRows; ++i) o[i] = og[0][i][ch] + og[1][i][ch] + og[2][i][ch] + og[3][i][ch];
+        }
+        __syncthreads();
+    }
 
     // ---- deviations from the dense output, summed over rows and channels
     float dev[2] = {0.0f, 0.0f};
