@@ -332,3 +332,53 @@ def attention_step(Q, K, V, O, tile_map: TileMap, head_is_temporal, Qp, Kp, Vp, 
     else:
         sparse_attention(Q, K, V, O, tile_map, head_is_temporal, lse, stream=stream)
     return O
+
+
+def attention_step_host(hQ, hK, hV, hO, tile_map: TileMap, head_is_temporal, workspace, heads_per_chunk: int = 2,
+                        stream=None):
+    """The per-layer path from pinned HOST buffers: H2D copies of Q, K, V, the
+    permute -> block-sparse attention -> unpermute path, and the D2H copy of O,
+    pipelined over groups of heads so that copies of one group overlap the
+    kernels of another (heads are independent).
+
+    hQ, hK, hV, hO: pinned CPU bf16 [H][N][d]; head_is_temporal: device uint8[H];
+    workspace: dict from ``step_workspace`` (device buffers, reused across calls).
+    All work is queued on ``stream`` (default: current) and two side streams;
+    the call returns once the D2H copy of O is queued (synchronize ``stream``)."""
+    import torch
+    H = hQ.shape[0]
+    main = torch.cuda.current_stream() if stream is None else stream
+    cs, os_ = workspace["copy_stream"], workspace["out_stream"]
+    Q, K, V, O = workspace["Q"], workspace["K"], workspace["V"], workspace["O"]
+    Qp, Kp, Vp, Op = workspace["Qp"], workspace["Kp"], workspace["Vp"], workspace["Op"]
+    cs.wait_stream(main)
+    os_.wait_stream(main)
+    for h0 in range(0, H, heads_per_chunk):
+        h1 = min(H, h0 + heads_per_chunk)
+        with torch.cuda.stream(cs):
+            for src, dst in ((hQ, Q), (hK, K), (hV, V)):
+                dst[h0:h1].copy_(src[h0:h1], non_blocking=True)
+        ready = torch.cuda.Event()
+        ready.record(cs)
+        main.wait_event(ready)
+        with torch.cuda.stream(main):
+            attention_step(Q[h0:h1], K[h0:h1], V[h0:h1], O[h0:h1], tile_map, head_is_temporal[h0:h1],
+                           Qp[h0:h1], Kp[h0:h1], Vp[h0:h1], Op[h0:h1], stream=main)
+        done = torch.cuda.Event()
+        done.record(main)
+        os_.wait_event(done)
+        with torch.cuda.stream(os_):
+            hO[h0:h1].copy_(O[h0:h1], non_blocking=True)
+    main.wait_stream(os_)
+    return hO
+
+
+def step_workspace(H: int, N: int, d: int, device=None):
+    """Device buffers and side streams reused by ``attention_step_host``."""
+    import torch
+    device = device or torch.device("cuda")
+    ws = {k: torch.empty(H, N, d, dtype=torch.bfloat16, device=device)
+          for k in ("Q", "K", "V", "O", "Qp", "Kp", "Vp", "Op")}
+    ws["copy_stream"] = torch.cuda.Stream(device=device)
+    ws["out_stream"] = torch.cuda.Stream(device=device)
+    return ws
