@@ -386,10 +386,26 @@ def variants(bss, torch, W, w, H, Q, K, V, dev, peaks, flags):
         ms_perm = _time(torch, with_perm)
         ms_attn = _time(torch, lambda: bss.sparse_attention(Qp, Kp, Vp, Op, tm1, ones))
         ms_noperm = _time(torch, lambda: bss.sparse_attention(Q, K, V, O, tm0, ones))
+        ms_fused = _time(torch, lambda: bss.sparse_attention_fused(Q, K, V, O, tm1, ones))
         out["temporal_heads"] = {
             "with_permutation_ms": ms_perm, "attention_only_ms": ms_attn, "in_kernel_indexing_ms": ms_noperm,
+            "fused_permutation_ms": ms_fused,
             "tflops_attention": fl_ / ms_attn / 1e9, "tflops_in_kernel_indexing": fl_ / ms_noperm / 1e9,
+            "tflops_fused_permutation": fl_ / ms_fused / 1e9,
             "tiles_permuted": tm1.stats(1), "tiles_in_kernel_indexing": tm0.stats(1)}
+        # the mixed-flag step as one launch: permutation fused into the attention kernel
+        fl_mixed = torch.tensor(flags, dtype=torch.uint8, device=dev)
+        mixed_fl = 4.0 * w.d * sum(tm1.stats(f)["retained_pairs"] for f in flags)
+
+        def explicit_step():
+            bss.attention_step(Q, K, V, O, tm1, fl_mixed, Qp, Kp, Vp, Op)
+
+        ms_exp = _time(torch, explicit_step)
+        ms_fst = _time(torch, lambda: bss.sparse_attention_fused(Q, K, V, O, tm1, fl_mixed))
+        out["mixed_step_fused_permutation"] = {
+            "explicit_step_ms": ms_exp, "fused_ms": ms_fst, "tflops_fused": mixed_fl / ms_fst / 1e9,
+            "speedup": ms_exp / ms_fst,
+            "note": "permute QKV -> attention -> unpermute O (5 launches) vs one launch reading (F,H,W) memory"}
         rows = torch.tensor(W.sample_rows(w.N, 64, seed=w.index), dtype=torch.int32, device=dev)
         rflags = torch.empty(H, dtype=torch.uint8, device=dev)
         rerr = torch.empty(H, 2, dtype=torch.float32, device=dev)

@@ -74,7 +74,8 @@ class MaskParams:
 EXPORTED = ("bss_build_tile_map", "bss_tile_map_stats", "bss_tile_map_dims", "bss_tile_map_copy_csr",
             "bss_destroy_tile_map", "bss_permute", "bss_sparse_attention", "bss_dense_attention",
             "bss_get_device_status", "bss_status_string", "bss_last_error_message", "bss_version",
-            "bss_diag_mma_tile", "bss_build_tile_map_csr_noalloc", "bss_route_heads")
+            "bss_diag_mma_tile", "bss_build_tile_map_csr_noalloc", "bss_route_heads",
+            "bss_sparse_attention_fused")
 
 
 def load(path: str | None = None):
@@ -102,6 +103,8 @@ def load(path: str | None = None):
     lib.bss_permute.restype = st
     lib.bss_sparse_attention.argtypes = [p, p, p, p, p, p, p, i32, ctypes.c_float, p]
     lib.bss_sparse_attention.restype = st
+    lib.bss_sparse_attention_fused.argtypes = [p, p, p, p, p, p, p, i32, ctypes.c_float, p]
+    lib.bss_sparse_attention_fused.restype = st
     lib.bss_dense_attention.argtypes = [p, p, p, p, p, i32, i32, i32, ctypes.c_float, p]
     lib.bss_dense_attention.restype = st
     lib.bss_get_device_status.argtypes = [p]
@@ -252,6 +255,21 @@ def sparse_attention(Q, K, V, O, tile_map: TileMap, head_is_temporal=None, lse=N
     _dev_tensor(lse, "lse", torch.float32)
     _check(load().bss_sparse_attention(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(lse), tile_map.handle,
                                        _ptr(head_is_temporal), Q.shape[0], float(softmax_scale), _stream(stream)))
+    return O
+
+
+def sparse_attention_fused(Q, K, V, O, tile_map: TileMap, head_is_temporal=None, lse=None,
+                           softmax_scale: float = 0.0, stream=None):
+    """O <- block-sparse attention of [H][N][d] bf16 Q, K, V, all heads in (F,H,W)
+    order: the temporal heads' permutation is applied inside the kernel."""
+    import torch
+    for t, n in ((Q, "Q"), (K, "K"), (V, "V"), (O, "O")):
+        _dev_tensor(t, n, torch.bfloat16)
+    _dev_tensor(head_is_temporal, "head_is_temporal", torch.uint8)
+    _dev_tensor(lse, "lse", torch.float32)
+    _check(load().bss_sparse_attention_fused(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(lse), tile_map.handle,
+                                             _ptr(head_is_temporal), Q.shape[0], float(softmax_scale),
+                                             _stream(stream)))
     return O
 
 

@@ -104,29 +104,53 @@ int num_sms() {
     return g_num_sms[dev];
 }
 
+namespace {
+bss_status encode_fn(PFN_cuTensorMapEncodeTiled_v12000* out) {
+    std::lock_guard<std::mutex> lk(g_mutex);
+    if (g_encode == nullptr) {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || fn == nullptr)
+            return set_error(BSS_ERR_CUDA, "cuTensorMapEncodeTiled entry point not available");
+        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    *out = g_encode;
+    return BSS_OK;
+}
+}  // namespace
+
 bss_status encode_tmap_3d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint64_t heads,
                           uint64_t row_stride_bytes, uint64_t head_stride_bytes, uint32_t box_inner,
                           uint32_t box_rows) {
-    {
-        std::lock_guard<std::mutex> lk(g_mutex);
-        if (g_encode == nullptr) {
-            void* fn = nullptr;
-            cudaDriverEntryPointQueryResult q;
-            if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
-                    cudaSuccess ||
-                q != cudaDriverEntryPointSuccess || fn == nullptr)
-                return set_error(BSS_ERR_CUDA, "cuTensorMapEncodeTiled entry point not available");
-            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-        }
-    }
+    PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
+    bss_status st = encode_fn(&enc);
+    if (st != BSS_OK) return st;
     cuuint64_t dims[3] = {inner, rows, heads};
     cuuint64_t strides[2] = {row_stride_bytes, head_stride_bytes};
     cuuint32_t box[3] = {box_inner, box_rows, 1};
     cuuint32_t estr[3] = {1, 1, 1};
-    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
-                          estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return set_error(BSS_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
+    return BSS_OK;
+}
+
+bss_status encode_tmap_rows_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows,
+                               uint64_t row_stride_bytes, uint32_t box_inner) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
+    bss_status st = encode_fn(&enc);
+    if (st != BSS_OK) return st;
+    cuuint64_t dims[2] = {inner, rows};
+    cuuint64_t strides[1] = {row_stride_bytes};
+    cuuint32_t box[2] = {box_inner, 1};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return set_error(BSS_ERR_CUDA, "cuTensorMapEncodeTiled (rows) failed (CUresult %d)", (int)r);
     return BSS_OK;
 }
 
@@ -260,9 +284,10 @@ bss_status bss_permute(const void* in, void* out, const uint8_t* head_is_tempora
                           inverse, stream);
 }
 
-bss_status bss_sparse_attention(const void* Q, const void* K, const void* V, void* O, float* lse,
-                                bss_tile_map map, const uint8_t* head_is_temporal, int32_t H, float softmax_scale,
-                                cudaStream_t stream) {
+namespace {
+bss_status sparse_attention_impl(const void* Q, const void* K, const void* V, void* O, float* lse, bss_tile_map map,
+                                 const uint8_t* head_is_temporal, int32_t H, float softmax_scale, int32_t fused,
+                                 cudaStream_t stream) {
     using namespace bss;
     t_last_error[0] = '\0';
     if (!map_is_live(map)) return set_error(BSS_ERR_INVALID_ARG, "invalid or destroyed tile map");
@@ -303,7 +328,21 @@ bss_status bss_sparse_attention(const void* Q, const void* K, const void* V, voi
         a.order[k] = map->kind[k].d_order;
     }
     a.softmax_scale = softmax_scale;
+    a.fused = fused;
     return launch_attention(a, stream);
+}
+}  // namespace
+
+bss_status bss_sparse_attention(const void* Q, const void* K, const void* V, void* O, float* lse,
+                                bss_tile_map map, const uint8_t* head_is_temporal, int32_t H, float softmax_scale,
+                                cudaStream_t stream) {
+    return sparse_attention_impl(Q, K, V, O, lse, map, head_is_temporal, H, softmax_scale, 0, stream);
+}
+
+bss_status bss_sparse_attention_fused(const void* Q, const void* K, const void* V, void* O, float* lse,
+                                      bss_tile_map map, const uint8_t* head_is_temporal, int32_t H,
+                                      float softmax_scale, cudaStream_t stream) {
+    return sparse_attention_impl(Q, K, V, O, lse, map, head_is_temporal, H, softmax_scale, 1, stream);
 }
 
 bss_status bss_dense_attention(const void* Q, const void* K, const void* V, void* O, float* lse, int32_t H,

@@ -57,6 +57,8 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale when max grows
 
 struct AttnArgs {
     CUtensorMap tm_q, tm_k, tm_v, tm_o, tm_ks, tm_vs;
+    CUtensorMap tm_qg, tm_kg, tm_vg;  // [H*N] rows views, one-row boxes (fused permutation)
+    uint16_t* o_rows;                 // O as bf16 bits (fused permutation: row-wise stores)
     const int32_t* row_ptr[2];
     const int32_t* entries[2];
     const int32_t* order[2];
@@ -64,9 +66,28 @@ struct AttnArgs {
     float* lse;
     int* status;
     int32_t code[2];
-    int32_t H, N, nq, F, S, S_pad, wf, ws, dense, nkv_dense;
+    int32_t H, N, nq, F, S, S_pad, wf, ws, dense, nkv_dense, fused;
     float scale_log2;
 };
+
+static_assert(kHalf == 128 && kBKV == 128, "the gather producer maps 4 rows to each of 32 lanes");
+
+// Fused permutation: row of the (F,H,W)-ordered tensor (in the [H*N] rows view)
+// holding (H,W,F)-permuted rows p0 .. p0+3 of head h, p = s*F + f -> f*S + s.
+// Rows past the end of the sequence repeat the last row: they are padding
+// (query rows never stored, key columns masked with P = 0).
+__device__ __forceinline__ void fused_rows4(const AttnArgs& a, int h, int p0, int (&r)[4]) {
+    int s = p0 / a.F, f = p0 - s * a.F;
+    const int base = h * a.N;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        r[i] = p0 + i < a.N ? base + f * a.S + s : base + a.N - 1;
+        if (++f == a.F) {
+            f = 0;
+            ++s;
+        }
+    }
+}
 
 template <int D>
 struct Smem {
@@ -232,7 +253,84 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 0) {
+    // temporal head whose (H,W,F) permutation is applied by the loads and stores
+    const bool gather = args.fused != 0 && code == MASK_TEMPORAL_VIRT;
+
+    if (warp == 0 && gather) {
+        // =========================== TMA producer, fused permutation: each lane
+        // gathers 4 permuted rows of every 128-row tile (tile::gather4 per 64-column
+        // chunk); frame-0 keys of the sink segment are contiguous, one box load.
+        if (lane == 0) {
+            tma_prefetch_desc(&args.tm_qg);
+            tma_prefetch_desc(&args.tm_kg);
+            tma_prefetch_desc(&args.tm_vg);
+            mbar_arrive_expect_tx(bar_q, 2 * L::kTile);
+        }
+        __syncwarp();
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            int r4[4];
+            fused_rows4(args, h, qt * kBQ + hh * kHalf + 4 * lane, r4);
+#pragma unroll
+            for (int c = 0; c < kChunks; ++c)
+                tma_gather4_2d(sQ + hh * L::kTile + c * kChunkBytesSw128 + lane * 512, &args.tm_qg, c * 64, r4[0],
+                               r4[1], r4[2], r4[3], bar_q);
+        }
+        bool ok = true;
+        int jk = 0, jv = 0;
+        for (; jv < n; ++jv) {
+            const int st = jv % kStages;
+            const uint32_t e = entry_at(args, ents, jv);
+            const int col0 = static_cast<int>(e & BSS_TILE_INDEX_MASK) * kBKV;
+            const bool sink = col0 < args.S_pad;
+            int r4[4] = {0, 0, 0, 0};
+            if (!sink) fused_rows4(args, h, col0 - args.S_pad + 4 * lane, r4);
+            if (jv >= kStages)
+                ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_k_empty + st, ((jv / kStages) - 1) & 1, status));
+            if (!ok) break;
+            if (lane == 0) mbar_arrive_expect_tx(bar_k_full + st, L::kTile);
+            __syncwarp();
+            if (sink) {
+                if (lane == 0) {
+#pragma unroll
+                    for (int c = 0; c < kChunks; ++c)
+                        tma_load_3d(sK + st * L::kTile + c * kChunkBytesSw128, &args.tm_ks, c * 64, col0, h,
+                                    bar_k_full + st);
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < kChunks; ++c)
+                    tma_gather4_2d(sK + st * L::kTile + c * kChunkBytesSw128 + lane * 512, &args.tm_kg, c * 64, r4[0],
+                                   r4[1], r4[2], r4[3], bar_k_full + st);
+            }
+            jk = jv + 1;
+            if (jv >= kStages)
+                ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_v_empty + st, ((jv / kStages) - 1) & 1, status));
+            if (!ok) break;
+            if (lane == 0) mbar_arrive_expect_tx(bar_v_full + st, L::kTile);
+            __syncwarp();
+            if (sink) {
+                if (lane == 0) {
+#pragma unroll
+                    for (int c = 0; c < kChunks; ++c)
+                        tma_load_3d(sV + st * L::kTile + c * kChunkBytesSw128, &args.tm_vs, c * 64, col0, h,
+                                    bar_v_full + st);
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < kChunks; ++c)
+                    tma_gather4_2d(sV + st * L::kTile + c * kChunkBytesSw128 + lane * 512, &args.tm_vg, c * 64, r4[0],
+                                   r4[1], r4[2], r4[3], bar_v_full + st);
+            }
+        }
+        if (lane == 0) {
+            mbar_wait(bar_q, 0, status);
+            for (int jj = (jk - kStages > 0 ? jk - kStages : 0); jj < jk; ++jj)
+                mbar_wait(bar_k_full + jj % kStages, (jj / kStages) & 1, status);
+            for (int jj = (jv - kStages > 0 ? jv - kStages : 0); jj < jv; ++jj)
+                mbar_wait(bar_v_full + jj % kStages, (jj / kStages) & 1, status);
+        }
+    } else if (warp == 0) {
         // =========================== TMA producer
         if (lane == 0) {
             tma_prefetch_desc(&args.tm_q);
@@ -369,6 +467,9 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         const uint32_t t_o = tmem + lane_base + kColO + hf * 128;
         const int q = qt * kBQ + hf * kHalf + r;
         const RowPred rp = row_pred(args, code, q);
+        // output row of this query: its own index, or its (F,H,W) position when the
+        // kernel applies the permutation
+        const int orow = (gather && q < args.N) ? (q % args.F) * args.S + q / args.F : q;
         const float c = args.scale_log2;
         float m = -INFINITY;
         float l = 0.0f;
@@ -535,24 +636,34 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
 #pragma unroll
                 for (int i = 0; i < 16; ++i)
                     w[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
-                // columns [32cc, 32cc+32) = 16-byte units 4*(cc%2) .. +3 of 64-column chunk cc/2
-                uint8_t* chunk = stage + (cc >> 1) * kChunkBytesSw128 + r * 128;
+                if (gather) {
+                    // fused permutation: the row goes straight to its (F,H,W) position
+                    if (q < args.N) {
+                        uint4* dst = reinterpret_cast<uint4*>(args.o_rows + (static_cast<int64_t>(h) * args.N + orow) * D) +
+                                     cc * 4;
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const int unit = (cc & 1) * 4 + u;
-                    *reinterpret_cast<uint4*>(chunk + ((unit ^ (r & 7)) << 4)) =
-                        make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+                        for (int u = 0; u < 4; ++u) dst[u] = make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+                    }
+                } else {
+                    // columns [32cc, 32cc+32) = 16-byte units 4*(cc%2) .. +3 of 64-column chunk cc/2
+                    uint8_t* chunk = stage + (cc >> 1) * kChunkBytesSw128 + r * 128;
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int unit = (cc & 1) * 4 + u;
+                        *reinterpret_cast<uint4*>(chunk + ((unit ^ (r & 7)) << 4)) =
+                            make_uint4(w[4 * u], w[4 * u + 1], w[4 * u + 2], w[4 * u + 3]);
+                    }
                 }
             }
             if (args.lse != nullptr && q < args.N) {
                 const float lse = l > 0.0f ? (m + log2f(l)) * 0.69314718055994530942f : -INFINITY;
-                args.lse[static_cast<int64_t>(h) * args.N + q] = lse;
+                args.lse[static_cast<int64_t>(h) * args.N + orow] = lse;
             }
             fence_proxy_async_smem();
         }
         named_barrier_sync(1 + hf, 128);
         const int row0 = qt * kBQ + hf * kHalf;
-        if (r == 0 && ok && row0 < args.N) {
+        if (r == 0 && ok && row0 < args.N && !gather) {
 #pragma unroll
             for (int cc = 0; cc < kChunks; ++cc)
                 tma_store_3d(&args.tm_o, stage + cc * kChunkBytesSw128, cc * 64, row0, h);
@@ -581,9 +692,20 @@ bss_status launch_d(const AttnLaunch& a, cudaStream_t stream) {
     if ((st = encode_tmap_3d(&args.tm_k, a.K, a.d, a.N, a.H, rs, hs, 64, kBKV)) != BSS_OK) return st;
     if ((st = encode_tmap_3d(&args.tm_v, a.V, a.d, a.N, a.H, rs, hs, 64, kBKV)) != BSS_OK) return st;
     if ((st = encode_tmap_3d(&args.tm_o, a.O, a.d, a.N, a.H, rs, hs, 64, kHalf)) != BSS_OK) return st;
-    // frame-0 keys of a (H,W,F)-permuted head: row s of this view is permuted row s*F
-    if ((st = encode_tmap_3d(&args.tm_ks, a.K, a.d, a.S, a.H, rs * a.F, hs, 64, kBKV)) != BSS_OK) return st;
-    if ((st = encode_tmap_3d(&args.tm_vs, a.V, a.d, a.S, a.H, rs * a.F, hs, 64, kBKV)) != BSS_OK) return st;
+    // frame-0 keys of a temporal head: row s of this view is key (f = 0, s), which
+    // is permuted row s*F of a permuted tensor, or row s of an (F,H,W) tensor
+    const uint64_t sink_rs = a.fused ? rs : rs * a.F;
+    if ((st = encode_tmap_3d(&args.tm_ks, a.K, a.d, a.S, a.H, sink_rs, hs, 64, kBKV)) != BSS_OK) return st;
+    if ((st = encode_tmap_3d(&args.tm_vs, a.V, a.d, a.S, a.H, sink_rs, hs, 64, kBKV)) != BSS_OK) return st;
+    if (a.fused) {
+        const uint64_t rows = static_cast<uint64_t>(a.H) * static_cast<uint64_t>(a.N);
+        if (rows > 0x7FFFFFFFull) return set_error(BSS_ERR_UNSUPPORTED, "H*N too large for the fused permutation");
+        if ((st = encode_tmap_rows_2d(&args.tm_qg, a.Q, a.d, rows, rs, 64)) != BSS_OK) return st;
+        if ((st = encode_tmap_rows_2d(&args.tm_kg, a.K, a.d, rows, rs, 64)) != BSS_OK) return st;
+        if ((st = encode_tmap_rows_2d(&args.tm_vg, a.V, a.d, rows, rs, 64)) != BSS_OK) return st;
+    }
+    args.o_rows = static_cast<uint16_t*>(a.O);
+    args.fused = a.fused;
     for (int k = 0; k < 2; ++k) {
         args.row_ptr[k] = a.row_ptr[k];
         args.entries[k] = a.entries[k];

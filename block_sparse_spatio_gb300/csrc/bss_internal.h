@@ -65,6 +65,10 @@ struct AttnLaunch {
     const int32_t* entries[2];
     const int32_t* order[2];
     float softmax_scale;
+    // 1: Q, K, V, O and lse are in (F,H,W) token order for every head; the
+    // temporal kind's (H,W,F) permutation is applied by the kernel's loads and
+    // stores instead of separate permute passes
+    int32_t fused;
 };
 bss_status launch_attention(const AttnLaunch& a, cudaStream_t stream);
 int attention_block_q();   // query rows per attention tile (the map's BQ)
@@ -77,6 +81,9 @@ int* device_status_ptr();  // per-device status word (device address)
 bss_status encode_tmap_3d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint64_t heads,
                           uint64_t row_stride_bytes, uint64_t head_stride_bytes, uint32_t box_inner,
                           uint32_t box_rows);
+// 2-D rows view (inner x rows) with a one-row box, for tile::gather4 loads
+bss_status encode_tmap_rows_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows,
+                               uint64_t row_stride_bytes, uint32_t box_inner);
 int num_sms();
 bss_status check_mask_params(const bss_mask_params* p);  // validation shared by the entry points
 

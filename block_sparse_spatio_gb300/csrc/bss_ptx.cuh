@@ -130,6 +130,18 @@ __device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* m
         : "memory");
 }
 
+// Four rows (r0..r3, any order) of a 2-D tensor map whose box is one row high:
+// the rows land one after another at smem_dst (4 x box bytes), swizzled by
+// their shared-memory address like a tiled load of the same rows.
+__device__ __forceinline__ void tma_gather4_2d(void* smem_dst, const CUtensorMap* map, int32_t c0, int32_t r0,
+                                               int32_t r1, int32_t r2, int32_t r3, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cta.global.tile::gather4.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(smem_u32(bar))
+        : "memory");
+}
+
 // Same load multicast to every CTA of the cluster in `cta_mask`: the box lands
 // at the same shared-memory offset in each of them and completes `bar` at the
 // same offset in each.

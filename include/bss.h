@@ -166,6 +166,25 @@ bss_status bss_sparse_attention(const void* Q, const void* K, const void* V, voi
                                 bss_tile_map map, const uint8_t* head_is_temporal, int32_t H,
                                 float softmax_scale, cudaStream_t stream);
 
+/* The same attention with the token permutation fused into the kernel (blog,
+ * section "Arrange tokens for efficient temporal access": the (H,W,F) order
+ * makes a temporal head's window one contiguous band; here the kernel reads
+ * that order straight from (F,H,W) memory instead of a separate permute pass).
+ *   Q, K, V, O  device [H][N][d] bf16 in (F,H,W) token order for EVERY head
+ *               (no permute before, no unpermute after).  For heads with
+ *               head_is_temporal[h] != 0 and a map built with
+ *               temporal_permuted = 1 the kernel walks the permuted tile map
+ *               and gathers its query / key rows (row s*F + f of the permuted
+ *               order is row f*S + s of the input) with 4-row TMA gathers,
+ *               and writes each output row to its (F,H,W) position.
+ *   lse         optional device float[H][N] in (F,H,W) order.
+ * Results are bit-identical to bss_permute -> bss_sparse_attention ->
+ * inverse bss_permute of O (and of lse) with the same flags.  H*N must be
+ * below 2^31.  Errors as bss_sparse_attention. */
+bss_status bss_sparse_attention_fused(const void* Q, const void* K, const void* V, void* O, float* lse,
+                                      bss_tile_map map, const uint8_t* head_is_temporal, int32_t H,
+                                      float softmax_scale, cudaStream_t stream);
+
 /* Dense attention control (the blog's B0 dense baseline): the same kernel
  * visiting every tile, masking only padding columns of the last kv tile.
  * Q, K, V, O: device [H][N][d] bf16, d = 64 or 128; lse optional. */
