@@ -23,6 +23,7 @@ the host cores.
 from __future__ import annotations
 
 import argparse
+import datetime
 import hashlib
 import json
 import math
@@ -47,7 +48,7 @@ TRAFFIC_FILE = os.path.join(ROOT, "profiles", "attn_fwd_mixed75k_dram_traffic.tx
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=60)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="mixed_75600tok_10h_d128")
@@ -99,7 +100,7 @@ def traffic_from_profile():
 
 class ClockSampler:
     """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
-    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    QUERY = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -108,11 +109,18 @@ class ClockSampler:
         self.proc = None
         self.lines = []
         self.thread = None
+        self.t_begin = self.t_end = None
+
+    def mark_begin(self):
+        self.t_begin = datetime.datetime.now()
+
+    def mark_end(self):
+        self.t_end = datetime.datetime.now()
 
     def start(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
-                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
@@ -133,22 +141,28 @@ class ClockSampler:
             self.proc.kill()
         if self.thread:
             self.thread.join(timeout=2)
-        sm, smax, reasons = [], [], set()
+        sm, smax, power, reasons = [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for ln in self.lines:
             parts = [x.strip() for x in ln.split(",")]
             if len(parts) < 9:
                 continue
             try:
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f")
+                if self.t_begin is not None and not (self.t_begin <= ts <= self.t_end):
+                    continue  # outside the timed region
                 sm.append(float(parts[1]))
                 smax.append(float(parts[2]))
+                power.append(float(parts[3]))
             except ValueError:
                 continue
             for nm, val in zip(names, parts[5:9]):
                 if val.lower() == "active":
                     reasons.add(nm)
         return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "sm_mhz_min": min(sm) if sm else None, "power_w_max": max(power) if power else None,
+                "reasons": sorted(reasons), "samples": len(sm),
+                "window": "samples taken between the start and the end of the timed region"}
 
 
 # --------------------------------------------------------------------------- oracle (host)
@@ -274,6 +288,7 @@ def main():
     sampler = ClockSampler(local_rank)
     sampler.start()
     time.sleep(0.3)
+    sampler.mark_begin()
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
@@ -286,6 +301,7 @@ def main():
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
+    sampler.mark_end()
     clocks = sampler.stop()
     elapsed_ms = t0.elapsed_time(t1)
     if world > 1:
@@ -372,6 +388,7 @@ def variants(bss, torch, W, w, H, Q, K, V, dev, peaks, flags):
             out[name] = {"ms": ms, "tflops": fl_ / ms / 1e9, "frac_of_peak": fl_ / ms / 1e9 / peaks["bf16_tflops"],
                          "speedup_vs_dense": dense_ms / ms, "retained_fraction": s0["retained_pairs"] / w.N ** 2,
                          "tiles": s0}
+    out["tile_shape_sweep"] = tile_shape_sweep(bss, torch, w)
     ones = torch.ones(H, dtype=torch.uint8, device=dev)
     Qp, Kp, Vp, Op = (torch.empty_like(Q) for _ in range(4))
     p1 = bss.MaskParams(w.F, w.Hs, w.Ws, w.d, w.wf, w.ws, temporal_permuted=1, rounding=0)
@@ -419,10 +436,41 @@ def variants(bss, torch, W, w, H, Q, K, V, dev, peaks, flags):
     return out
 
 
+def tile_shape_sweep(bss, torch, w):
+    """Masking work against tile shape (the blog's Figure 7 axis), from the tile
+    maps of both mask kinds of this workload's exact masks: the share of executed
+    tiles that need an intra-tile mask (boundary + padding), and the executed
+    pairs (tiles x tile area) per retained pair.  The attention kernel runs the
+    256 x 128 shape; 3328 / 4864 / 1024 x 1536 are the pages' TPU shapes."""
+    rows = []
+    p = bss.MaskParams(w.F, w.Hs, w.Ws, w.d, w.wf, w.ws, temporal_permuted=1, rounding=0)
+    for bq, bkv in ((128, 64), (128, 128), (256, 64), (256, 128), (256, 256), (512, 128), (1024, 1536),
+                    (3328, 1536), (4864, 1536)):
+        s0 = torch.cuda.Event(enable_timing=True)
+        s1 = torch.cuda.Event(enable_timing=True)
+        s0.record()
+        tm = bss.build_tile_map(p, BQ=bq, BKV=bkv)
+        s1.record()
+        torch.cuda.synchronize()
+        row = {"BQ": bq, "BKV": bkv, "build_ms": s0.elapsed_time(s1)}
+        for kind, name in ((0, "spatial"), (1, "temporal")):
+            st = tm.stats(kind)
+            ex = st["full"] + st["boundary"] + st["pad"]
+            row[name] = {"executed_tiles": ex, "masked_share": (st["boundary"] + st["pad"]) / max(ex, 1),
+                         "executed_pairs_per_retained": ex * bq * bkv / st["retained_pairs"]}
+        tm.destroy()
+        rows.append(row)
+    return rows
+
+
 def e2e(bss, torch, params, tm, flags, Qd, Kd, Vd, flops, args):
-    """The same step through the public API from pinned host buffers: the H2D
-    copies of Q, K, V and the flags and the D2H copy of O are inside the timed
-    region every step; ``attention_step_host`` pipelines them over head groups."""
+    """The same step through the public API from pinned host buffers.  Every
+    step copies its Q, K, V and flags host -> device and its O device -> host;
+    ``attention_step_host`` pipelines the copies over head groups and over
+    consecutive steps (two workspace sets).  K consecutive steps are timed with
+    one pair of events on the compute stream: the side streams start after the
+    first event and the compute stream waits for the last step's D2H copy
+    before the second, so every step's copies are inside the timed region."""
     H, N, d = Qd.shape
     hq, hk, hv = (torch.empty(H, N, d, dtype=torch.bfloat16, pin_memory=True) for _ in range(3))
     ho = torch.empty(H, N, d, dtype=torch.bfloat16, pin_memory=True)
@@ -431,17 +479,28 @@ def e2e(bss, torch, params, tm, flags, Qd, Kd, Vd, flops, args):
     dev = Qd.device
     ws = bss.step_workspace(H, N, d, dev)
     fl_host = torch.tensor(flags, dtype=torch.uint8).pin_memory()
-    fl = torch.empty(H, dtype=torch.uint8, device=dev)
+    main = torch.cuda.current_stream()
+    steps = max(3, min(args.steps, 20))
 
-    def one():
-        fl.copy_(fl_host, non_blocking=True)
-        bss.attention_step_host(hq, hk, hv, ho, tm, fl, ws, heads_per_chunk=2)
+    def run(n):
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        t0.record(main)
+        ws["copy_stream"].wait_event(t0)
+        ws["out_stream"].wait_event(t0)
+        last = None
+        for _ in range(n):
+            last = bss.attention_step_host(hq, hk, hv, ho, tm, fl_host, ws, heads_per_chunk=1)
+        main.wait_event(last)
+        t1.record(main)
+        torch.cuda.synchronize()
+        return t0.elapsed_time(t1) / n
 
-    steps = max(3, min(args.steps, 10))
-    ms = _time(torch, one, reps=steps, warm=3)
-    return {"value": flops / (ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": ms,
+    run(3)
+    ms = run(steps)
+    return {"value": flops / (ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": ms, "steps": steps,
             "h2d_bytes_per_step": 3 * H * N * d * 2 + H, "d2h_bytes_per_step": H * N * d * 2,
-            "pipelining": "2-head groups: H2D, kernels and D2H of different groups overlap"}
+            "pipelining": "1-head groups within a step, two workspace sets across steps: H2D, kernels and "
+                          "D2H of different groups and steps overlap"}
 
 
 def cpu_baseline(w, Q, K, V, flags, args, flops):

@@ -352,25 +352,37 @@ def attention_step(Q, K, V, O, tile_map: TileMap, head_is_temporal, Qp, Kp, Vp, 
     return O
 
 
-def attention_step_host(hQ, hK, hV, hO, tile_map: TileMap, head_is_temporal, workspace, heads_per_chunk: int = 2,
+def attention_step_host(hQ, hK, hV, hO, tile_map: TileMap, head_is_temporal, workspace, heads_per_chunk: int = 1,
                         stream=None):
     """The per-layer path from pinned HOST buffers: H2D copies of Q, K, V, the
     permute -> block-sparse attention -> unpermute path, and the D2H copy of O,
-    pipelined over groups of heads so that copies of one group overlap the
-    kernels of another (heads are independent).
+    pipelined over groups of heads (heads are independent) on three streams.
 
-    hQ, hK, hV, hO: pinned CPU bf16 [H][N][d]; head_is_temporal: device uint8[H];
-    workspace: dict from ``step_workspace`` (device buffers, reused across calls).
-    All work is queued on ``stream`` (default: current) and two side streams;
-    the call returns once the D2H copy of O is queued (synchronize ``stream``)."""
+    hQ, hK, hV, hO: pinned CPU bf16 [H][N][d]; head_is_temporal: device uint8[H],
+    or a pinned CPU uint8[H] that is copied to the device as part of the step;
+    workspace: from ``step_workspace``.  The
+    workspace holds ``depth`` buffer sets used in turn, so the copies of one
+    call overlap the kernels of the previous call; a set is reused only after
+    the kernels and the D2H copy of its previous call are done.  Kernels run on
+    ``stream`` (default: current), copies on the workspace's two side streams.
+    Returns a CUDA event that completes when the D2H copy of O is done."""
     import torch
     H = hQ.shape[0]
     main = torch.cuda.current_stream() if stream is None else stream
     cs, os_ = workspace["copy_stream"], workspace["out_stream"]
-    Q, K, V, O = workspace["Q"], workspace["K"], workspace["V"], workspace["O"]
-    Qp, Kp, Vp, Op = workspace["Qp"], workspace["Kp"], workspace["Vp"], workspace["Op"]
-    cs.wait_stream(main)
-    os_.wait_stream(main)
+    k = workspace["next"]
+    workspace["next"] = (k + 1) % len(workspace["sets"])
+    buf = workspace["sets"][k]
+    Q, K, V, O = buf["Q"], buf["K"], buf["V"], buf["O"]
+    Qp, Kp, Vp, Op = buf["Qp"], buf["Kp"], buf["Vp"], buf["Op"]
+    free = workspace["free"][k]
+    if free is not None:
+        cs.wait_event(free)
+    flags = head_is_temporal
+    if not head_is_temporal.is_cuda:
+        flags = buf["flags"][:H]
+        with torch.cuda.stream(cs):
+            flags.copy_(head_is_temporal, non_blocking=True)
     for h0 in range(0, H, heads_per_chunk):
         h1 = min(H, h0 + heads_per_chunk)
         with torch.cuda.stream(cs):
@@ -380,23 +392,26 @@ def attention_step_host(hQ, hK, hV, hO, tile_map: TileMap, head_is_temporal, wor
         ready.record(cs)
         main.wait_event(ready)
         with torch.cuda.stream(main):
-            attention_step(Q[h0:h1], K[h0:h1], V[h0:h1], O[h0:h1], tile_map, head_is_temporal[h0:h1],
+            attention_step(Q[h0:h1], K[h0:h1], V[h0:h1], O[h0:h1], tile_map, flags[h0:h1],
                            Qp[h0:h1], Kp[h0:h1], Vp[h0:h1], Op[h0:h1], stream=main)
         done = torch.cuda.Event()
         done.record(main)
         os_.wait_event(done)
         with torch.cuda.stream(os_):
             hO[h0:h1].copy_(O[h0:h1], non_blocking=True)
-    main.wait_stream(os_)
-    return hO
+    finished = torch.cuda.Event()
+    finished.record(os_)
+    workspace["free"][k] = finished
+    return finished
 
 
-def step_workspace(H: int, N: int, d: int, device=None):
-    """Device buffers and side streams reused by ``attention_step_host``."""
+def step_workspace(H: int, N: int, d: int, device=None, depth: int = 2):
+    """Device buffer sets and side streams reused by ``attention_step_host``."""
     import torch
     device = device or torch.device("cuda")
-    ws = {k: torch.empty(H, N, d, dtype=torch.bfloat16, device=device)
-          for k in ("Q", "K", "V", "O", "Qp", "Kp", "Vp", "Op")}
-    ws["copy_stream"] = torch.cuda.Stream(device=device)
-    ws["out_stream"] = torch.cuda.Stream(device=device)
-    return ws
+    sets = [{k: torch.empty(H, N, d, dtype=torch.bfloat16, device=device)
+             for k in ("Q", "K", "V", "O", "Qp", "Kp", "Vp", "Op")} for _ in range(depth)]
+    for st in sets:
+        st["flags"] = torch.empty(H, dtype=torch.uint8, device=device)
+    return {"sets": sets, "free": [None] * depth, "next": 0,
+            "copy_stream": torch.cuda.Stream(device=device), "out_stream": torch.cuda.Stream(device=device)}

@@ -1,4 +1,5 @@
-"""The pipelined host-buffer step gives the same O as the device step."""
+"""The pipelined host-buffer step gives the same O as the device step, also when
+consecutive calls overlap (two workspace sets used in turn)."""
 import pytest
 import torch
 
@@ -7,23 +8,33 @@ import workloads as W
 
 @pytest.mark.gpu
 @pytest.mark.parametrize("hpc", [1, 2, 3])
-def test_host_step_matches_device_step(bss, hpc):
+@pytest.mark.parametrize("host_flags", [False, True])
+def test_host_steps_match_device_step(bss, hpc, host_flags):
     w = W.SMALL
     H = 5
-    q, k, v = W.qkv(w, H=H, seed=21)
     flags = torch.tensor([0, 1, 1, 0, 1], dtype=torch.uint8)
     p = bss.MaskParams(w.F, w.Hs, w.Ws, w.d, w.wf, w.ws)
     dev = torch.device("cuda")
+    calls = 3
+    inputs = [W.qkv(w, H=H, seed=21 + c) for c in range(calls)]
     with bss.build_tile_map(p) as tm:
         fl = flags.to(dev)
-        Q, K, V = (x.to(dev) for x in (q, k, v))
-        O = torch.empty_like(Q)
-        ws = [torch.empty_like(Q) for _ in range(4)]
-        bss.attention_step(Q, K, V, O, tm, fl, *ws)
-        hq, hk, hv = (x.pin_memory() for x in (q, k, v))
-        ho = torch.empty_like(q).pin_memory()
+        expect = []
+        for q, k, v in inputs:
+            Q, K, V = (x.to(dev) for x in (q, k, v))
+            O = torch.empty_like(Q)
+            ws = [torch.empty_like(Q) for _ in range(4)]
+            bss.attention_step(Q, K, V, O, tm, fl, *ws)
+            expect.append(O.cpu())
+        hosts = [tuple(x.pin_memory() for x in qkv) for qkv in inputs]
+        outs = [torch.empty_like(inputs[0][0]).pin_memory() for _ in range(calls)]
         wsp = bss.step_workspace(H, w.N, w.d, dev)
-        bss.attention_step_host(hq, hk, hv, ho, tm, fl, wsp, heads_per_chunk=hpc)
+        hfl = flags.pin_memory() if host_flags else fl
+        events = [bss.attention_step_host(*hosts[c], outs[c], tm, hfl, wsp, heads_per_chunk=hpc)
+                  for c in range(calls)]
+        for e in events:
+            e.synchronize()
         torch.cuda.synchronize()
         assert bss.get_device_status() == 0
-        assert torch.equal(ho.view(torch.int16), O.cpu().view(torch.int16))
+        for c in range(calls):
+            assert torch.equal(outs[c].view(torch.int16), expect[c].view(torch.int16)), f"call {c}"
