@@ -59,6 +59,9 @@ struct AttnArgs {
     CUtensorMap tm_q, tm_k, tm_v, tm_o, tm_ks, tm_vs;
     CUtensorMap tm_qg, tm_kg, tm_vg;  // [H*N] rows views, one-row boxes (fused permutation)
     uint16_t* o_rows;                 // O as bf16 bits (fused permutation: row-wise stores)
+    const int32_t* qmap;              // routing: token index of each query row (mask predicate)
+    float* o_f32;                     // routing: [splits][3H][Nq][D] normalised fp32 outputs
+    float* lse_f32;                   // routing: [splits][3H][Nq] natural-log LSE
     const int32_t* row_ptr[2];
     const int32_t* entries[2];
     const int32_t* order[2];
@@ -67,6 +70,7 @@ struct AttnArgs {
     int* status;
     int32_t code[2];
     int32_t H, N, nq, F, S, S_pad, wf, ws, dense, nkv_dense, fused;
+    int32_t route, Nq, splits;  // routing mode: query rows per head, kv splits
     float scale_log2;
 };
 
@@ -178,15 +182,21 @@ __device__ __forceinline__ void tile_bits(uint32_t (&bits)[4], const AttnArgs& a
     }
 }
 
-__device__ __forceinline__ uint32_t entry_at(const AttnArgs& a, const int32_t* ents, int j) {
-    if (a.dense) {
-        const uint32_t cls = (j == a.nkv_dense - 1 && (a.N % kBKV) != 0) ? BSS_CLASS_PAD : BSS_CLASS_FULL;
-        return static_cast<uint32_t>(j) | (cls << BSS_CLASS_SHIFT);
+// j-th kv tile of the work item: from the tile map, or every tile from j0 on
+// (dense control and routing: FULL, PAD for a ragged last tile; BOUNDARY for a
+// masked routing kind, whose rows are scattered sampled queries)
+template <bool ROUTE>
+__device__ __forceinline__ uint32_t entry_at(const AttnArgs& a, const int32_t* ents, int j, int code, int j0) {
+    if (ROUTE || a.dense) {
+        const int t = j0 + j;
+        uint32_t cls = (t == a.nkv_dense - 1 && (a.N % kBKV) != 0) ? BSS_CLASS_PAD : BSS_CLASS_FULL;
+        if (code != MASK_DENSE) cls = BSS_CLASS_BOUNDARY;
+        return static_cast<uint32_t>(t) | (cls << BSS_CLASS_SHIFT);
     }
     return static_cast<uint32_t>(__ldg(ents + j));
 }
 
-template <int D>
+template <int D, bool ROUTE>
 __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_constant__ AttnArgs args) {
     using L = Smem<D>;
     constexpr int kChunks = D / 64;  // 64-column (128-byte) swizzle atoms per row
@@ -212,23 +222,39 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     const int lane = threadIdx.x & 31;
     int* status = args.status;
 
-    // ---- work item: (head, q tile); heads in order, q tiles longest first
+    // ---- work item: (head, q tile); heads in order, q tiles longest first.
+    // Routing: (output head vh = mask * H + head, q tile, kv split), masks dense /
+    // spatial / temporal in (F,H,W) order, every kv tile of the split.
     const int item = blockIdx.x;
-    const int h = item / args.nq;
-    const int local = item - h * args.nq;
-    int kind = 0;
-    if (!args.dense && args.flags != nullptr) kind = args.flags[h] ? 1 : 0;
-    const int code = args.dense ? static_cast<int>(MASK_DENSE) : args.code[kind];
+    int h, vh = 0, split = 0, j0 = 0, code;
     int qt, n;
     const int32_t* ents = nullptr;
-    if (args.dense) {
-        qt = local;
-        n = args.nkv_dense;
+    if constexpr (ROUTE) {
+        vh = item / (args.nq * args.splits);
+        const int rem = item - vh * args.nq * args.splits;
+        qt = rem / args.splits;
+        split = rem - qt * args.splits;
+        const int mk = vh / args.H;
+        h = vh - mk * args.H;
+        code = mk == 0 ? static_cast<int>(MASK_DENSE) : (mk == 1 ? static_cast<int>(MASK_SPATIAL)
+                                                                  : static_cast<int>(MASK_TEMPORAL_FHW));
+        j0 = static_cast<int>(static_cast<int64_t>(split) * args.nkv_dense / args.splits);
+        n = static_cast<int>(static_cast<int64_t>(split + 1) * args.nkv_dense / args.splits) - j0;
     } else {
-        qt = __ldg(args.order[kind] + local);
-        const int rb = __ldg(args.row_ptr[kind] + qt);
-        n = __ldg(args.row_ptr[kind] + qt + 1) - rb;
-        ents = args.entries[kind] + rb;
+        h = item / args.nq;
+        const int local = item - h * args.nq;
+        int kind = 0;
+        if (!args.dense && args.flags != nullptr) kind = args.flags[h] ? 1 : 0;
+        code = args.dense ? static_cast<int>(MASK_DENSE) : args.code[kind];
+        if (args.dense) {
+            qt = local;
+            n = args.nkv_dense;
+        } else {
+            qt = __ldg(args.order[kind] + local);
+            const int rb = __ldg(args.row_ptr[kind] + qt);
+            n = __ldg(args.row_ptr[kind] + qt + 1) - rb;
+            ents = args.entries[kind] + rb;
+        }
     }
 
     if (threadIdx.x == 0) {
@@ -254,7 +280,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
     const uint32_t tmem = *tmem_slot;
 
     // temporal head whose (H,W,F) permutation is applied by the loads and stores
-    const bool gather = args.fused != 0 && code == MASK_TEMPORAL_VIRT;
+    const bool gather = !ROUTE && args.fused != 0 && code == MASK_TEMPORAL_VIRT;
 
     if (warp == 0 && gather) {
         // =========================== TMA producer, fused permutation: each lane
@@ -280,7 +306,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         int jk = 0, jv = 0;
         for (; jv < n; ++jv) {
             const int st = jv % kStages;
-            const uint32_t e = entry_at(args, ents, jv);
+            const uint32_t e = entry_at<ROUTE>(args, ents, jv, code, j0);
             const int col0 = static_cast<int>(e & BSS_TILE_INDEX_MASK) * kBKV;
             const bool sink = col0 < args.S_pad;
             int r4[4] = {0, 0, 0, 0};
@@ -347,7 +373,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             int jk = 0, jv = 0;  // K tiles and V tiles issued
             for (; jv < n; ++jv) {
                 const int st = jv % kStages;
-                const uint32_t e = entry_at(args, ents, jv);
+                const uint32_t e = entry_at<ROUTE>(args, ents, jv, code, j0);
                 const int col0 = static_cast<int>(e & BSS_TILE_INDEX_MASK) * kBKV;
                 const CUtensorMap* mk = &args.tm_k;
                 const CUtensorMap* mv = &args.tm_v;
@@ -466,7 +492,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         const uint32_t t_s = tmem + lane_base + kColS + hf * 128;
         const uint32_t t_o = tmem + lane_base + kColO + hf * 128;
         const int q = qt * kBQ + hf * kHalf + r;
-        const RowPred rp = row_pred(args, code, q);
+        // mask predicate row: the query itself, or (routing) the sampled token
+        int qo = q;
+        if constexpr (ROUTE) {
+            qo = __ldg(args.qmap + (q < args.Nq ? q : args.Nq - 1));
+            qo = qo < 0 ? 0 : (qo >= args.N ? args.N - 1 : qo);
+        }
+        const RowPred rp = row_pred(args, code, qo);
         // output row of this query: its own index, or its (F,H,W) position when the
         // kernel applies the permutation
         const int orow = (gather && q < args.N) ? (q % args.F) * args.S + q / args.F : q;
@@ -475,7 +507,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         float l = 0.0f;
         bool ok = true;
         for (int j = 0; j < n; ++j) {
-            const uint32_t e = entry_at(args, ents, j);
+            const uint32_t e = entry_at<ROUTE>(args, ents, j, code, j0);
             const int cls = static_cast<int>(e >> BSS_CLASS_SHIFT);
             const int c0 = static_cast<int>(e & BSS_TILE_INDEX_MASK) * kBKV;
             ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_s_full + hf, j & 1, status));
@@ -636,7 +668,20 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
 #pragma unroll
                 for (int i = 0; i < 16; ++i)
                     w[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
-                if (gather) {
+                if constexpr (ROUTE) {
+                    // routing: normalised fp32 row of this split
+                    if (q < args.Nq) {
+                        float4* dst = reinterpret_cast<float4*>(
+                                          args.o_f32 +
+                                          ((static_cast<int64_t>(split) * 3 * args.H + vh) * args.Nq + q) * D) +
+                                      cc * 8;
+#pragma unroll
+                        for (int u = 0; u < 8; ++u)
+                            dst[u] = make_float4(__uint_as_float(o[4 * u]) * inv_l, __uint_as_float(o[4 * u + 1]) * inv_l,
+                                                 __uint_as_float(o[4 * u + 2]) * inv_l,
+                                                 __uint_as_float(o[4 * u + 3]) * inv_l);
+                    }
+                } else if (gather) {
                     // fused permutation: the row goes straight to its (F,H,W) position
                     if (q < args.N) {
                         uint4* dst = reinterpret_cast<uint4*>(args.o_rows + (static_cast<int64_t>(h) * args.N + orow) * D) +
@@ -655,7 +700,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                     }
                 }
             }
-            if (args.lse != nullptr && q < args.N) {
+            if constexpr (ROUTE) {
+                if (q < args.Nq) {
+                    const float lse = l > 0.0f ? (m + log2f(l)) * 0.69314718055994530942f : -INFINITY;
+                    args.lse_f32[(static_cast<int64_t>(split) * 3 * args.H + vh) * args.Nq + q] = lse;
+                }
+            } else if (args.lse != nullptr && q < args.N) {
                 const float lse = l > 0.0f ? (m + log2f(l)) * 0.69314718055994530942f : -INFINITY;
                 args.lse[static_cast<int64_t>(h) * args.N + orow] = lse;
             }
@@ -663,7 +713,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         }
         named_barrier_sync(1 + hf, 128);
         const int row0 = qt * kBQ + hf * kHalf;
-        if (r == 0 && ok && row0 < args.N && !gather) {
+        if (r == 0 && ok && row0 < args.N && !gather && !ROUTE) {
 #pragma unroll
             for (int cc = 0; cc < kChunks; ++cc)
                 tma_store_3d(&args.tm_o, stage + cc * kChunkBytesSw128, cc * 64, row0, h);
@@ -688,10 +738,14 @@ bss_status launch_d(const AttnLaunch& a, cudaStream_t stream) {
     const uint64_t rs = static_cast<uint64_t>(a.d) * 2;
     const uint64_t hs = rs * static_cast<uint64_t>(a.N);
     bss_status st;
-    if ((st = encode_tmap_3d(&args.tm_q, a.Q, a.d, a.N, a.H, rs, hs, 64, kHalf)) != BSS_OK) return st;
+    // query rows per head: N, or the sampled rows in routing mode
+    const int64_t nq_rows = a.route ? a.Nq : a.N;
+    if ((st = encode_tmap_3d(&args.tm_q, a.Q, a.d, nq_rows, a.H, rs, rs * nq_rows, 64, kHalf)) != BSS_OK) return st;
     if ((st = encode_tmap_3d(&args.tm_k, a.K, a.d, a.N, a.H, rs, hs, 64, kBKV)) != BSS_OK) return st;
     if ((st = encode_tmap_3d(&args.tm_v, a.V, a.d, a.N, a.H, rs, hs, 64, kBKV)) != BSS_OK) return st;
-    if ((st = encode_tmap_3d(&args.tm_o, a.O, a.d, a.N, a.H, rs, hs, 64, kHalf)) != BSS_OK) return st;
+    if ((st = encode_tmap_3d(&args.tm_o, a.route ? a.Q : a.O, a.d, nq_rows, a.H, rs, rs * nq_rows, 64, kHalf)) !=
+        BSS_OK)
+        return st;
     // frame-0 keys of a temporal head: row s of this view is key (f = 0, s), which
     // is permuted row s*F of a permuted tensor, or row s of an (F,H,W) tensor
     const uint64_t sink_rs = a.fused ? rs : rs * a.F;
@@ -706,6 +760,12 @@ bss_status launch_d(const AttnLaunch& a, cudaStream_t stream) {
     }
     args.o_rows = static_cast<uint16_t*>(a.O);
     args.fused = a.fused;
+    args.route = a.route;
+    args.qmap = a.qmap;
+    args.o_f32 = a.o_f32;
+    args.lse_f32 = a.lse_f32;
+    args.Nq = a.Nq;
+    args.splits = a.route ? a.splits : 1;
     for (int k = 0; k < 2; ++k) {
         args.row_ptr[k] = a.row_ptr[k];
         args.entries[k] = a.entries[k];
@@ -730,13 +790,13 @@ bss_status launch_d(const AttnLaunch& a, cudaStream_t stream) {
     args.scale_log2 = scale * 1.4426950408889634f;
 
     const uint32_t smem = Smem<D>::kAlloc;
-    cudaError_t e = cudaFuncSetAttribute(attn_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+    auto kernel = a.route ? attn_fwd_kernel<D, true> : attn_fwd_kernel<D, false>;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return cuda_check(e, "cudaFuncSetAttribute(attention)");
-    const int64_t items = static_cast<int64_t>(a.H) * a.nq;
+    const int64_t items = static_cast<int64_t>(a.H) * a.nq * (a.route ? 3 * a.splits : 1);
     if (items <= 0) return BSS_OK;
     if (items > 0x7FFFFFFF) return set_error(BSS_ERR_UNSUPPORTED, "too many work items");
-    attn_fwd_kernel<D><<<static_cast<unsigned>(items), kThreads, smem, stream>>>(args);
+    kernel<<<static_cast<unsigned>(items), kThreads, smem, stream>>>(args);
     return cuda_check(cudaGetLastError(), "attention launch");
 }
 

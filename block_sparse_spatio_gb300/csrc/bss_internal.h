@@ -69,6 +69,13 @@ struct AttnLaunch {
     // temporal kind's (H,W,F) permutation is applied by the kernel's loads and
     // stores instead of separate permute passes
     int32_t fused;
+    // routing mode: 3 x H output heads (dense, spatial, temporal in (F,H,W)
+    // order) over Nq sampled query rows per head whose tokens are qmap[r]; every
+    // kv tile, split into `splits` ranges; normalised fp32 O and LSE per split
+    int32_t route, Nq, splits;
+    const int32_t* qmap;
+    float* o_f32;
+    float* lse_f32;
 };
 bss_status launch_attention(const AttnLaunch& a, cudaStream_t stream);
 int attention_block_q();   // query rows per attention tile (the map's BQ)

@@ -197,17 +197,21 @@ bss_status bss_dense_attention(const void* Q, const void* K, const void* V, void
  * output deviates least from the dense one; Figure 8: one flag per head).
  * Reading: deviation = squared L2 distance to the dense output summed over the
  * sampled rows and channels; a head is temporal iff its temporal deviation is
- * strictly smaller.  Exact fp32 softmaxes, masks in (F,H,W) order.
+ * strictly smaller.  Masks in (F,H,W) order.  The three outputs come from the
+ * attention kernel (tensor cores; bf16 P, fp32 accumulation and output), the
+ * kv range split across CTAs and merged through the log-sum-exps.
  *   Q, K, V           device [H][N][d] bf16 in (F,H,W) order, 16-byte aligned.
- *   rows              device int32[R]: sampled query tokens (F,H,W index), the
- *                     same rows for every head; a row outside [0, N) is skipped
- *                     and recorded as BSS_ERR_INVALID_ARG in the status word.
+ *   rows              device int32[R], 1 <= R <= 65535: sampled query tokens
+ *                     ((F,H,W) index), the same rows for every head; a row
+ *                     outside [0, N) is skipped and recorded as
+ *                     BSS_ERR_INVALID_ARG in the status word.
  *   head_is_temporal  device uint8[H] output (1 = temporal).
  *   errors            device float[2 * H] output: per head the spatial and the
- *                     temporal deviation (accumulated with atomics: exact ties
- *                     may resolve either way).
- * Asynchronous on `stream`; allocates nothing.  Errors: INVALID_ARG,
- * UNSUPPORTED, CUDA. */
+ *                     temporal deviation.
+ * Asynchronous on `stream`.  Scratch of H*R*d*2 + 3*H*R*(d+1)*4*splits bytes
+ * (splits <= number of SMs / (3 * H * ceil(R / 256))) is taken from and
+ * returned to the device's stream-ordered memory pool (cudaMallocAsync).
+ * Errors: INVALID_ARG, UNSUPPORTED, CUDA. */
 bss_status bss_route_heads(const void* Q, const void* K, const void* V, int32_t H, const bss_mask_params* params,
                            const int32_t* rows, int32_t R, uint8_t* head_is_temporal, float* errors,
                            cudaStream_t stream);
