@@ -187,13 +187,18 @@ __device__ __forceinline__ void tile_bits(uint32_t (&bits)[4], const AttnArgs& a
 // masked routing kind, whose rows are scattered sampled queries)
 template <bool ROUTE>
 __device__ __forceinline__ uint32_t entry_at(const AttnArgs& a, const int32_t* ents, int j, int code, int j0) {
-    if (ROUTE || a.dense) {
+    if constexpr (ROUTE) {
         const int t = j0 + j;
         uint32_t cls = (t == a.nkv_dense - 1 && (a.N % kBKV) != 0) ? BSS_CLASS_PAD : BSS_CLASS_FULL;
         if (code != MASK_DENSE) cls = BSS_CLASS_BOUNDARY;
         return static_cast<uint32_t>(t) | (cls << BSS_CLASS_SHIFT);
+    } else {
+        if (a.dense) {
+            const uint32_t cls = (j == a.nkv_dense - 1 && (a.N % kBKV) != 0) ? BSS_CLASS_PAD : BSS_CLASS_FULL;
+            return static_cast<uint32_t>(j) | (cls << BSS_CLASS_SHIFT);
+        }
+        return static_cast<uint32_t>(__ldg(ents + j));
     }
-    return static_cast<uint32_t>(__ldg(ents + j));
 }
 
 template <int D, bool ROUTE>
