@@ -63,6 +63,28 @@ def dist_env():
             int(os.environ.get("WORLD_SIZE", "1")))
 
 
+# ---- replicas: every rank runs its own batch, no data exchange (weak scaling)
+def replica_seed(w, rank: int) -> int:
+    """Seed of rank `rank`'s synthetic batch: a different batch on every rank."""
+    return w.index + 1000 * rank
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The slowest rank's figure (the timing rule: max over ranks)."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(flops_per_rank: float, world: int, ms_per_step: float) -> float:
+    """Whole-job throughput: every rank's work over the slowest rank's time."""
+    return flops_per_rank * world / (ms_per_step * 1e-3) / 1e12
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -250,7 +272,7 @@ def main():
     H = args.heads or w.H
     flags = w.head_flags()[:H]
     # replicas: every rank runs its own batch (different seed), no data exchange
-    Q, K, V = W.qkv_device(w, dev, seed=w.index + 1000 * rank)
+    Q, K, V = W.qkv_device(w, dev, seed=replica_seed(w, rank))
     if H != w.H:
         Q, K, V = (x[:H].contiguous() for x in (Q, K, V))
     O = torch.empty_like(Q)
@@ -303,17 +325,13 @@ def main():
         dist.barrier()
     sampler.mark_end()
     clocks = sampler.stop()
-    elapsed_ms = t0.elapsed_time(t1)
-    if world > 1:
-        tt = torch.tensor([elapsed_ms], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(tt.item())
+    elapsed_ms = max_over_ranks(t0.elapsed_time(t1), world, dev)
     status = bss.get_device_status()
     if status != 0:
         raise RuntimeError(f"device status {bss.status_string(status)} in the timed region")
     ms_per_step = elapsed_ms / args.steps
     attn_ms = statistics.mean(a.elapsed_time(b) for a, b in attn_events)
-    value = flops * world / (ms_per_step * 1e-3) / 1e12
+    value = whole_job_tflops(flops, world, ms_per_step)
     attn_tflops = flops / (attn_ms * 1e-3) / 1e12
 
     line = {

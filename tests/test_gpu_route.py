@@ -47,3 +47,42 @@ def test_route_random_heads_match_oracle(bss, wl):
     np.testing.assert_allclose(err, oerr, rtol=5e-3, atol=1e-7)
     clear = np.abs(oerr[:, 0] - oerr[:, 1]) > 1e-2 * np.maximum(oerr[:, 0], oerr[:, 1])
     assert np.array_equal(flags[clear], oflags[clear])
+
+
+@pytest.mark.gpu
+def test_route_more_rows_than_one_query_tile_and_ragged_geometry(bss):
+    # 300 sampled rows span two 256-row query tiles; N = 390 is not a multiple of
+    # the 128-key tile (padding columns in the last kv tile)
+    F, Hs, Ws, d, wf, ws = 3, 10, 13, 128, 0, 20
+    N = F * Hs * Ws
+    q, k, v = W.qkv(W.SMALL, H=3, N=N, d=d, seed=31)
+    g = torch.Generator().manual_seed(7)
+    rows = torch.randint(0, N, (300,), generator=g).tolist()
+    p = bss.MaskParams(F, Hs, Ws, d, wf, ws)
+    flags, err = _run(bss, q, k, v, p, rows)
+    oflags, oerr = oracle.route(W.bf16_bits(q), W.bf16_bits(k), W.bf16_bits(v),
+                                oracle.Geometry(F, Hs, Ws, wf=wf, ws=ws), rows)
+    np.testing.assert_allclose(err, oerr, rtol=5e-3, atol=1e-7)
+    clear = np.abs(oerr[:, 0] - oerr[:, 1]) > 1e-2 * np.maximum(oerr[:, 0], oerr[:, 1])
+    assert np.array_equal(flags[clear], oflags[clear])
+
+
+@pytest.mark.gpu
+def test_route_rows_outside_the_sequence_are_skipped_and_recorded(bss):
+    wl = W.SMALL
+    q, k, v = W.qkv(wl, H=2, seed=12)
+    good = W.sample_rows(wl.N, 20, seed=6)
+    rows = good[:5] + [-3] + good[5:] + [wl.N + 4]
+    p = bss.MaskParams(wl.F, wl.Hs, wl.Ws, wl.d, wl.wf, wl.ws)
+    dev = torch.device("cuda")
+    Q, K, V = (x.to(dev) for x in (q, k, v))
+    R = torch.tensor(rows, dtype=torch.int32, device=dev)
+    flags = torch.empty(2, dtype=torch.uint8, device=dev)
+    err = torch.empty(2, 2, dtype=torch.float32, device=dev)
+    bss.route_heads(Q, K, V, p, R, flags, err)
+    torch.cuda.synchronize()
+    assert bss.status_string(bss.get_device_status()) == "BSS_ERR_INVALID_ARG"
+    assert bss.get_device_status() == 0  # reading clears the word
+    _, oerr = oracle.route(W.bf16_bits(q), W.bf16_bits(k), W.bf16_bits(v),
+                           oracle.Geometry(wl.F, wl.Hs, wl.Ws, wf=wl.wf, ws=wl.ws), good)
+    np.testing.assert_allclose(err.cpu().numpy(), oerr, rtol=5e-3, atol=1e-7)
