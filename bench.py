@@ -407,6 +407,18 @@ def variants(bss, torch, W, w, H, Q, K, V, dev, peaks, flags):
                          "speedup_vs_dense": dense_ms / ms, "retained_fraction": s0["retained_pairs"] / w.N ** 2,
                          "tiles": s0}
     out["tile_shape_sweep"] = tile_shape_sweep(bss, torch, w)
+    # latency side of the sweep: the kernel at both query-tile heights it runs
+    pe = bss.MaskParams(w.F, w.Hs, w.Ws, w.d, w.wf, w.ws, temporal_permuted=1, rounding=0)
+    zeros_ = torch.zeros(H, dtype=torch.uint8, device=dev)
+    lat = {}
+    for bq in bss.ATTN_BQ_SUPPORTED:
+        with bss.build_tile_map(pe, BQ=bq) as tmq:
+            st0 = tmq.stats(0)
+            ms = _time(torch, lambda: bss.sparse_attention(Q, K, V, O, tmq, zeros_))
+            ex = st0["full"] + st0["boundary"] + st0["pad"]
+            lat[f"BQ{bq}_BKV128"] = {"ms": ms, "tflops": 4.0 * w.d * H * st0["retained_pairs"] / ms / 1e9,
+                                     "masked_share": (st0["boundary"] + st0["pad"]) / ex}
+    out["tile_shape_latency_spatial"] = lat
     ones = torch.ones(H, dtype=torch.uint8, device=dev)
     Qp, Kp, Vp, Op = (torch.empty_like(Q) for _ in range(4))
     p1 = bss.MaskParams(w.F, w.Hs, w.Ws, w.d, w.wf, w.ws, temporal_permuted=1, rounding=0)

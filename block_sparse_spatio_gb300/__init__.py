@@ -23,7 +23,8 @@ LIB_PATH = os.path.join(HERE, "libbss.so")
 
 KIND_SPATIAL, KIND_TEMPORAL = 0, 1
 CLASS_FULL, CLASS_BOUNDARY, CLASS_PAD = 0, 1, 2
-ATTN_BQ, ATTN_BKV = 256, 128   # tile shape bss_sparse_attention requires of its map
+ATTN_BQ, ATTN_BKV = 256, 128   # default tile shape of bss_sparse_attention's map
+ATTN_BQ_SUPPORTED = (128, 256)  # query rows per tile it runs (one or two 128-row MMA halves)
 CLASS_SHIFT = 30
 TILE_INDEX_MASK = (1 << 30) - 1
 STAT_NAMES = ("full", "boundary", "pad", "skip", "retained_pairs", "exact_retained_pairs")

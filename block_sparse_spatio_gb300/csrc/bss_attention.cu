@@ -45,10 +45,13 @@
 namespace bss {
 namespace {
 
-constexpr int kBQ = 256;        // query rows per CTA (two halves of 128)
+constexpr int kBQ = 256;        // query rows per CTA of the default shape (two halves of 128)
 constexpr int kHalf = 128;      // rows per half = MMA M
 constexpr int kBKV = 128;       // key columns per tile = MMA N of S
-constexpr int kThreads = 384;
+// threads per CTA: producer, MMA and two spare warps, plus four softmax warps
+// per 128-row half
+template <int HALVES>
+constexpr int threads_for() { return 128 * (1 + HALVES); }
 constexpr int kStages = 2;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0;    // S_h at kColS + 128 h (P_h over its first 64 columns)
@@ -93,11 +96,11 @@ __device__ __forceinline__ void fused_rows4(const AttnArgs& a, int h, int p0, in
     }
 }
 
-template <int D>
+template <int D, int HALVES = 2>
 struct Smem {
     static constexpr uint32_t kTile = kHalf * D * 2;  // bytes of one 128-row bf16 tile
-    static constexpr uint32_t kQ = 0;                 // two halves
-    static constexpr uint32_t kK = 2 * kTile;
+    static constexpr uint32_t kQ = 0;                 // the q halves
+    static constexpr uint32_t kK = HALVES * kTile;
     static constexpr uint32_t kV = kK + kStages * kTile;
     static constexpr uint32_t kBar = kV + kStages * kTile;
     // q, k_full[S], v_full[S], k_empty[S], v_empty[S], s_full[2], p_full[2], o_done[2], mma_done
@@ -201,9 +204,12 @@ __device__ __forceinline__ uint32_t entry_at(const AttnArgs& a, const int32_t* e
     }
 }
 
-template <int D, bool ROUTE>
-__global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_constant__ AttnArgs args) {
-    using L = Smem<D>;
+template <int D, bool ROUTE, int HALVES>
+__global__ void __launch_bounds__(threads_for<HALVES>(), 1) attn_fwd_kernel(const __grid_constant__ AttnArgs args) {
+    static_assert(HALVES == 1 || HALVES == 2, "one or two 128-row halves per CTA");
+    static_assert(!ROUTE || HALVES == 2, "routing uses the two-half shape");
+    using L = Smem<D, HALVES>;
+    constexpr int kBQt = HALVES * kHalf;  // query rows per CTA
     constexpr int kChunks = D / 64;  // 64-column (128-byte) swizzle atoms per row
 
     extern __shared__ uint8_t smem_raw[];
@@ -295,13 +301,13 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             tma_prefetch_desc(&args.tm_qg);
             tma_prefetch_desc(&args.tm_kg);
             tma_prefetch_desc(&args.tm_vg);
-            mbar_arrive_expect_tx(bar_q, 2 * L::kTile);
+            mbar_arrive_expect_tx(bar_q, HALVES * L::kTile);
         }
         __syncwarp();
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
+        for (int hh = 0; hh < HALVES; ++hh) {
             int r4[4];
-            fused_rows4(args, h, qt * kBQ + hh * kHalf + 4 * lane, r4);
+            fused_rows4(args, h, qt * kBQt + hh * kHalf + 4 * lane, r4);
 #pragma unroll
             for (int c = 0; c < kChunks; ++c)
                 tma_gather4_2d(sQ + hh * L::kTile + c * kChunkBytesSw128 + lane * 512, &args.tm_qg, c * 64, r4[0],
@@ -367,12 +373,12 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             tma_prefetch_desc(&args.tm_q);
             tma_prefetch_desc(&args.tm_k);
             tma_prefetch_desc(&args.tm_v);
-            mbar_arrive_expect_tx(bar_q, 2 * L::kTile);
+            mbar_arrive_expect_tx(bar_q, HALVES * L::kTile);
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh)
+            for (int hh = 0; hh < HALVES; ++hh)
 #pragma unroll
                 for (int c = 0; c < kChunks; ++c)
-                    tma_load_3d(sQ + hh * L::kTile + c * kChunkBytesSw128, &args.tm_q, c * 64, qt * kBQ + hh * kHalf,
+                    tma_load_3d(sQ + hh * L::kTile + c * kChunkBytesSw128, &args.tm_q, c * 64, qt * kBQt + hh * kHalf,
                                 h, bar_q);
             bool ok = true;
             int jk = 0, jv = 0;  // K tiles and V tiles issued
@@ -449,6 +455,36 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             };
             bool ok = __all_sync(0xFFFFFFFFu, mbar_wait_spin(bar_q, 0, status));
             if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait_spin(bar_k_full, 0, status));
+            if constexpr (HALVES == 1) {
+                // one half: S in two TMEM buffers (columns 0 / 128 by tile parity), so
+                // S(j+1) is issued before PV(j) and overlaps the softmax of tile j
+                if (ok) {
+                    tc_fence_after();
+                    issue_s(kColS, dq0, dk0);
+                    commit(bar_s_full + 0);
+                    commit(bar_k_empty + 0);
+                }
+                for (int j = 0; ok && j < n; ++j) {
+                    const int st = j % kStages;
+                    if (j + 1 < n) {
+                        const int st1 = (j + 1) % kStages;
+                        ok = __all_sync(0xFFFFFFFFu,
+                                        mbar_wait_spin(bar_k_full + st1, ((j + 1) / kStages) & 1, status));
+                        if (!ok) break;
+                        tc_fence_after();
+                        issue_s(kColS + 128 * ((j + 1) & 1), dq0, dk0 + st1 * kStageStep);
+                        commit(bar_s_full + ((j + 1) & 1));
+                        commit(bar_k_empty + st1);
+                    }
+                    ok = __all_sync(0xFFFFFFFFu, mbar_wait_spin(bar_v_full + st, (j / kStages) & 1, status));
+                    if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait_spin(bar_p_full + 0, j & 1, status));
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_pv(kColO, kColS + 128 * (j & 1), dv0 + st * kStageStep, j > 0);
+                    commit(bar_o_done + 0);
+                    commit(bar_v_empty + st);
+                }
+            } else {
             if (ok) {
                 tc_fence_after();
                 issue_s(kColS, dq0, dk0);
@@ -486,6 +522,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                 commit(bar_o_done + 1);
                 commit(bar_v_empty + st);
             }
+            }
             commit(bar_mma_done);
             mbar_wait(bar_mma_done, 0, status);
         }
@@ -494,9 +531,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
         const int hf = (warp - 4) >> 2;  // half
         const int r = threadIdx.x - 128 - hf * 128;
         const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-        const uint32_t t_s = tmem + lane_base + kColS + hf * 128;
+        // S of this half (two halves), or S buffer 0 of the single half, whose
+        // tile j uses buffer j % 2
+        const uint32_t t_s0 = tmem + lane_base + kColS + hf * 128;
         const uint32_t t_o = tmem + lane_base + kColO + hf * 128;
-        const int q = qt * kBQ + hf * kHalf + r;
+        const int q = qt * kBQt + hf * kHalf + r;
         // mask predicate row: the query itself, or (routing) the sampled token
         int qo = q;
         if constexpr (ROUTE) {
@@ -515,7 +554,11 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             const uint32_t e = entry_at<ROUTE>(args, ents, j, code, j0);
             const int cls = static_cast<int>(e >> BSS_CLASS_SHIFT);
             const int c0 = static_cast<int>(e & BSS_TILE_INDEX_MASK) * kBKV;
-            ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_s_full + hf, j & 1, status));
+            const uint32_t t_s = HALVES == 2 ? t_s0 : t_s0 + 128 * (j & 1);
+            if constexpr (HALVES == 2)
+                ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_s_full + hf, j & 1, status));
+            else
+                ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_s_full + (j & 1), (j >> 1) & 1, status));
             if (!ok) break;
             tc_fence_after();
             // ---- fast path: every row of the warp already has a finite reference
@@ -606,8 +649,10 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
                 const float m_new = (tmax_s > m + kRescaleThreshold) ? tmax_s : m;
                 const float alpha = (m_new == m) ? 1.0f : ex2_approx(m - m_new);
                 const float mref = (m_new == -INFINITY) ? 0.0f : m_new;
-                // O_h is rescaled only when some row's reference max moved.  PV_h(j-1)
-                // was issued before S_h(j), so it has completed; the wait only orders.
+                // O_h is rescaled only when some row's reference max moved.  With two
+                // halves PV_h(j-1) was issued before S_h(j), so it has completed and
+                // the wait only orders; with one half S(j) was issued before PV(j-1)
+                // and the wait is real.
                 if (j >= 1 && __any_sync(0xFFFFFFFFu, alpha != 1.0f)) {
                     ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_o_done + hf, (j - 1) & 1, status));
                     if (!ok) break;
@@ -717,7 +762,7 @@ __global__ void __launch_bounds__(kThreads, 1) attn_fwd_kernel(const __grid_cons
             fence_proxy_async_smem();
         }
         named_barrier_sync(1 + hf, 128);
-        const int row0 = qt * kBQ + hf * kHalf;
+        const int row0 = qt * kBQt + hf * kHalf;
         if (r == 0 && ok && row0 < args.N && !gather && !ROUTE) {
 #pragma unroll
             for (int cc = 0; cc < kChunks; ++cc)
@@ -794,20 +839,26 @@ bss_status launch_d(const AttnLaunch& a, cudaStream_t stream) {
     const float scale = a.softmax_scale > 0.0f ? a.softmax_scale : 1.0f / sqrtf(static_cast<float>(a.d));
     args.scale_log2 = scale * 1.4426950408889634f;
 
-    const uint32_t smem = Smem<D>::kAlloc;
-    auto kernel = a.route ? attn_fwd_kernel<D, true> : attn_fwd_kernel<D, false>;
+    // one or two 128-row q halves per CTA: the map's BQ (dense control and
+    // routing use two)
+    const int halves = (a.route || a.dense) ? 2 : a.bq / kHalf;
+    if (halves != 1 && halves != 2) return set_error(BSS_ERR_UNSUPPORTED, "query tile of %d rows", a.bq);
+    const uint32_t smem = halves == 2 ? Smem<D, 2>::kAlloc : Smem<D, 1>::kAlloc;
+    auto kernel = a.route ? attn_fwd_kernel<D, true, 2>
+                          : (halves == 2 ? attn_fwd_kernel<D, false, 2> : attn_fwd_kernel<D, false, 1>);
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return cuda_check(e, "cudaFuncSetAttribute(attention)");
     const int64_t items = static_cast<int64_t>(a.H) * a.nq * (a.route ? 3 * a.splits : 1);
     if (items <= 0) return BSS_OK;
     if (items > 0x7FFFFFFF) return set_error(BSS_ERR_UNSUPPORTED, "too many work items");
-    kernel<<<static_cast<unsigned>(items), kThreads, smem, stream>>>(args);
+    kernel<<<static_cast<unsigned>(items), 128 * (1 + halves), smem, stream>>>(args);
     return cuda_check(cudaGetLastError(), "attention launch");
 }
 
 }  // namespace
 
 int attention_block_q() { return kBQ; }
+bool attention_supports_block_q(int bq) { return bq == kHalf || bq == 2 * kHalf; }
 int attention_block_kv() { return kBKV; }
 
 bss_status launch_attention(const AttnLaunch& a, cudaStream_t stream) {

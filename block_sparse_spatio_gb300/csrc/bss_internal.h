@@ -73,12 +73,14 @@ struct AttnLaunch {
     // order) over Nq sampled query rows per head whose tokens are qmap[r]; every
     // kv tile, split into `splits` ranges; normalised fp32 O and LSE per split
     int32_t route, Nq, splits;
+    int32_t bq;  // query rows per CTA: the map's BQ (128 or 256)
     const int32_t* qmap;
     float* o_f32;
     float* lse_f32;
 };
 bss_status launch_attention(const AttnLaunch& a, cudaStream_t stream);
-int attention_block_q();   // query rows per attention tile (the map's BQ)
+int attention_block_q();   // query rows per attention tile of the default shape (the map's BQ)
+bool attention_supports_block_q(int bq);  // 128 (one MMA half per CTA) or 256 (two)
 int attention_block_kv();  // key columns per attention tile (the map's BKV)
 
 // helpers (bss_api.cu)

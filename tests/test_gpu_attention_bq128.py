@@ -1,0 +1,30 @@
+"""Attention on 128-row query tiles (one MMA half per CTA, S double-buffered in
+tensor memory) against the fp64 oracle; for exact masks it must equal the
+256-row kernel bit for bit (each row sees its retained keys in the same order;
+the extra tiles of a 256-row tile are fully masked for it and add exact zeros)."""
+import pytest
+import torch
+
+import oracle
+from _util import compare, oracle_kind, oracle_rows, run_gpu
+from test_gpu_attention import SMALL_CASES, _inputs
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("case", SMALL_CASES, ids=[c[0] for c in SMALL_CASES])
+@pytest.mark.parametrize("rounding", [0, 1, 2])
+@pytest.mark.parametrize("tperm", [1, 0])
+def test_bq128_matches_oracle_and_bq256(bss, case, rounding, tperm):
+    name, F, Hs, Ws, d, wf, ws, flags = case
+    N = F * Hs * Ws
+    q, k, v = _inputs(len(flags), N, d, seed=len(name) + 40)
+    p = bss.MaskParams(F, Hs, Ws, d, wf, ws, temporal_permuted=tperm, rounding=rounding)
+    out, lse, _ = run_gpu(bss, q, k, v, flags, p, BQ=128)
+    g = oracle.Geometry(F, Hs, Ws, wf=wf, ws=ws, bkv=128)
+    for h, fl in enumerate(flags):
+        Oref, lref = oracle_rows(q, k, v, h, oracle_kind(fl, tperm), g, None, rounding == 1, BQ=128)
+        compare(out[h].numpy(), lse[h].numpy(), Oref, lref, f"BQ=128 {name} head {h} rounding {rounding}")
+    if rounding != 1:
+        out2, lse2, _ = run_gpu(bss, q, k, v, flags, p, BQ=256)
+        assert torch.equal(out.view(torch.int32), out2.view(torch.int32)), f"{name}: O differs from BQ=256"
+        assert torch.equal(lse.view(torch.int32), lse2.view(torch.int32)), f"{name}: LSE differs from BQ=256"
