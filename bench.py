@@ -358,7 +358,7 @@ def main():
         traffic = traffic * H / w.H
     line["roofline"] = {"bound": "tensor", "achieved": attn_tflops, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                         "frac": attn_tflops / peaks["bf16_tflops"], "traffic": traffic,
-                        "peak_source": f"{peak_src} bf16 burst (cuBLAS 8192^3)", "kernel": "attn_fwd_kernel<128>"}
+                        "peak_source": f"{peak_src} bf16 burst (cuBLAS 8192^3)", "kernel": "attn_fwd_kernel<128, false, 2>"}
 
     if not args.no_extras and rank == 0:
         line["variants"] = variants(bss, torch, W, w, H, Q, K, V, dev, peaks, flags)
