@@ -16,7 +16,9 @@
 //   warp 0       TMA producer: Q (both halves) once, then K and V tiles of the
 //                list into separate KV_STAGES-deep rings (128-byte swizzled,
 //                64-column boxes).
-//   warp 1       TMEM allocator and single-thread tcgen05.mma issuer.
+//   warp 1       TMEM allocator and single-thread tcgen05.mma issuer; it
+//                waits with the suspending try_wait, which leaves the issue
+//                slots of its SM sub-partition to the softmax warps there.
 //                TMEM: S_h (128 fp32 columns) and O_h (D columns) per half h;
 //                the bf16 P_h is written over the first 64 columns of S_h.
 //                Issue order  S_1(j) PV_0(j) S_0(j+1) PV_1(j) S_1(j+1) ...
@@ -453,8 +455,8 @@ __global__ void __launch_bounds__(threads_for<HALVES>(), 1) attn_fwd_kernel(cons
             auto commit = [&](uint64_t* bar) {
                 if (leader) tc_commit(bar);
             };
-            bool ok = __all_sync(0xFFFFFFFFu, mbar_wait_spin(bar_q, 0, status));
-            if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait_spin(bar_k_full, 0, status));
+            bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_q, 0, status));
+            if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_k_full, 0, status));
             if constexpr (HALVES == 1) {
                 // one half: S in two TMEM buffers (columns 0 / 128 by tile parity), so
                 // S(j+1) is issued before PV(j) and overlaps the softmax of tile j
@@ -469,15 +471,15 @@ __global__ void __launch_bounds__(threads_for<HALVES>(), 1) attn_fwd_kernel(cons
                     if (j + 1 < n) {
                         const int st1 = (j + 1) % kStages;
                         ok = __all_sync(0xFFFFFFFFu,
-                                        mbar_wait_spin(bar_k_full + st1, ((j + 1) / kStages) & 1, status));
+                                        mbar_wait(bar_k_full + st1, ((j + 1) / kStages) & 1, status));
                         if (!ok) break;
                         tc_fence_after();
                         issue_s(kColS + 128 * ((j + 1) & 1), dq0, dk0 + st1 * kStageStep);
                         commit(bar_s_full + ((j + 1) & 1));
                         commit(bar_k_empty + st1);
                     }
-                    ok = __all_sync(0xFFFFFFFFu, mbar_wait_spin(bar_v_full + st, (j / kStages) & 1, status));
-                    if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait_spin(bar_p_full + 0, j & 1, status));
+                    ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_v_full + st, (j / kStages) & 1, status));
+                    if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_p_full + 0, j & 1, status));
                     if (!ok) break;
                     tc_fence_after();
                     issue_pv(kColO, kColS + 128 * (j & 1), dv0 + st * kStageStep, j > 0);
@@ -499,8 +501,8 @@ __global__ void __launch_bounds__(threads_for<HALVES>(), 1) attn_fwd_kernel(cons
                 commit(bar_s_full + 1);
                 commit(bar_k_empty + st);  // K_j is free once S_0(j) and S_1(j) complete
                 // PV_0(j)
-                ok = __all_sync(0xFFFFFFFFu, mbar_wait_spin(bar_v_full + st, (j / kStages) & 1, status));
-                if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait_spin(bar_p_full + 0, j & 1, status));
+                ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_v_full + st, (j / kStages) & 1, status));
+                if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_p_full + 0, j & 1, status));
                 if (!ok) break;
                 tc_fence_after();
                 issue_pv(kColO, kColS, dv, j > 0);
@@ -508,14 +510,14 @@ __global__ void __launch_bounds__(threads_for<HALVES>(), 1) attn_fwd_kernel(cons
                 // S_0(j+1)
                 if (j + 1 < n) {
                     const int st1 = (j + 1) % kStages;
-                    ok = __all_sync(0xFFFFFFFFu, mbar_wait_spin(bar_k_full + st1, ((j + 1) / kStages) & 1, status));
+                    ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_k_full + st1, ((j + 1) / kStages) & 1, status));
                     if (!ok) break;
                     tc_fence_after();
                     issue_s(kColS, dq0, dk0 + st1 * kStageStep);
                     commit(bar_s_full + 0);
                 }
                 // PV_1(j)
-                ok = __all_sync(0xFFFFFFFFu, mbar_wait_spin(bar_p_full + 1, j & 1, status));
+                ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_p_full + 1, j & 1, status));
                 if (!ok) break;
                 tc_fence_after();
                 issue_pv(kColO + 128, kColS + 128, dv, j > 0);

@@ -74,36 +74,6 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, int* s
     return true;
 }
 
-// Non-suspending poll of a phase (for the latency-critical MMA issuer).
-__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// Bounded busy-wait (no suspension): same contract as mbar_wait.
-__device__ __forceinline__ bool mbar_wait_spin(uint64_t* bar, uint32_t parity, int* status,
-                                               uint64_t limit_ns = 2000000000ull) {
-    if (mbar_test_wait(bar, parity)) return true;
-    const uint64_t t0 = global_timer_ns();
-    uint32_t spins = 0;
-    while (!mbar_test_wait(bar, parity)) {
-        if (((++spins) & 1023u) == 0u) {
-            if (global_timer_ns() - t0 > limit_ns) {
-                record_status(status, BSS_ERR_TIMEOUT);
-                return false;
-            }
-        }
-    }
-    return true;
-}
-
 // One lane of a converged warp, chosen by the hardware (true in exactly one lane).
 __device__ __forceinline__ bool elect_one() {
     uint32_t pred = 0;
