@@ -159,3 +159,19 @@ def test_full_size_1440p_302k_rounded_sampled(bss):
     wl = W.P1440_302K
     fl = wl.head_flags()
     _full_size(bss, wl, 1, 1, heads=[fl.index(0), fl.index(1)], nrows=12)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("geom", [(8, 16, 24, 128), (3, 10, 13, 64), (5, 7, 9, 128)], ids=["small", "ragged_d64", "ragged_d128"])
+def test_all_covering_windows_equal_dense_bit_for_bit(bss, geom):
+    # spatial with wf >= F-1 and the (F,H,W) temporal mask with ws >= S-1 retain
+    # every pair, visit every kv tile in ascending order and mask only the
+    # padding columns: the same arithmetic as the dense control
+    F, Hs, Ws, d = geom
+    S, N = Hs * Ws, F * Hs * Ws
+    q, k, v = _inputs(2, N, d, seed=N + 3)
+    dense, dlse, _ = run_gpu(bss, q, k, v, [0, 0], None, dense=True)
+    p = bss.MaskParams(F, Hs, Ws, d, F - 1, S - 1, temporal_permuted=0, rounding=0)
+    out, lse, _ = run_gpu(bss, q, k, v, [0, 1], p)
+    assert torch.equal(out.view(torch.int32), dense.view(torch.int32))
+    assert torch.equal(lse.view(torch.int32), dlse.view(torch.int32))
