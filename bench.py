@@ -54,7 +54,10 @@ def parse_args():
     ap.add_argument("--workload", default="mixed_75600tok_10h_d128")
     ap.add_argument("--heads", type=int, default=0, help="override head count (profiling runs)")
     ap.add_argument("--no-extras", action="store_true", help="skip variants, e2e and cpu baseline")
-    ap.add_argument("--cpu-rows-per-head", type=int, default=2048)
+    ap.add_argument("--cpu-rows-per-head", type=int, default=6144,
+                    help="oracle sample of the cpu_baseline entry (about 20 s on 16 cores)")
+    ap.add_argument("--ref-rows-per-head", type=int, default=256,
+                    help="oracle sample per step of --impl reference")
     return ap.parse_args()
 
 
@@ -216,7 +219,7 @@ def run_reference(args):
     q, k, v = W.qkv(w, H=H)
     flops_total = 4.0 * w.d * retained_total(w, flags)
     rows_total = H * w.N
-    rows_per_head = max(8, args.cpu_rows_per_head // 8)
+    rows_per_head = max(8, args.ref_rows_per_head)
     times = []
     for i in range(args.warmup + args.steps):
         dt, nrows = oracle_sample(w, q, k, v, flags, rows_per_head, seed=1000 + i)
