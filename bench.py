@@ -290,17 +290,18 @@ def main():
     attn_events = []
 
     def step(record=False):
-        bss.permute(Q, Qp, fl, params, False)
-        bss.permute(K, Kp, fl, params, False)
-        bss.permute(V, Vp, fl, params, False)
+        # temporal heads permuted into the workspaces, spatial heads used in place
+        bss.permute(Q, Qp, fl, params, False, only_flagged=True)
+        bss.permute(K, Kp, fl, params, False, only_flagged=True)
+        bss.permute(V, Vp, fl, params, False, only_flagged=True)
         if record:
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
-        bss.sparse_attention(Qp, Kp, Vp, Op, tm, fl)
+        bss.sparse_attention_split(Q, K, V, O, Qp, Kp, Vp, Op, tm, fl)
         if record:
             e1.record(stream)
             attn_events.append((e0, e1))
-        bss.permute(Op, O, fl, params, True)
+        bss.permute(Op, O, fl, params, True, only_flagged=True)
 
     launches_per_step = 5
     for _ in range(max(3, args.warmup)):
@@ -344,7 +345,7 @@ def main():
         "config": {"workload": w.name, "tokens": w.N, "frames_x_h_x_w": [w.F, w.Hs, w.Ws], "heads": H,
                    "head_dim": w.d, "flags_temporal": flags, "spatial_frame_window": w.wf,
                    "temporal_raster_window": w.ws, "mask": "exact (full/boundary tiles, B2)", "tile": [128, 128],
-                   "step": "permute QKV -> sparse attention -> unpermute O",
+                   "step": "permute temporal heads' QKV -> sparse attention -> unpermute their O",
                    "l2": f"inputs larger than L2 (Q+K+V = {3 * Q.numel() * 2 / 1e6:.0f} MB)",
                    "parallelism": "replicas" if world > 1 else "single GPU",
                    "retained_pairs": retained,

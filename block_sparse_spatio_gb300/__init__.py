@@ -76,7 +76,7 @@ EXPORTED = ("bss_build_tile_map", "bss_tile_map_stats", "bss_tile_map_dims", "bs
             "bss_destroy_tile_map", "bss_permute", "bss_sparse_attention", "bss_dense_attention",
             "bss_get_device_status", "bss_status_string", "bss_last_error_message", "bss_version",
             "bss_diag_mma_tile", "bss_build_tile_map_csr_noalloc", "bss_route_heads",
-            "bss_sparse_attention_fused")
+            "bss_sparse_attention_fused", "bss_permute_flagged", "bss_sparse_attention_split")
 
 
 def load(path: str | None = None):
@@ -106,6 +106,10 @@ def load(path: str | None = None):
     lib.bss_sparse_attention.restype = st
     lib.bss_sparse_attention_fused.argtypes = [p, p, p, p, p, p, p, i32, ctypes.c_float, p]
     lib.bss_sparse_attention_fused.restype = st
+    lib.bss_sparse_attention_split.argtypes = [p, p, p, p, p, p, p, p, p, p, p, i32, ctypes.c_float, p]
+    lib.bss_sparse_attention_split.restype = st
+    lib.bss_permute_flagged.argtypes = [p, p, p, i32, MP, i32, p]
+    lib.bss_permute_flagged.restype = st
     lib.bss_dense_attention.argtypes = [p, p, p, p, p, i32, i32, i32, ctypes.c_float, p]
     lib.bss_dense_attention.restype = st
     lib.bss_get_device_status.argtypes = [p]
@@ -235,14 +239,17 @@ def destroy_tile_map(m):
         load().bss_destroy_tile_map(m)
 
 
-def permute(x, out, head_is_temporal, params: MaskParams, inverse: bool = False, stream=None):
-    """out <- per-head (F,H,W) -> (H,W,F) permutation of x (inverse=True: back)."""
+def permute(x, out, head_is_temporal, params: MaskParams, inverse: bool = False, stream=None,
+            only_flagged: bool = False):
+    """out <- per-head (F,H,W) -> (H,W,F) permutation of x (inverse=True: back).
+    Heads with flag 0 are copied, or left untouched with ``only_flagged``."""
     import torch
     _dev_tensor(x, "x", torch.bfloat16)
     _dev_tensor(out, "out", torch.bfloat16)
     _dev_tensor(head_is_temporal, "head_is_temporal", torch.uint8)
-    _check(load().bss_permute(_ptr(x), _ptr(out), _ptr(head_is_temporal), x.shape[0], ctypes.byref(params.c()),
-                              int(bool(inverse)), _stream(stream)))
+    fn = load().bss_permute_flagged if only_flagged else load().bss_permute
+    _check(fn(_ptr(x), _ptr(out), _ptr(head_is_temporal), x.shape[0], ctypes.byref(params.c()), int(bool(inverse)),
+              _stream(stream)))
     return out
 
 
@@ -256,6 +263,21 @@ def sparse_attention(Q, K, V, O, tile_map: TileMap, head_is_temporal=None, lse=N
     _dev_tensor(lse, "lse", torch.float32)
     _check(load().bss_sparse_attention(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(lse), tile_map.handle,
                                        _ptr(head_is_temporal), Q.shape[0], float(softmax_scale), _stream(stream)))
+    return O
+
+
+def sparse_attention_split(Q, K, V, O, Qt, Kt, Vt, Ot, tile_map: TileMap, head_is_temporal, lse=None,
+                           softmax_scale: float = 0.0, stream=None):
+    """Block-sparse attention with spatial heads in Q, K, V -> O and temporal
+    heads (flag 1) in the permuted buffers Qt, Kt, Vt -> Ot."""
+    import torch
+    for t, n in ((Q, "Q"), (K, "K"), (V, "V"), (O, "O"), (Qt, "Qt"), (Kt, "Kt"), (Vt, "Vt"), (Ot, "Ot")):
+        _dev_tensor(t, n, torch.bfloat16)
+    _dev_tensor(head_is_temporal, "head_is_temporal", torch.uint8)
+    _dev_tensor(lse, "lse", torch.float32)
+    _check(load().bss_sparse_attention_split(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(Qt), _ptr(Kt), _ptr(Vt),
+                                             _ptr(Ot), _ptr(lse), tile_map.handle, _ptr(head_is_temporal),
+                                             Q.shape[0], float(softmax_scale), _stream(stream)))
     return O
 
 
@@ -343,11 +365,13 @@ def attention_step(Q, K, V, O, tile_map: TileMap, head_is_temporal, Qp, Kp, Vp, 
     Q, K, V, O are in (F,H,W) order; Qp, Kp, Vp, Op are caller-owned workspaces."""
     p = tile_map.params
     if p.temporal_permuted:
-        permute(Q, Qp, head_is_temporal, p, False, stream)
-        permute(K, Kp, head_is_temporal, p, False, stream)
-        permute(V, Vp, head_is_temporal, p, False, stream)
-        sparse_attention(Qp, Kp, Vp, Op, tile_map, head_is_temporal, lse, stream=stream)
-        permute(Op, O, head_is_temporal, p, True, stream)
+        # only the temporal heads are permuted; spatial heads are read from Q, K, V
+        # and written to O in place
+        permute(Q, Qp, head_is_temporal, p, False, stream, only_flagged=True)
+        permute(K, Kp, head_is_temporal, p, False, stream, only_flagged=True)
+        permute(V, Vp, head_is_temporal, p, False, stream, only_flagged=True)
+        sparse_attention_split(Q, K, V, O, Qp, Kp, Vp, Op, tile_map, head_is_temporal, lse, stream=stream)
+        permute(Op, O, head_is_temporal, p, True, stream, only_flagged=True)
     else:
         sparse_attention(Q, K, V, O, tile_map, head_is_temporal, lse, stream=stream)
     return O

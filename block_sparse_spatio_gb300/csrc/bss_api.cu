@@ -265,8 +265,9 @@ void bss_destroy_tile_map(bss_tile_map map) {
     delete map;
 }
 
-bss_status bss_permute(const void* in, void* out, const uint8_t* head_is_temporal, int32_t H,
-                       const bss_mask_params* params, int32_t inverse, cudaStream_t stream) {
+namespace {
+bss_status permute_impl(const void* in, void* out, const uint8_t* head_is_temporal, int32_t H,
+                        const bss_mask_params* params, int32_t inverse, int32_t only_flagged, cudaStream_t stream) {
     using namespace bss;
     t_last_error[0] = '\0';
     bss_status st = validate_params(params);
@@ -275,19 +276,33 @@ bss_status bss_permute(const void* in, void* out, const uint8_t* head_is_tempora
     if (!aligned16(in) || !aligned16(out)) return set_error(BSS_ERR_INVALID_ARG, "tensors must be 16-byte aligned");
     if (H <= 0) return set_error(BSS_ERR_INVALID_ARG, "H must be positive");
     if (inverse != 0 && inverse != 1) return set_error(BSS_ERR_INVALID_ARG, "inverse must be 0 or 1");
+    if (only_flagged && head_is_temporal == nullptr)
+        return set_error(BSS_ERR_INVALID_ARG, "head_is_temporal is NULL (no head to permute)");
     const int64_t S = static_cast<int64_t>(params->Hs) * params->Ws;
     const int64_t bytes = static_cast<int64_t>(H) * S * params->F * params->head_dim * 2;
     const uintptr_t a = reinterpret_cast<uintptr_t>(in), b = reinterpret_cast<uintptr_t>(out);
     if (a < b + static_cast<uintptr_t>(bytes) && b < a + static_cast<uintptr_t>(bytes))
         return set_error(BSS_ERR_INVALID_ARG, "in and out overlap");
     return launch_permute(in, out, head_is_temporal, H, params->F, static_cast<int32_t>(S), params->head_dim,
-                          inverse, stream);
+                          inverse, only_flagged, stream);
+}
+}  // namespace
+
+bss_status bss_permute(const void* in, void* out, const uint8_t* head_is_temporal, int32_t H,
+                       const bss_mask_params* params, int32_t inverse, cudaStream_t stream) {
+    return permute_impl(in, out, head_is_temporal, H, params, inverse, 0, stream);
+}
+
+bss_status bss_permute_flagged(const void* in, void* out, const uint8_t* head_is_temporal, int32_t H,
+                               const bss_mask_params* params, int32_t inverse, cudaStream_t stream) {
+    return permute_impl(in, out, head_is_temporal, H, params, inverse, 1, stream);
 }
 
 namespace {
 bss_status sparse_attention_impl(const void* Q, const void* K, const void* V, void* O, float* lse, bss_tile_map map,
                                  const uint8_t* head_is_temporal, int32_t H, float softmax_scale, int32_t fused,
-                                 cudaStream_t stream) {
+                                 cudaStream_t stream, const void* Qt = nullptr, const void* Kt = nullptr,
+                                 const void* Vt = nullptr, void* Ot = nullptr) {
     using namespace bss;
     t_last_error[0] = '\0';
     if (!map_is_live(map)) return set_error(BSS_ERR_INVALID_ARG, "invalid or destroyed tile map");
@@ -331,6 +346,10 @@ bss_status sparse_attention_impl(const void* Q, const void* K, const void* V, vo
     a.softmax_scale = softmax_scale;
     a.fused = fused;
     a.bq = map->BQ;
+    a.Qt = Qt;
+    a.Kt = Kt;
+    a.Vt = Vt;
+    a.Ot = Ot;
     return launch_attention(a, stream);
 }
 }  // namespace
@@ -339,6 +358,18 @@ bss_status bss_sparse_attention(const void* Q, const void* K, const void* V, voi
                                 bss_tile_map map, const uint8_t* head_is_temporal, int32_t H, float softmax_scale,
                                 cudaStream_t stream) {
     return sparse_attention_impl(Q, K, V, O, lse, map, head_is_temporal, H, softmax_scale, 0, stream);
+}
+
+bss_status bss_sparse_attention_split(const void* Q, const void* K, const void* V, void* O, const void* Qt,
+                                      const void* Kt, const void* Vt, void* Ot, float* lse, bss_tile_map map,
+                                      const uint8_t* head_is_temporal, int32_t H, float softmax_scale,
+                                      cudaStream_t stream) {
+    using namespace bss;
+    if (Qt == nullptr || Kt == nullptr || Vt == nullptr || Ot == nullptr)
+        return set_error(BSS_ERR_INVALID_ARG, "NULL temporal-head tensor");
+    if (!aligned16(Qt) || !aligned16(Kt) || !aligned16(Vt) || !aligned16(Ot))
+        return set_error(BSS_ERR_INVALID_ARG, "tensors must be 16-byte aligned");
+    return sparse_attention_impl(Q, K, V, O, lse, map, head_is_temporal, H, softmax_scale, 0, stream, Qt, Kt, Vt, Ot);
 }
 
 bss_status bss_sparse_attention_fused(const void* Q, const void* K, const void* V, void* O, float* lse,

@@ -62,6 +62,7 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale when max grows
 
 struct AttnArgs {
     CUtensorMap tm_q, tm_k, tm_v, tm_o, tm_ks, tm_vs;
+    CUtensorMap tm_qt, tm_kt, tm_vt, tm_ot;  // heads with flag 1 (= the maps above unless split buffers)
     CUtensorMap tm_qg, tm_kg, tm_vg;  // [H*N] rows views, one-row boxes (fused permutation)
     uint16_t* o_rows;                 // O as bf16 bits (fused permutation: row-wise stores)
     const int32_t* qmap;              // routing: token index of each query row (mask predicate)
@@ -240,6 +241,7 @@ __global__ void __launch_bounds__(threads_for<HALVES>(), 1) attn_fwd_kernel(cons
     // spatial / temporal in (F,H,W) order, every kv tile of the split.
     const int item = blockIdx.x;
     int h, vh = 0, split = 0, j0 = 0, code;
+    bool tbuf = false;  // head with flag 1: its tensors come from the temporal-head buffers
     int qt, n;
     const int32_t* ents = nullptr;
     if constexpr (ROUTE) {
@@ -258,6 +260,7 @@ __global__ void __launch_bounds__(threads_for<HALVES>(), 1) attn_fwd_kernel(cons
         const int local = item - h * args.nq;
         int kind = 0;
         if (!args.dense && args.flags != nullptr) kind = args.flags[h] ? 1 : 0;
+        tbuf = kind == 1;
         code = args.dense ? static_cast<int>(MASK_DENSE) : args.code[kind];
         if (args.dense) {
             qt = local;
@@ -372,15 +375,18 @@ __global__ void __launch_bounds__(threads_for<HALVES>(), 1) attn_fwd_kernel(cons
     } else if (warp == 0) {
         // =========================== TMA producer
         if (lane == 0) {
-            tma_prefetch_desc(&args.tm_q);
-            tma_prefetch_desc(&args.tm_k);
-            tma_prefetch_desc(&args.tm_v);
+            const CUtensorMap* mq = tbuf ? &args.tm_qt : &args.tm_q;
+            const CUtensorMap* mk0 = tbuf ? &args.tm_kt : &args.tm_k;
+            const CUtensorMap* mv0 = tbuf ? &args.tm_vt : &args.tm_v;
+            tma_prefetch_desc(mq);
+            tma_prefetch_desc(mk0);
+            tma_prefetch_desc(mv0);
             mbar_arrive_expect_tx(bar_q, HALVES * L::kTile);
 #pragma unroll
             for (int hh = 0; hh < HALVES; ++hh)
 #pragma unroll
                 for (int c = 0; c < kChunks; ++c)
-                    tma_load_3d(sQ + hh * L::kTile + c * kChunkBytesSw128, &args.tm_q, c * 64, qt * kBQt + hh * kHalf,
+                    tma_load_3d(sQ + hh * L::kTile + c * kChunkBytesSw128, mq, c * 64, qt * kBQt + hh * kHalf,
                                 h, bar_q);
             bool ok = true;
             int jk = 0, jv = 0;  // K tiles and V tiles issued
@@ -388,8 +394,8 @@ __global__ void __launch_bounds__(threads_for<HALVES>(), 1) attn_fwd_kernel(cons
                 const int st = jv % kStages;
                 const uint32_t e = entry_at<ROUTE>(args, ents, jv, code, j0);
                 const int col0 = static_cast<int>(e & BSS_TILE_INDEX_MASK) * kBKV;
-                const CUtensorMap* mk = &args.tm_k;
-                const CUtensorMap* mv = &args.tm_v;
+                const CUtensorMap* mk = mk0;
+                const CUtensorMap* mv = mv0;
                 int row = col0;
                 if (code == MASK_TEMPORAL_VIRT) {
                     if (col0 < args.S_pad) {
@@ -768,7 +774,7 @@ __global__ void __launch_bounds__(threads_for<HALVES>(), 1) attn_fwd_kernel(cons
         if (r == 0 && ok && row0 < args.N && !gather && !ROUTE) {
 #pragma unroll
             for (int cc = 0; cc < kChunks; ++cc)
-                tma_store_3d(&args.tm_o, stage + cc * kChunkBytesSw128, cc * 64, row0, h);
+                tma_store_3d(tbuf ? &args.tm_ot : &args.tm_o, stage + cc * kChunkBytesSw128, cc * 64, row0, h);
             tma_store_commit();
             tma_store_wait_read_all();
         }
@@ -801,8 +807,17 @@ bss_status launch_d(const AttnLaunch& a, cudaStream_t stream) {
     // frame-0 keys of a temporal head: row s of this view is key (f = 0, s), which
     // is permuted row s*F of a permuted tensor, or row s of an (F,H,W) tensor
     const uint64_t sink_rs = a.fused ? rs : rs * a.F;
-    if ((st = encode_tmap_3d(&args.tm_ks, a.K, a.d, a.S, a.H, sink_rs, hs, 64, kBKV)) != BSS_OK) return st;
-    if ((st = encode_tmap_3d(&args.tm_vs, a.V, a.d, a.S, a.H, sink_rs, hs, 64, kBKV)) != BSS_OK) return st;
+    // heads with flag 1: split buffers if given
+    const void* Qt = a.Qt ? a.Qt : a.Q;
+    const void* Kt = a.Kt ? a.Kt : a.K;
+    const void* Vt = a.Vt ? a.Vt : a.V;
+    void* Ot = a.Ot ? a.Ot : (a.route ? const_cast<void*>(a.Q) : a.O);
+    if ((st = encode_tmap_3d(&args.tm_qt, Qt, a.d, nq_rows, a.H, rs, rs * nq_rows, 64, kHalf)) != BSS_OK) return st;
+    if ((st = encode_tmap_3d(&args.tm_kt, Kt, a.d, a.N, a.H, rs, hs, 64, kBKV)) != BSS_OK) return st;
+    if ((st = encode_tmap_3d(&args.tm_vt, Vt, a.d, a.N, a.H, rs, hs, 64, kBKV)) != BSS_OK) return st;
+    if ((st = encode_tmap_3d(&args.tm_ot, Ot, a.d, nq_rows, a.H, rs, rs * nq_rows, 64, kHalf)) != BSS_OK) return st;
+    if ((st = encode_tmap_3d(&args.tm_ks, Kt, a.d, a.S, a.H, sink_rs, hs, 64, kBKV)) != BSS_OK) return st;
+    if ((st = encode_tmap_3d(&args.tm_vs, Vt, a.d, a.S, a.H, sink_rs, hs, 64, kBKV)) != BSS_OK) return st;
     if (a.fused) {
         const uint64_t rows = static_cast<uint64_t>(a.H) * static_cast<uint64_t>(a.N);
         if (rows > 0x7FFFFFFFull) return set_error(BSS_ERR_UNSUPPORTED, "H*N too large for the fused permutation");

@@ -48,8 +48,9 @@ bss_status launch_tile_compact(int32_t nq, int32_t nkv, const uint8_t* cls, cons
                                cudaStream_t stream);
 
 // permutation kernel launch (bss_permute.cu)
+// only_flagged: heads whose flag is 0 are not touched (else they are copied)
 bss_status launch_permute(const void* in, void* out, const uint8_t* flags, int32_t H, int32_t F, int32_t S,
-                          int32_t d, int32_t inverse, cudaStream_t stream);
+                          int32_t d, int32_t inverse, int32_t only_flagged, cudaStream_t stream);
 
 // attention launch (bss_attention.cu)
 struct AttnLaunch {
@@ -74,6 +75,9 @@ struct AttnLaunch {
     // kv tile, split into `splits` ranges; normalised fp32 O and LSE per split
     int32_t route, Nq, splits;
     int32_t bq;  // query rows per CTA: the map's BQ (128 or 256)
+    // split buffers: heads with flag 1 read Qt, Kt, Vt and write Ot (NULL: Q, K, V, O)
+    const void *Qt, *Kt, *Vt;
+    void* Ot;
     const int32_t* qmap;
     float* o_f32;
     float* lse_f32;

@@ -39,9 +39,10 @@ __device__ __forceinline__ void st_stream(uint4* p, const uint4& v) {
 template <int VEC_PER_ROW, int UNROLL>
 __global__ void __launch_bounds__(256) permute_kernel(const uint4* __restrict__ in, uint4* __restrict__ out,
                                                       const uint8_t* __restrict__ flags, uint32_t N, uint32_t F,
-                                                      uint32_t S, int inverse) {
+                                                      uint32_t S, int inverse, int only_flagged) {
     const uint32_t h = blockIdx.y;
     const bool perm = flags != nullptr && flags[h] != 0;
+    if (only_flagged && !perm) return;  // the head's rows stay as they are in `out`
     const uint4* src_h = in + static_cast<size_t>(h) * N * VEC_PER_ROW;
     uint4* dst_h = out + static_cast<size_t>(h) * N * VEC_PER_ROW;
     const uint32_t piece = threadIdx.x % VEC_PER_ROW;
@@ -78,7 +79,7 @@ __global__ void __launch_bounds__(256) permute_kernel(const uint4* __restrict__ 
 }  // namespace
 
 bss_status launch_permute(const void* in, void* out, const uint8_t* flags, int32_t H, int32_t F, int32_t S,
-                          int32_t d, int32_t inverse, cudaStream_t stream) {
+                          int32_t d, int32_t inverse, int32_t only_flagged, cudaStream_t stream) {
     const int64_t N = static_cast<int64_t>(F) * S;
     if (N == 0 || H == 0) return BSS_OK;
     if (N > 0xFFFFFFFFll / 16) return set_error(BSS_ERR_UNSUPPORTED, "too many tokens per head");
@@ -96,10 +97,10 @@ bss_status launch_permute(const void* in, void* out, const uint8_t* flags, int32
     uint4* dst = static_cast<uint4*>(out);
     if (d == 128) {
         permute_kernel<16, kUnroll><<<grid, threads, 0, stream>>>(src, dst, flags, static_cast<uint32_t>(N), F, S,
-                                                                 inverse);
+                                                                 inverse, only_flagged);
     } else if (d == 64) {
         permute_kernel<8, kUnroll><<<grid, threads, 0, stream>>>(src, dst, flags, static_cast<uint32_t>(N), F, S,
-                                                                inverse);
+                                                                inverse, only_flagged);
     } else {
         return set_error(BSS_ERR_UNSUPPORTED, "head_dim %d not supported (64 or 128)", d);
     }

@@ -149,6 +149,13 @@ void bss_destroy_tile_map(bss_tile_map map);
 bss_status bss_permute(const void* in, void* out, const uint8_t* head_is_temporal, int32_t H,
                        const bss_mask_params* params, int32_t inverse, cudaStream_t stream);
 
+/* The same permutation for the flagged (temporal) heads only: heads with
+ * head_is_temporal[h] == 0 are not read and their rows of `out` are left as
+ * they are.  head_is_temporal must not be NULL.  Used with
+ * bss_sparse_attention_split so that spatial heads are never copied. */
+bss_status bss_permute_flagged(const void* in, void* out, const uint8_t* head_is_temporal, int32_t H,
+                               const bss_mask_params* params, int32_t inverse, cudaStream_t stream);
+
 /* Block-sparse attention O = softmax(Q K^T * scale) V over the retained pairs
  * of each head's mask (blog: tiles of Q[i1:i2] K[j1:j2]^T with running softmax
  * statistics; full tiles mask-free, boundary tiles masked, skipped tiles never
@@ -167,6 +174,18 @@ bss_status bss_permute(const void* in, void* out, const uint8_t* head_is_tempora
 bss_status bss_sparse_attention(const void* Q, const void* K, const void* V, void* O, float* lse,
                                 bss_tile_map map, const uint8_t* head_is_temporal, int32_t H,
                                 float softmax_scale, cudaStream_t stream);
+
+/* bss_sparse_attention with the two head kinds in separate buffers: heads with
+ * head_is_temporal[h] == 0 read Q, K, V and write O, heads with flag 1 read Qt,
+ * Kt, Vt and write Ot (all device [H][N][d] bf16, only each kind's heads are
+ * touched).  With Qt, Kt, Vt the bss_permute_flagged images of Q, K, V and O
+ * restored by the inverse bss_permute_flagged of Ot, the step permutes only
+ * the temporal heads.  lse as in bss_sparse_attention (each head in its own
+ * layout).  Errors as bss_sparse_attention. */
+bss_status bss_sparse_attention_split(const void* Q, const void* K, const void* V, void* O, const void* Qt,
+                                      const void* Kt, const void* Vt, void* Ot, float* lse, bss_tile_map map,
+                                      const uint8_t* head_is_temporal, int32_t H, float softmax_scale,
+                                      cudaStream_t stream);
 
 /* The same attention with the token permutation fused into the kernel (blog,
  * section "Arrange tokens for efficient temporal access": the (H,W,F) order

@@ -175,3 +175,34 @@ def test_all_covering_windows_equal_dense_bit_for_bit(bss, geom):
     out, lse, _ = run_gpu(bss, q, k, v, [0, 1], p)
     assert torch.equal(out.view(torch.int32), dense.view(torch.int32))
     assert torch.equal(lse.view(torch.int32), dlse.view(torch.int32))
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("wl_name", ["small_3072tok_2h_d128", "mixed_75600tok_10h_d128"])
+def test_split_step_equals_full_permutation_step(bss, wl_name):
+    # temporal heads permuted alone + split attention == every head permuted (spatial
+    # heads copied) + one-buffer attention, bit for bit, O and LSE
+    import workloads as W
+    wl = W.BY_NAME[wl_name]
+    dev = torch.device("cuda")
+    Q, K, V = W.qkv_device(wl, dev)
+    H = Q.shape[0]
+    flags = wl.head_flags()
+    fl = torch.tensor(flags, dtype=torch.uint8, device=dev)
+    p = bss.MaskParams(wl.F, wl.Hs, wl.Ws, wl.d, wl.wf, wl.ws, temporal_permuted=1, rounding=0)
+    O1, O2 = torch.empty_like(Q), torch.empty_like(Q)
+    l1 = torch.empty(H, wl.N, device=dev)
+    l2 = torch.empty(H, wl.N, device=dev)
+    ws = [torch.empty_like(Q) for _ in range(4)]
+    with bss.build_tile_map(p) as tm:
+        bss.attention_step(Q, K, V, O1, tm, fl, *ws, lse=l1)
+        Qp, Kp, Vp, Op = (torch.empty_like(Q) for _ in range(4))
+        bss.permute(Q, Qp, fl, p, False)
+        bss.permute(K, Kp, fl, p, False)
+        bss.permute(V, Vp, fl, p, False)
+        bss.sparse_attention(Qp, Kp, Vp, Op, tm, fl, lse=l2)
+        bss.permute(Op, O2, fl, p, True)
+        torch.cuda.synchronize()
+    assert bss.get_device_status() == 0
+    assert torch.equal(O1.view(torch.int16), O2.view(torch.int16))
+    assert torch.equal(l1.view(torch.int32), l2.view(torch.int32))

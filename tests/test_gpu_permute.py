@@ -61,3 +61,34 @@ def test_permute_full_size_round_trip_and_samples(bss):
         for t in rng.integers(0, w.N, 50):
             dst = oracle.perm_index(int(t), w.F, w.S) if flags[h] else int(t)
             assert torch.equal(Y[h, dst].view(torch.int16), X[h, int(t)].view(torch.int16))
+
+
+@pytest.mark.gpu
+def test_permute_flagged_touches_only_flagged_heads(bss):
+    w = W.SMALL
+    H = 4
+    x, _, _ = W.qkv(w, H=H, seed=5)
+    flags = [1, 0, 0, 1]
+    p = bss.MaskParams(w.F, w.Hs, w.Ws, w.d, w.wf, w.ws)
+    dev = torch.device("cuda")
+    xd = x.to(dev)
+    out = torch.full_like(xd, 7.0)
+    fl = torch.tensor(flags, dtype=torch.uint8, device=dev)
+    bss.permute(xd, out, fl, p, False, only_flagged=True)
+    torch.cuda.synchronize()
+    o = out.cpu()
+    ref = oracle.permute(W.bf16_bits(x), w.F, w.S, flags)
+    for h in range(H):
+        if flags[h]:
+            assert np.array_equal(o[h].view(torch.int16).numpy().view(np.uint16), ref[h])
+        else:
+            assert torch.all(o[h] == 7.0)
+    back = torch.full_like(xd, 7.0)
+    bss.permute(out, back, fl, p, True, only_flagged=True)
+    torch.cuda.synchronize()
+    b = back.cpu()
+    for h in range(H):
+        if flags[h]:
+            assert torch.equal(b[h].view(torch.int16), x[h].view(torch.int16))
+        else:
+            assert torch.all(b[h] == 7.0)
