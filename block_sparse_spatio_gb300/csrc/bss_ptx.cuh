@@ -112,30 +112,6 @@ __device__ __forceinline__ void tma_gather4_2d(void* smem_dst, const CUtensorMap
         : "memory");
 }
 
-// Same load multicast to every CTA of the cluster in `cta_mask`: the box lands
-// at the same shared-memory offset in each of them and completes `bar` at the
-// same offset in each.
-__device__ __forceinline__ void tma_load_3d_multicast(void* smem_dst, const CUtensorMap* map, int32_t c0,
-                                                      int32_t c1, int32_t c2, uint64_t* bar, uint16_t cta_mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1, {%2, %3, %4}], [%5], %6;" ::"r"(smem_u32(smem_dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_u32(bar)), "h"(cta_mask)
-        : "memory");
-}
-
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-    uint32_t r;
-    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-    return r;
-}
-
-// Every thread of every CTA of the cluster arrives and waits.
-__device__ __forceinline__ void cluster_sync() {
-    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
 // 3-D tiled bulk tensor store shared -> global (rows outside the tensor are clipped).
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* smem_src, int32_t c0,
                                              int32_t c1, int32_t c2) {
@@ -187,16 +163,6 @@ __device__ __forceinline__ void tc_commit(uint64_t* bar) {
                  : "memory");
 }
 
-// Like tc_commit, but the arrival goes to the mbarrier at the same offset in
-// every CTA of the cluster in `cta_mask`.
-__device__ __forceinline__ void tc_commit_multicast(uint64_t* bar, uint16_t cta_mask) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-            smem_u32(bar)),
-        "h"(cta_mask)
-        : "memory");
-}
-
 // D[tmem] (+)= A[smem] * B[smem]^T-style UMMA, both operands via descriptors.
 __device__ __forceinline__ void umma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
                                         uint32_t accumulate) {
@@ -216,88 +182,6 @@ __device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64
         "setp.ne.b32 p, %4, 0;\n\t"
         "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
         "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-// A whole K = 128 contraction (8 MMAs, K step 16) for operands with both
-// matrices in shared memory, K-major, 128-byte swizzled, D columns of bf16:
-// descriptor start addresses step by 32 bytes inside a swizzle row and by
-// 16 KiB to the next 64-column chunk.  One asm block keeps the issue tight.
-__device__ __forceinline__ void umma_ss_k128(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                             uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p, t;\n\t.reg .b64 a, b;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\tsetp.eq.u32 t, 0, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t"
-        "add.s64 a, %1, 2;\n\tadd.s64 b, %2, 2;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, t;\n\t"
-        "add.s64 a, %1, 4;\n\tadd.s64 b, %2, 4;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, t;\n\t"
-        "add.s64 a, %1, 6;\n\tadd.s64 b, %2, 6;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, t;\n\t"
-        "add.s64 a, %1, 1024;\n\tadd.s64 b, %2, 1024;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, t;\n\t"
-        "add.s64 a, %1, 1026;\n\tadd.s64 b, %2, 1026;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, t;\n\t"
-        "add.s64 a, %1, 1028;\n\tadd.s64 b, %2, 1028;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, t;\n\t"
-        "add.s64 a, %1, 1030;\n\tadd.s64 b, %2, 1030;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, t;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-// The same for K = 64 (4 MMAs, one 64-column chunk).
-__device__ __forceinline__ void umma_ss_k64(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
-                                            uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p, t;\n\t.reg .b64 a, b;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\tsetp.eq.u32 t, 0, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t"
-        "add.s64 a, %1, 2;\n\tadd.s64 b, %2, 2;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, t;\n\t"
-        "add.s64 a, %1, 4;\n\tadd.s64 b, %2, 4;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, t;\n\t"
-        "add.s64 a, %1, 6;\n\tadd.s64 b, %2, 6;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], a, b, %3, t;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-// O += P V over 128 keys: A = P in tensor memory (8 columns per K step of 16),
-// B = V in shared memory, MN-major, 128-byte swizzled (2 KiB per K step).
-__device__ __forceinline__ void umma_ts_k128(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                             uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p, t;\n\t.reg .b64 b;\n\t.reg .b32 a;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\tsetp.eq.u32 t, 0, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t"
-        "add.u32 a, %1, 8;\n\tadd.s64 b, %2, 128;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, t;\n\t"
-        "add.u32 a, %1, 16;\n\tadd.s64 b, %2, 256;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, t;\n\t"
-        "add.u32 a, %1, 24;\n\tadd.s64 b, %2, 384;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, t;\n\t"
-        "add.u32 a, %1, 32;\n\tadd.s64 b, %2, 512;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, t;\n\t"
-        "add.u32 a, %1, 40;\n\tadd.s64 b, %2, 640;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, t;\n\t"
-        "add.u32 a, %1, 48;\n\tadd.s64 b, %2, 768;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, t;\n\t"
-        "add.u32 a, %1, 56;\n\tadd.s64 b, %2, 896;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [a], b, %3, t;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-// Arrive on the mbarrier at the same shared-memory offset in CTA `cta` of the
-// cluster (release at cluster scope).
-__device__ __forceinline__ void mbar_arrive_cluster(uint64_t* bar, uint32_t cta) {
-    asm volatile(
-        "{\n\t.reg .b32 ra;\n\t"
-        "mapa.shared::cluster.u32 ra, %0, %1;\n\t"
-        "mbarrier.arrive.release.cluster.shared::cluster.b64 _, [ra];\n\t}" ::"r"(smem_u32(bar)),
-        "r"(cta)
         : "memory");
 }
 
@@ -328,16 +212,6 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint64_t* bar, uint32_t cta)
         ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),     \
         "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])              \
         : "memory")
-
-// Warpgroup register re-balancing (all four warps of a warpgroup execute it).
-template <uint32_t N>
-__device__ __forceinline__ void setmaxnreg_inc() {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
-}
-template <uint32_t N>
-__device__ __forceinline__ void setmaxnreg_dec() {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
-}
 
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
