@@ -38,3 +38,22 @@ def test_host_steps_match_device_step(bss, hpc, host_flags):
         assert bss.get_device_status() == 0
         for c in range(calls):
             assert torch.equal(outs[c].view(torch.int16), expect[c].view(torch.int16)), f"call {c}"
+
+
+@pytest.mark.gpu
+def test_head_local_path_on_one_rank_is_the_attention_step(bss):
+    from block_sparse_spatio_gb300.head_local import head_local_attention, make_attention_step
+    w = W.SMALL
+    q, k, v = W.qkv(w, H=4, seed=33)
+    dev = torch.device("cuda")
+    Q, K, V = (x.to(dev) for x in (q, k, v))
+    fl = torch.tensor([1, 0, 1, 0], dtype=torch.uint8, device=dev)
+    p = bss.MaskParams(w.F, w.Hs, w.Ws, w.d, w.wf, w.ws)
+    with bss.build_tile_map(p) as tm:
+        O = head_local_attention(Q, K, V, fl, make_attention_step(tm, 4, w.N, w.d, dev)).clone()
+        O2 = torch.empty_like(Q)
+        ws = [torch.empty_like(Q) for _ in range(4)]
+        bss.attention_step(Q, K, V, O2, tm, fl, *ws)
+        torch.cuda.synchronize()
+    assert bss.get_device_status() == 0
+    assert torch.equal(O.view(torch.int16), O2.view(torch.int16))
