@@ -76,7 +76,8 @@ EXPORTED = ("bss_build_tile_map", "bss_tile_map_stats", "bss_tile_map_dims", "bs
             "bss_destroy_tile_map", "bss_permute", "bss_sparse_attention", "bss_dense_attention",
             "bss_get_device_status", "bss_status_string", "bss_last_error_message", "bss_version",
             "bss_diag_mma_tile", "bss_build_tile_map_csr_noalloc", "bss_route_heads",
-            "bss_sparse_attention_fused", "bss_permute_flagged", "bss_sparse_attention_split")
+            "bss_sparse_attention_fused", "bss_permute_flagged", "bss_sparse_attention_split",
+            "bss_diag_wait_timeout")
 
 
 def load(path: str | None = None):
@@ -110,6 +111,8 @@ def load(path: str | None = None):
     lib.bss_sparse_attention_split.restype = st
     lib.bss_permute_flagged.argtypes = [p, p, p, i32, MP, i32, p]
     lib.bss_permute_flagged.restype = st
+    lib.bss_diag_wait_timeout.argtypes = [ctypes.c_int64, p, p]
+    lib.bss_diag_wait_timeout.restype = st
     lib.bss_dense_attention.argtypes = [p, p, p, p, p, i32, i32, i32, ctypes.c_float, p]
     lib.bss_dense_attention.restype = st
     lib.bss_get_device_status.argtypes = [p]
@@ -158,6 +161,20 @@ def _dev_tensor(t, name, dtype=None):
         raise ValueError(f"{name} must be contiguous")
     if dtype is not None and t.dtype != dtype:
         raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+
+
+def _check_shapes(tile_map, lse, *named):
+    """Every tensor [H][N][d] of the map's geometry (same H), lse [H][N]: a
+    map built for another geometry is refused before any launch."""
+    p = tile_map.params
+    N, d = p.F * p.Hs * p.Ws, p.head_dim
+    H = named[0][0].shape[0]
+    for t, n in named:
+        if tuple(t.shape) != (H, N, d):
+            raise ValueError(f"{n} has shape {tuple(t.shape)}, the tile map wants ({H}, {N}, {d})")
+    if lse is not None and tuple(lse.shape) != (H, N):
+        raise ValueError(f"lse has shape {tuple(lse.shape)}, the tile map wants ({H}, {N})")
+    return H
 
 
 class TileMap:
@@ -261,6 +278,7 @@ def sparse_attention(Q, K, V, O, tile_map: TileMap, head_is_temporal=None, lse=N
         _dev_tensor(t, n, torch.bfloat16)
     _dev_tensor(head_is_temporal, "head_is_temporal", torch.uint8)
     _dev_tensor(lse, "lse", torch.float32)
+    _check_shapes(tile_map, lse, (Q, "Q"), (K, "K"), (V, "V"), (O, "O"))
     _check(load().bss_sparse_attention(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(lse), tile_map.handle,
                                        _ptr(head_is_temporal), Q.shape[0], float(softmax_scale), _stream(stream)))
     return O
@@ -275,6 +293,8 @@ def sparse_attention_split(Q, K, V, O, Qt, Kt, Vt, Ot, tile_map: TileMap, head_i
         _dev_tensor(t, n, torch.bfloat16)
     _dev_tensor(head_is_temporal, "head_is_temporal", torch.uint8)
     _dev_tensor(lse, "lse", torch.float32)
+    _check_shapes(tile_map, lse, (Q, "Q"), (K, "K"), (V, "V"), (O, "O"), (Qt, "Qt"), (Kt, "Kt"), (Vt, "Vt"),
+                  (Ot, "Ot"))
     _check(load().bss_sparse_attention_split(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(Qt), _ptr(Kt), _ptr(Vt),
                                              _ptr(Ot), _ptr(lse), tile_map.handle, _ptr(head_is_temporal),
                                              Q.shape[0], float(softmax_scale), _stream(stream)))
@@ -290,6 +310,7 @@ def sparse_attention_fused(Q, K, V, O, tile_map: TileMap, head_is_temporal=None,
         _dev_tensor(t, n, torch.bfloat16)
     _dev_tensor(head_is_temporal, "head_is_temporal", torch.uint8)
     _dev_tensor(lse, "lse", torch.float32)
+    _check_shapes(tile_map, lse, (Q, "Q"), (K, "K"), (V, "V"), (O, "O"))
     _check(load().bss_sparse_attention_fused(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(lse), tile_map.handle,
                                              _ptr(head_is_temporal), Q.shape[0], float(softmax_scale),
                                              _stream(stream)))
@@ -315,6 +336,14 @@ def get_device_status(stream=None) -> int:
 
 def status_string(status: int) -> str:
     return load().bss_status_string(status).decode()
+
+
+def diag_wait_timeout(limit_ns: int, waited_ns=None, stream=None):
+    """Run a bounded wait that nothing completes (see include/bss_diag.h); the
+    device status word then holds BSS_ERR_TIMEOUT."""
+    import torch
+    _dev_tensor(waited_ns, "waited_ns", torch.int64)
+    _check(load().bss_diag_wait_timeout(int(limit_ns), _ptr(waited_ns), _stream(stream)))
 
 
 def diag_mma_tile(A, B, P, V, S, O, stream=None):

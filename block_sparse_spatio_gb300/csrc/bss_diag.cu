@@ -142,3 +142,35 @@ extern "C" bss_status bss_diag_mma_tile(const void* A, const void* B, const void
     if (d == 64) return diag_launch<64>(A, B, P, V, S, O, stream);
     return set_error(BSS_ERR_UNSUPPORTED, "d must be 64 or 128");
 }
+
+namespace bss {
+namespace {
+// An mbarrier with one expected arrival that never comes: the bounded wait
+// must give up, record BSS_ERR_TIMEOUT and return.
+__global__ void wait_timeout_kernel(uint64_t limit_ns, int64_t* waited_ns, int* status) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        mbar_fence_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        const uint64_t t0 = global_timer_ns();
+        const bool ok = mbar_wait(&bar, 0, status, limit_ns);
+        const uint64_t t1 = global_timer_ns();
+        if (waited_ns != nullptr) *waited_ns = ok ? -1 : static_cast<int64_t>(t1 - t0);
+    }
+}
+}  // namespace
+}  // namespace bss
+
+extern "C" bss_status bss_diag_wait_timeout(int64_t limit_ns, int64_t* waited_ns, cudaStream_t stream) {
+    using namespace bss;
+    if (limit_ns < 1000 || limit_ns > 1000000000ll) return set_error(BSS_ERR_INVALID_ARG, "limit_ns out of range");
+    if (waited_ns != nullptr && (reinterpret_cast<uintptr_t>(waited_ns) & 7u))
+        return set_error(BSS_ERR_INVALID_ARG, "waited_ns must be 8-byte aligned");
+    int* status = device_status_ptr();
+    if (status == nullptr) return set_error(BSS_ERR_CUDA, "cannot resolve the device status word");
+    wait_timeout_kernel<<<1, 32, 0, stream>>>(static_cast<uint64_t>(limit_ns), waited_ns, status);
+    return cuda_check(cudaGetLastError(), "wait timeout launch");
+}

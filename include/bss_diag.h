@@ -27,6 +27,16 @@ extern "C" {
 bss_status bss_diag_mma_tile(const void* A, const void* B, const void* P, const void* V, float* S, float* O,
                              int32_t d, cudaStream_t stream);
 
+/* Failure-detection check of the bounded waits every kernel uses: one CTA
+ * initialises an mbarrier that nothing ever arrives on and waits on it with
+ * the same bounded wait as the attention kernel, giving up after limit_ns
+ * nanoseconds (1e3 .. 1e9).  The wait records BSS_ERR_TIMEOUT in the device
+ * status word and the kernel returns normally, so the context stays usable;
+ * the host reads the status with bss_get_device_status.  *waited_ns (device
+ * int64, may be NULL) receives the time the wait took.
+ * Errors: INVALID_ARG (limit out of range, misaligned pointer), CUDA. */
+bss_status bss_diag_wait_timeout(int64_t limit_ns, int64_t* waited_ns, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -139,3 +139,14 @@ def test_noalloc_rejects_oversized_and_bad_buffers(lib):
     assert lib.bss_build_tile_map_csr_noalloc(ctypes.byref(small), 0, 128, 128, a, a, 10, a, None) == 1
     assert lib.bss_build_tile_map_csr_noalloc(ctypes.byref(small), 0, 128, 128, a, a, 1 << 20,
                                               ctypes.c_void_p(0x10004), None) == 1
+
+
+@pytest.mark.parametrize("limit", [0, 999, 1_000_000_001, -5])
+def test_wait_timeout_diag_rejects_limits_before_any_launch(lib, limit):
+    assert lib.bss_diag_wait_timeout(limit, None, None) == 1  # BSS_ERR_INVALID_ARG
+
+
+def test_permute_flagged_needs_flags(lib):
+    p = _params()
+    buf = ctypes.c_void_p(16)  # never dereferenced: the call is rejected on the host
+    assert lib.bss_permute_flagged(buf, ctypes.c_void_p(1 << 40), None, 2, ctypes.byref(p), 0, None) == 1
