@@ -54,6 +54,12 @@ def parse_args():
     ap.add_argument("--workload", default="mixed_75600tok_10h_d128")
     ap.add_argument("--heads", type=int, default=0, help="override head count (profiling runs)")
     ap.add_argument("--no-extras", action="store_true", help="skip variants, e2e and cpu baseline")
+    ap.add_argument("--rounding", type=int, default=0, choices=[0, 1, 2],
+                    help="mask of the timed step: 0 exact (B2, default), 1 tile-aligned (B3), 2 every visited "
+                         "tile masked (B1); profiling runs")
+    ap.add_argument("--dense", action="store_true",
+                    help="time the dense control (every tile, no permutation) instead of the sparse step; "
+                         "profiling runs")
     ap.add_argument("--cpu-rows-per-head", type=int, default=6144,
                     help="oracle sample of the cpu_baseline entry (about 20 s on 16 cores)")
     ap.add_argument("--ref-rows-per-head", type=int, default=256,
@@ -281,15 +287,26 @@ def main():
     O = torch.empty_like(Q)
     Qp, Kp, Vp, Op = (torch.empty_like(Q) for _ in range(4))
     fl = torch.tensor(flags, dtype=torch.uint8, device=dev)
-    params = bss.MaskParams(w.F, w.Hs, w.Ws, w.d, w.wf, w.ws, temporal_permuted=1, rounding=0)
+    params = bss.MaskParams(w.F, w.Hs, w.Ws, w.d, w.wf, w.ws, temporal_permuted=1, rounding=args.rounding)
     tm = bss.build_tile_map(params)
     st = (tm.stats(0), tm.stats(1))
     retained = sum(st[f]["retained_pairs"] for f in flags)
+    if args.dense:
+        retained = H * w.N * w.N
     flops = 4.0 * w.d * retained
     stream = torch.cuda.current_stream()
     attn_events = []
 
     def step(record=False):
+        if args.dense:
+            if record:
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+            bss.dense_attention(Q, K, V, O)
+            if record:
+                e1.record(stream)
+                attn_events.append((e0, e1))
+            return
         # temporal heads permuted into the workspaces, spatial heads used in place
         bss.permute(Q, Qp, fl, params, False, only_flagged=True)
         bss.permute(K, Kp, fl, params, False, only_flagged=True)
@@ -303,7 +320,7 @@ def main():
             attn_events.append((e0, e1))
         bss.permute(Op, O, fl, params, True, only_flagged=True)
 
-    launches_per_step = 5
+    launches_per_step = 1 if args.dense else 5
     for _ in range(max(3, args.warmup)):
         step()
     torch.cuda.synchronize()
@@ -344,8 +361,11 @@ def main():
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": w.name, "tokens": w.N, "frames_x_h_x_w": [w.F, w.Hs, w.Ws], "heads": H,
                    "head_dim": w.d, "flags_temporal": flags, "spatial_frame_window": w.wf,
-                   "temporal_raster_window": w.ws, "mask": "exact (full/boundary tiles, B2)", "tile": [128, 128],
-                   "step": "permute temporal heads' QKV -> sparse attention -> unpermute their O",
+                   "temporal_raster_window": w.ws, "mask": ("dense control" if args.dense else
+                            ["exact (full/boundary tiles, B2)", "tile-aligned (B3)",
+                             "every visited tile masked (B1)"][args.rounding]), "tile": [128, 128],
+                   "step": ("dense attention" if args.dense else
+                            "permute temporal heads' QKV -> sparse attention -> unpermute their O"),
                    "l2": f"inputs larger than L2 (Q+K+V = {3 * Q.numel() * 2 / 1e6:.0f} MB)",
                    "parallelism": "replicas" if world > 1 else "single GPU",
                    "retained_pairs": retained,
