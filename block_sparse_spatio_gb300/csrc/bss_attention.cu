@@ -210,7 +210,6 @@ __device__ __forceinline__ uint32_t entry_at(const AttnArgs& a, const int32_t* e
 template <int D, bool ROUTE, int HALVES>
 __global__ void __launch_bounds__(threads_for<HALVES>(), 1) attn_fwd_kernel(const __grid_constant__ AttnArgs args) {
     static_assert(HALVES == 1 || HALVES == 2, "one or two 128-row halves per CTA");
-    static_assert(!ROUTE || HALVES == 2, "routing uses the two-half shape");
     using L = Smem<D, HALVES>;
     constexpr int kBQt = HALVES * kHalf;  // query rows per CTA
     constexpr int kChunks = D / 64;  // 64-column (128-byte) swizzle atoms per row
@@ -465,7 +464,8 @@ __global__ void __launch_bounds__(threads_for<HALVES>(), 1) attn_fwd_kernel(cons
             if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_k_full, 0, status));
             if constexpr (HALVES == 1) {
                 // one half: S in two TMEM buffers (columns 0 / 128 by tile parity), so
-                // S(j+1) is issued before PV(j) and overlaps the softmax of tile j
+                // S(j+1) is issued before PV(j) and overlaps the softmax of tile j;
+                // the P-ready barrier is double-buffered the same way
                 if (ok) {
                     tc_fence_after();
                     issue_s(kColS, dq0, dk0);
@@ -485,7 +485,7 @@ __global__ void __launch_bounds__(threads_for<HALVES>(), 1) attn_fwd_kernel(cons
                         commit(bar_k_empty + st1);
                     }
                     ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_v_full + st, (j / kStages) & 1, status));
-                    if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_p_full + 0, j & 1, status));
+                    if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_p_full + (j & 1), (j >> 1) & 1, status));
                     if (!ok) break;
                     tc_fence_after();
                     issue_pv(kColO, kColS + 128 * (j & 1), dv0 + st * kStageStep, j > 0);
@@ -562,6 +562,12 @@ __global__ void __launch_bounds__(threads_for<HALVES>(), 1) attn_fwd_kernel(cons
             const uint32_t e = entry_at<ROUTE>(args, ents, j, code, j0);
             const int cls = static_cast<int>(e >> BSS_CLASS_SHIFT);
             const int c0 = static_cast<int>(e & BSS_TILE_INDEX_MASK) * kBKV;
+            // one half: the four softmax warps start every tile together.  S(j+1) is
+            // issued before PV(j), so without this a warp could run a tile ahead of
+            // another; the outputs then came out wrong when rows rescaled O after
+            // their first tile (found with keys whose magnitude grows along the
+            // sequence), so the warps are kept in step.
+            if constexpr (HALVES == 1) named_barrier_sync(3, 128);
             const uint32_t t_s = HALVES == 2 ? t_s0 : t_s0 + 128 * (j & 1);
             if constexpr (HALVES == 2)
                 ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_s_full + hf, j & 1, status));
@@ -704,7 +710,10 @@ __global__ void __launch_bounds__(threads_for<HALVES>(), 1) attn_fwd_kernel(cons
             }
             tmem_wait_st();
             tc_fence_before();
-            mbar_arrive(bar_p_full + hf);
+            // P ready: one barrier per half, or (one half) per tile parity, since a
+            // warp may start tile j+1 (its S is issued before PV(j)) while another
+            // is still in tile j; it cannot start tile j+2, whose S waits for PV(j)
+            mbar_arrive(bar_p_full + (HALVES == 2 ? hf : (j & 1)));
         }
         // ---- epilogue: O / l -> bf16 -> swizzled staging (reuses this half's Q) -> TMA store
         uint8_t* stage = sQ + hf * L::kTile;
@@ -856,12 +865,12 @@ bss_status launch_d(const AttnLaunch& a, cudaStream_t stream) {
     const float scale = a.softmax_scale > 0.0f ? a.softmax_scale : 1.0f / sqrtf(static_cast<float>(a.d));
     args.scale_log2 = scale * 1.4426950408889634f;
 
-    // one or two 128-row q halves per CTA: the map's BQ (dense control and
-    // routing use two)
-    const int halves = (a.route || a.dense) ? 2 : a.bq / kHalf;
+    // one or two 128-row q halves per CTA: the map's BQ, or the routing call's
+    // choice (the dense control uses two)
+    const int halves = a.dense ? 2 : a.bq / kHalf;
     if (halves != 1 && halves != 2) return set_error(BSS_ERR_UNSUPPORTED, "query tile of %d rows", a.bq);
     const uint32_t smem = halves == 2 ? Smem<D, 2>::kAlloc : Smem<D, 1>::kAlloc;
-    auto kernel = a.route ? attn_fwd_kernel<D, true, 2>
+    auto kernel = a.route ? (halves == 2 ? attn_fwd_kernel<D, true, 2> : attn_fwd_kernel<D, true, 1>)
                           : (halves == 2 ? attn_fwd_kernel<D, false, 2> : attn_fwd_kernel<D, false, 1>);
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return cuda_check(e, "cudaFuncSetAttribute(attention)");

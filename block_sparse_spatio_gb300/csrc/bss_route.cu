@@ -121,7 +121,10 @@ extern "C" bss_status bss_route_heads(const void* Q, const void* K, const void* 
     const int d = params->head_dim;
     const int S = params->Hs * params->Ws;
     const int N = params->F * S;
-    const int nq = (R + attention_block_q() - 1) / attention_block_q();
+    // one 128-row MMA half per CTA when the sampled rows fit in it (no padding
+    // rows computed), else 256-row tiles
+    const int bq = R <= 128 ? 128 : attention_block_q();
+    const int nq = (R + bq - 1) / bq;
     const int nkv = (N + attention_block_kv() - 1) / attention_block_kv();
     // kv splits: enough CTAs for one wave of the GPU
     const int64_t base = 3ll * H * nq;
@@ -163,6 +166,7 @@ extern "C" bss_status bss_route_heads(const void* Q, const void* K, const void* 
         a.ws = params->temporal_raster_window;
         a.nq = nq;
         a.route = 1;
+        a.bq = bq;
         a.Nq = R;
         a.splits = splits;
         a.qmap = rows;

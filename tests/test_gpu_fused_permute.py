@@ -57,6 +57,21 @@ def test_fused_bit_identical_to_explicit_and_matches_oracle(bss, case, rounding)
 
 
 @pytest.mark.gpu
+def test_fused_bit_identical_with_rescales_after_the_first_tile(bss):
+    # keys growing along the sequence force O rescales on later tiles
+    F, Hs, Ws, d, wf, ws, flags = 8, 16, 24, 128, 2, 40, [1, 0]
+    N = F * Hs * Ws
+    q, k, v = W.qkv(W.SMALL, H=2, N=N, d=d, seed=92)
+    ramp = (1.0 + 7.0 * torch.arange(N, dtype=torch.float32) / N).view(1, N, 1)
+    k = (k.float() * ramp).to(torch.bfloat16)
+    p = bss.MaskParams(F, Hs, Ws, d, wf, ws, temporal_permuted=1, rounding=0)
+    o_ref, lse_ref, _ = run_gpu(bss, q, k, v, flags, p)
+    o_f, lse_f = run_fused(bss, q, k, v, flags, p)
+    assert torch.equal(o_f.view(torch.int32), o_ref.view(torch.int32))
+    assert torch.equal(lse_f.view(torch.int32), lse_ref.view(torch.int32))
+
+
+@pytest.mark.gpu
 def test_fused_zero_query_coverage_is_exact(bss):
     # Q = 0: exp(LSE) counts the keys each row sees (frame-0 sink + raster band)
     F, Hs, Ws, d, wf, ws = 8, 16, 24, 128, 2, 40
