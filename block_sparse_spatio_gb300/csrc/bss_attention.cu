@@ -10,11 +10,12 @@
 // mask (section "Align the sparse mask with final execution").
 //
 // GB300 design.  One CTA per (head, 256-row q tile), 384 threads.  The q tile
-// is two 128-row halves that share every K/V tile brought into shared memory,
-// which halves the L2 -> SM traffic per FLOP compared with 128-row tiles (at
-// 128 rows the kernel ran at the L2 bandwidth limit).
+// is two 128-row halves that share every K/V tile brought into shared memory
+// (half the L2 -> SM bytes and TMA operations per FLOP of 128-row tiles) and
+// whose softmaxes alternate with each other's MMAs.  A one-half instance
+// (128-row tiles, 256 threads, S double-buffered in TMEM) serves 128-row maps.
 //   warp 0       TMA producer: Q (both halves) once, then K and V tiles of the
-//                list into separate KV_STAGES-deep rings (128-byte swizzled,
+//                list into separate kStages-deep rings (128-byte swizzled,
 //                64-column boxes).
 //   warp 1       TMEM allocator and single-thread tcgen05.mma issuer; it
 //                waits with the suspending try_wait, which leaves the issue
