@@ -104,11 +104,35 @@ def load_peaks():
         return dict(FALLBACK_PEAKS), "fallback"
 
 
+def _code_only(text: str) -> str:
+    """C++ source without comments and with whitespace collapsed: what the
+    compiler sees (a comment edit does not change the kernel)."""
+    out, i, n = [], 0, len(text)
+    while i < n:
+        if text.startswith("//", i):
+            j = text.find("\n", i)
+            i = n if j < 0 else j
+        elif text.startswith("/*", i):
+            j = text.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+        elif text[i] == '"':
+            j = i + 1
+            while j < n and text[j] != '"':
+                j += 2 if text[j] == "\\" else 1
+            out.append(text[i:j + 1])
+            i = j + 1
+        else:
+            out.append(text[i])
+            i += 1
+    return " ".join("".join(out).split())
+
+
 def source_hash():
+    """Hash of the attention kernel's code (comments and layout excluded)."""
     h = hashlib.sha256()
     for rel in ATTN_SOURCES:
-        with open(os.path.join(ROOT, rel), "rb") as fh:
-            h.update(fh.read())
+        with open(os.path.join(ROOT, rel), encoding="utf-8") as fh:
+            h.update(_code_only(fh.read()).encode())
     return h.hexdigest()[:16]
 
 
