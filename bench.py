@@ -436,6 +436,29 @@ def _time(torch, fn, reps=5, warm=3):
     return statistics.median(a.elapsed_time(b) for a, b in ev)
 
 
+def _time_interleaved(torch, fns, rounds=9, warm=2):
+    """Median time of each of several launches compared with one another: every
+    round times each once, in an order rotated from round to round, so clock
+    drift under the power cap falls on all of them alike."""
+    names = list(fns)
+    for _ in range(warm):
+        for n in names:
+            fns[n]()
+    torch.cuda.synchronize()
+    s = torch.cuda.current_stream()
+    ev = {n: [] for n in names}
+    for r in range(rounds):
+        for i in range(len(names)):
+            n = names[(i + r) % len(names)]
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(s)
+            fns[n]()
+            b.record(s)
+            ev[n].append((a, b))
+    torch.cuda.synchronize()
+    return {n: statistics.median(a.elapsed_time(b) for a, b in ev[n]) for n in names}
+
+
 def variants(bss, torch, W, w, H, Q, K, V, dev, peaks, flags):
     """Attention-kernel timings of the pages' other measurements, same inputs."""
     out = {}
@@ -445,27 +468,41 @@ def variants(bss, torch, W, w, H, Q, K, V, dev, peaks, flags):
     out["dense_control"] = {"ms": dense_ms, "tflops": dense_flops / dense_ms / 1e9,
                             "frac_of_peak": dense_flops / dense_ms / 1e9 / peaks["bf16_tflops"]}
     zeros = torch.zeros(H, dtype=torch.uint8, device=dev)
-    for name, rnd in (("spatial_naive_B1", 2), ("spatial_exact_B2", 0), ("spatial_tile_aligned_B3", 1)):
-        p = bss.MaskParams(w.F, w.Hs, w.Ws, w.d, w.wf, w.ws, temporal_permuted=1, rounding=rnd)
-        with bss.build_tile_map(p) as tm:
-            s0 = tm.stats(0)
-            ms = _time(torch, lambda: bss.sparse_attention(Q, K, V, O, tm, zeros))
+    # the pages' B1 -> B2 -> B3 progression, timed interleaved
+    bvars = (("spatial_naive_B1", 2), ("spatial_exact_B2", 0), ("spatial_tile_aligned_B3", 1))
+    maps = {name: bss.build_tile_map(bss.MaskParams(w.F, w.Hs, w.Ws, w.d, w.wf, w.ws, temporal_permuted=1,
+                                                    rounding=rnd)) for name, rnd in bvars}
+    try:
+        bms = _time_interleaved(torch, {name: (lambda tm=tm: bss.sparse_attention(Q, K, V, O, tm, zeros))
+                                        for name, tm in maps.items()})
+        for name, _ in bvars:
+            s0 = maps[name].stats(0)
+            ms = bms[name]
             fl_ = 4.0 * w.d * H * s0["retained_pairs"]
             out[name] = {"ms": ms, "tflops": fl_ / ms / 1e9, "frac_of_peak": fl_ / ms / 1e9 / peaks["bf16_tflops"],
                          "speedup_vs_dense": dense_ms / ms, "retained_fraction": s0["retained_pairs"] / w.N ** 2,
                          "tiles": s0}
+    finally:
+        for tm in maps.values():
+            tm.destroy()
     out["tile_shape_sweep"] = tile_shape_sweep(bss, torch, w)
     # latency side of the sweep: the kernel at both query-tile heights it runs
     pe = bss.MaskParams(w.F, w.Hs, w.Ws, w.d, w.wf, w.ws, temporal_permuted=1, rounding=0)
     zeros_ = torch.zeros(H, dtype=torch.uint8, device=dev)
     lat = {}
-    for bq in bss.ATTN_BQ_SUPPORTED:
-        with bss.build_tile_map(pe, BQ=bq) as tmq:
+    qmaps = {bq: bss.build_tile_map(pe, BQ=bq) for bq in bss.ATTN_BQ_SUPPORTED}
+    try:
+        qms = _time_interleaved(torch, {bq: (lambda tmq=tmq: bss.sparse_attention(Q, K, V, O, tmq, zeros_))
+                                        for bq, tmq in qmaps.items()})
+        for bq, tmq in qmaps.items():
             st0 = tmq.stats(0)
-            ms = _time(torch, lambda: bss.sparse_attention(Q, K, V, O, tmq, zeros_))
+            ms = qms[bq]
             ex = st0["full"] + st0["boundary"] + st0["pad"]
             lat[f"BQ{bq}_BKV128"] = {"ms": ms, "tflops": 4.0 * w.d * H * st0["retained_pairs"] / ms / 1e9,
                                      "masked_share": (st0["boundary"] + st0["pad"]) / ex}
+    finally:
+        for tmq in qmaps.values():
+            tmq.destroy()
     out["tile_shape_latency_spatial"] = lat
     ones = torch.ones(H, dtype=torch.uint8, device=dev)
     Qp, Kp, Vp, Op = (torch.empty_like(Q) for _ in range(4))
@@ -478,10 +515,12 @@ def variants(bss, torch, W, w, H, Q, K, V, dev, peaks, flags):
         def with_perm():
             bss.attention_step(Q, K, V, O, tm1, ones, Qp, Kp, Vp, Op)
 
-        ms_perm = _time(torch, with_perm)
-        ms_attn = _time(torch, lambda: bss.sparse_attention(Qp, Kp, Vp, Op, tm1, ones))
-        ms_noperm = _time(torch, lambda: bss.sparse_attention(Q, K, V, O, tm0, ones))
-        ms_fused = _time(torch, lambda: bss.sparse_attention_fused(Q, K, V, O, tm1, ones))
+        tms = _time_interleaved(torch, {
+            "perm": with_perm,
+            "attn": lambda: bss.sparse_attention(Qp, Kp, Vp, Op, tm1, ones),
+            "noperm": lambda: bss.sparse_attention(Q, K, V, O, tm0, ones),
+            "fused": lambda: bss.sparse_attention_fused(Q, K, V, O, tm1, ones)}, rounds=5)
+        ms_perm, ms_attn, ms_noperm, ms_fused = tms["perm"], tms["attn"], tms["noperm"], tms["fused"]
         out["temporal_heads"] = {
             "with_permutation_ms": ms_perm, "attention_only_ms": ms_attn, "in_kernel_indexing_ms": ms_noperm,
             "fused_permutation_ms": ms_fused,
@@ -495,8 +534,10 @@ def variants(bss, torch, W, w, H, Q, K, V, dev, peaks, flags):
         def explicit_step():
             bss.attention_step(Q, K, V, O, tm1, fl_mixed, Qp, Kp, Vp, Op)
 
-        ms_exp = _time(torch, explicit_step)
-        ms_fst = _time(torch, lambda: bss.sparse_attention_fused(Q, K, V, O, tm1, fl_mixed))
+        mms = _time_interleaved(torch, {"explicit": explicit_step,
+                                        "fused": lambda: bss.sparse_attention_fused(Q, K, V, O, tm1, fl_mixed)},
+                                rounds=5)
+        ms_exp, ms_fst = mms["explicit"], mms["fused"]
         out["mixed_step_fused_permutation"] = {
             "explicit_step_ms": ms_exp, "fused_ms": ms_fst, "tflops_fused": mixed_fl / ms_fst / 1e9,
             "speedup": ms_exp / ms_fst,

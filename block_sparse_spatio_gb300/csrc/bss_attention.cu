@@ -719,6 +719,10 @@ __global__ void __launch_bounds__(threads_for<HALVES>(), 1) attn_fwd_kernel(cons
         // ---- epilogue: O / l -> bf16 -> swizzled staging (reuses this half's Q) -> TMA store
         uint8_t* stage = sQ + hf * L::kTile;
         if (ok && n > 0) ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_o_done + hf, (n - 1) & 1, status));
+        // a q tile with no kv tiles (a rounded mask can drop all of them) computes
+        // nothing, but its Q load was issued: let it land before the staging
+        // buffer, which is this half's Q, is overwritten with the zero rows
+        if (ok && n == 0) ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_q, 0, status));
         if (ok) {
             tc_fence_after();
             const float inv_l = l > 0.0f ? 1.0f / l : 0.0f;

@@ -17,6 +17,14 @@ SMALL_CASES = [  # name, F, Hs, Ws, d, wf, ws, flags
     ("ragged_s63_d64", 5, 7, 9, 64, 1, 5, [1, 0]),
     ("ragged_s130_d128", 3, 10, 13, 128, 0, 20, [1, 1, 0]),
     ("ragged_s130_d64", 3, 10, 13, 64, 1, 200, [0, 1]),
+    # degenerate geometries: one token, one frame, one raster position, fewer
+    # tokens than a tile, zero-width windows (a row keeps its own frame / raster
+    # position and frame 0)
+    ("one_token", 1, 1, 1, 64, 0, 0, [0, 1]),
+    ("one_frame_s300", 1, 12, 25, 128, 0, 3, [1, 0]),
+    ("one_position_f130", 130, 1, 1, 128, 2, 0, [1, 0]),
+    ("n100_below_a_tile", 4, 5, 5, 128, 1, 2, [1, 0]),
+    ("windows_zero", 3, 10, 13, 128, 0, 0, [1, 0]),
 ]
 
 
@@ -108,6 +116,51 @@ def test_poisoned_excluded_keys_leave_output_bit_identical(bss, tperm):
     assert torch.equal(out1[1, rows1], out2[1, rows1])
     assert torch.equal(lse1[1, rows1], lse2[1, rows1])
     assert not torch.equal(out1[0, :S], out2[0, :S])  # frame-0 queries do see frames 1..2
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("path", ["step", "bq128", "fused"])
+def test_rounded_mask_with_empty_q_tiles_gives_zero_rows(bss, path):
+    # One raster position, 130 frames: a spatial row keeps 6 keys, so the rounded
+    # mask drops every tile of the spatial heads at BQ = 256 and all but the
+    # 2 x 2 tile of the last two frames at BQ = 128; rows of a q tile with an
+    # empty list get O = 0, LSE = -inf.  The temporal head keeps every frame.
+    # Q is large, so a Q row leaking into the output (the zero rows are staged
+    # in Q's shared-memory buffer) would show; the launch is repeated because
+    # such a leak depends on timing.
+    F, Hs, Ws, d, wf, ws = 130, 1, 1, 128, 2, 0
+    N = F
+    flags = [0, 1, 0]
+    q, k, v = _inputs(3, N, d, seed=81)
+    q[0] = 100.0
+    q[2] = -60.0
+    p = bss.MaskParams(F, Hs, Ws, d, wf, ws, temporal_permuted=1, rounding=1)
+    g = oracle.Geometry(F, Hs, Ws, wf=wf, ws=ws, bkv=128)
+    BQ = 128 if path == "bq128" else bss.ATTN_BQ
+    ref = {h: oracle_rows(q, k, v, h, oracle_kind(flags[h], 1), g, None, True, BQ=BQ) for h in range(3)}
+    empty = {h: np.isneginf(ref[h][1]) for h in (0, 2)}
+    assert all(e[:128].all() for e in empty.values())  # the first q tile has an empty list
+    dev = torch.device("cuda")
+    Q, K, V = (x.to(dev) for x in (q, k, v))
+    fl = torch.tensor(flags, dtype=torch.uint8, device=dev)
+    ws_ = [torch.empty_like(Q) for _ in range(4)]
+    with bss.build_tile_map(p, BQ=BQ) as tm:
+        for it in range(10):
+            O = torch.full_like(Q, 3.0)
+            lse = torch.zeros(3, N, device=dev)
+            if path == "fused":
+                bss.sparse_attention_fused(Q, K, V, O, tm, fl, lse=lse)
+            else:
+                bss.attention_step(Q, K, V, O, tm, fl, *ws_, lse=lse)
+            torch.cuda.synchronize()
+            assert bss.get_device_status() == 0
+            for h in (0, 2):
+                e = torch.from_numpy(empty[h])
+                assert torch.count_nonzero(O[h].cpu()[e]).item() == 0, f"launch {it} head {h}: O is not zero"
+                assert torch.all(torch.isneginf(lse[h].cpu()[e])), f"launch {it} head {h}: LSE is not -inf"
+    for h in range(3):
+        lrow = lse[h].cpu()  # one raster position: the permutation is the identity
+        compare(O[h].float().cpu().numpy(), lrow.numpy(), ref[h][0], ref[h][1], f"{path} head {h}")
 
 
 def _full_size(bss, wl, tperm, rounding, heads, nrows):

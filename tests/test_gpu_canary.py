@@ -22,11 +22,12 @@ def intact(buf, fill):
     return bool(torch.all(buf[:G] == fill)) and bool(torch.all(buf[-G:] == fill))
 
 
-GEOMS = [(5, 7, 9, 64, 1, 5, [1, 0]), (3, 10, 13, 128, 0, 20, [1, 1, 0])]
+GEOMS = [(5, 7, 9, 64, 1, 5, [1, 0]), (3, 10, 13, 128, 0, 20, [1, 1, 0]), (1, 1, 1, 64, 0, 0, [1, 0]),
+         (4, 5, 5, 128, 1, 2, [0, 1])]
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("geom", GEOMS, ids=["s63_d64", "s130_d128"])
+@pytest.mark.parametrize("geom", GEOMS, ids=["s63_d64", "s130_d128", "one_token", "n100"])
 @pytest.mark.parametrize("path", ["step", "explicit", "fused", "dense", "bq128"])
 def test_attention_writes_only_its_outputs(bss, geom, path):
     F, Hs, Ws, d, wf, ws, flags = geom

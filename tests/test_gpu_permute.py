@@ -10,6 +10,10 @@ CASES = [  # F, Hs, Ws, d, flags
     (8, 16, 24, 128, [0, 1]),
     (5, 7, 9, 64, [1, 0, 1]),
     (3, 10, 13, 128, [1, 1]),
+    (1, 1, 1, 64, [1, 0]),      # one token
+    (1, 12, 25, 128, [1]),      # one frame: the permutation is the identity
+    (130, 1, 1, 128, [0, 1]),   # one raster position: the identity too
+    (4, 5, 5, 64, [1]),         # fewer rows than one thread block covers
 ]
 
 

@@ -62,6 +62,17 @@ def test_tile_map_tiny_golden(bss):
         assert (st["full"], st["boundary"], st["skip"], st["retained_pairs"]) == (12, 0, 4, 49152)
 
 
+@pytest.mark.gpu
+def test_tile_map_destroy_is_idempotent_and_blocks_use(bss):
+    w = W.TINY
+    tm = bss.build_tile_map(bss.MaskParams(w.F, w.Hs, w.Ws, w.d, w.wf, w.ws), 64, 64)
+    assert tm.dims(0)[0] == 4
+    bss.destroy_tile_map(tm)
+    bss.destroy_tile_map(tm)  # a second destroy is a no-op
+    with pytest.raises(ValueError):
+        tm.stats(0)
+
+
 def closed_form_spatial(F, S, wf):
     return S * S * sum(min(f + wf, F - 1) - max(f - wf, 0) + 1 + (1 if f > wf else 0) for f in range(F))
 

@@ -337,6 +337,32 @@ def test_attention_rounded_mask_vs_bruteforce(g, kind):
     _oracle_vs_torch(*g, kind=kind, rounding=1)
 
 
+@pytest.mark.parametrize("BQ", [128, 256])
+def test_rounded_mask_rows_left_empty_give_zero_and_minus_infinity(BQ):
+    # One raster position and 130 frames: a spatial row keeps 6 of 128 keys in its
+    # tiles, so rounding drops all tiles of the first q tile (and at BQ = 256 every
+    # tile); an empty row's output is 0 and its LSE -inf, the rest is the textbook
+    # softmax over the kept tiles.
+    F, Hs, Ws, wf, ws, BKV, d = 130, 1, 1, 2, 0, 128, 64
+    N = F
+    q, k, v = rand_head(N, d, 12)
+    gg = geom(F, Hs, Ws, wf, ws, BKV)
+    O, lse = oracle.attention(bits(q), bits(k), bits(v), SPATIAL, gg, rounding=True, BQ=BQ, BKV=BKV)
+    M, col_tok, col_real, pt = layout_mask(SPATIAL, F, Hs, Ws, wf, ws, BKV)
+    _, cls = tile_classes(M, col_real, BQ, BKV, 1)
+    keep = np.repeat(np.repeat(cls != oracle.SKIP, BQ, 0), BKV, 1)[:N, :N]
+    M = keep & col_real[None, :]
+    empty = ~M.any(axis=1)
+    assert empty[:128].all() and empty.all() == (BQ == 256)
+    assert np.all(O[empty] == 0.0) and np.all(np.isneginf(lse[empty]))
+    live = ~empty
+    if live.any():
+        Qf, Kf, Vf = q.double(), k.double(), v.double()
+        Ol, ll = torch_attention(Qf[live], Kf, Vf, torch.from_numpy(M[live]), 1.0 / np.sqrt(d))
+        np.testing.assert_allclose(O[live], Ol.numpy(), rtol=0, atol=1e-12)
+        np.testing.assert_allclose(lse[live], ll.numpy(), rtol=0, atol=1e-12)
+
+
 def test_attention_d128_small_rows_subset():
     w = W.SMALL
     q, k, v = W.qkv(w)

@@ -6,7 +6,8 @@ and enforces its own limit, or a latency-critical loop where cudaMalloc /
 cudaFree would synchronize the device.  It keeps its scratch in a fixed
 __device__ array that every call shares, so this test makes two calls in a row
 (a large map, then a smaller one of a different kind) through the C ABI and
-compares each, bit for bit, with what bss_build_tile_map produces.  It lives in
+compares each (the first made through the C ABI, the second through the
+Python binding), bit for bit, with what bss_build_tile_map produces.  It lives in
 its own file so that pytest collects it last."""
 import ctypes
 
@@ -33,13 +34,16 @@ def test_noalloc_tile_map_matches_allocating_build_on_two_calls_in_a_row(bss):
         row_ptr = torch.full((nq + 1,), -7, dtype=torch.int32, device=dev)
         entries = torch.full((nq * nkv,), -7, dtype=torch.int32, device=dev)
         stats = torch.full((6,), -7, dtype=torch.int64, device=dev)
-        mp = p.c()
-        st = lib.bss_build_tile_map_csr_noalloc(ctypes.byref(mp), kind, BQ, BKV,
-                                                ctypes.c_void_p(row_ptr.data_ptr()),
-                                                ctypes.c_void_p(entries.data_ptr()), entries.numel(),
-                                                ctypes.c_void_p(stats.data_ptr()),
-                                                ctypes.c_void_p(stream.cuda_stream))
-        assert st == 0, lib.bss_last_error_message()
+        if w is W.SMALL:  # through the Python binding
+            bss.build_tile_map_csr_noalloc(p, kind, row_ptr, entries, stats, BQ, BKV, stream=stream)
+        else:  # straight through the C ABI
+            mp = p.c()
+            st = lib.bss_build_tile_map_csr_noalloc(ctypes.byref(mp), kind, BQ, BKV,
+                                                    ctypes.c_void_p(row_ptr.data_ptr()),
+                                                    ctypes.c_void_p(entries.data_ptr()), entries.numel(),
+                                                    ctypes.c_void_p(stats.data_ptr()),
+                                                    ctypes.c_void_p(stream.cuda_stream))
+            assert st == 0, lib.bss_last_error_message()
         torch.cuda.synchronize()
         assert bss.get_device_status() == 0
         with bss.build_tile_map(p, BQ, BKV) as tm:
