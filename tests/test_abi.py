@@ -150,3 +150,52 @@ def test_permute_flagged_needs_flags(lib):
     p = _params()
     buf = ctypes.c_void_p(16)  # never dereferenced: the call is rejected on the host
     assert lib.bss_permute_flagged(buf, ctypes.c_void_p(1 << 40), None, 2, ctypes.byref(p), 0, None) == 1
+
+
+def _cuda_include():
+    for root in (os.environ.get("CUDA_HOME"), os.environ.get("CUDA_PATH"), "/usr/local/cuda"):
+        if root and os.path.exists(os.path.join(root, "include", "cuda_runtime_api.h")):
+            return os.path.join(root, "include")
+    pytest.skip("no CUDA headers")
+
+
+@pytest.mark.parametrize("lang", ["c99", "c++17"])
+def test_headers_compile_as_plain_c_and_cxx_and_link(lib, tmp_path, lang):
+    """A program that includes only include/*.h, takes the address of every
+    declared entry point, and calls host-side ones, builds with gcc / g++ and
+    links against the shared library: the headers are the whole interface."""
+    import shutil
+    import subprocess
+    cc = "gcc" if lang == "c99" else "g++"
+    if shutil.which(cc) is None:
+        pytest.skip(f"no {cc}")
+    names = declared_functions()
+    table = "\n".join(f"    (fnptr)&{n}," for n in names)
+    src = f"""#include <stdio.h>
+#include "bss.h"
+#include "bss_diag.h"
+
+typedef void (*fnptr)(void);
+static const fnptr every_entry_point[] = {{
+{table}
+}};
+
+int main(void) {{
+    bss_tile_map h = 0;
+    bss_status st = bss_build_tile_map(NULL, 128, 128, &h, 0);
+    printf("%d %d %s %s %d\\n", (int)(sizeof(every_entry_point) / sizeof(every_entry_point[0])), bss_version(),
+           bss_status_string(BSS_ERR_TIMEOUT), bss_status_string(st), h == 0);
+    return st == BSS_ERR_INVALID_ARG ? 0 : 1;
+}}
+"""
+    prog = tmp_path / "prog.c"
+    prog.write_text(src)
+    libdir = os.path.dirname(lib._name)
+    flags = ["-std=c99"] if lang == "c99" else ["-std=c++17", "-x", "c++"]
+    cmd = [cc, *flags, "-Wall", "-Wextra", "-Werror", "-I", os.path.join(ROOT, "include"), "-I", _cuda_include(),
+           str(prog), "-L", libdir, "-lbss", f"-Wl,-rpath,{libdir}", "-o", str(tmp_path / "prog")]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([str(tmp_path / "prog")], capture_output=True, text=True)
+    assert r.returncode == 0, r.stdout + r.stderr
+    assert r.stdout.split() == [str(len(names)), str(lib.bss_version()), "BSS_ERR_TIMEOUT", "BSS_ERR_INVALID_ARG", "1"]
