@@ -50,10 +50,11 @@ def test_route_random_heads_match_oracle(bss, wl):
 
 
 @pytest.mark.gpu
-def test_route_more_rows_than_one_query_tile_and_ragged_geometry(bss):
+@pytest.mark.parametrize("d", [128, 64])
+def test_route_more_rows_than_one_query_tile_and_ragged_geometry(bss, d):
     # 300 sampled rows span two 256-row query tiles; N = 390 is not a multiple of
     # the 128-key tile (padding columns in the last kv tile)
-    F, Hs, Ws, d, wf, ws = 3, 10, 13, 128, 0, 20
+    F, Hs, Ws, wf, ws = 3, 10, 13, 0, 20
     N = F * Hs * Ws
     q, k, v = W.qkv(W.SMALL, H=3, N=N, d=d, seed=31)
     g = torch.Generator().manual_seed(7)
