@@ -26,10 +26,11 @@
 //                gives each half's softmax one full MMA tile of time.
 //   warps 4..7   softmax of half 0, warps 8..11 softmax of half 1: one thread
 //                per query row (= TMEM lane).  Reads S, masks boundary /
-//                padding tiles, keeps the running max with a lazy rescale (O
-//                and l are rescaled only when the max grows by more than 2^8),
-//                writes bf16 P to TMEM; finally normalises O, stores it with a
-//                TMA store and writes the LSE.
+//                padding tiles, keeps a reference max with a lazy rescale (a
+//                tile is exponentiated against the reference and kept unless a
+//                row's sum of P over the tile exceeds 2^16; only then are the
+//                max, O and l moved), writes bf16 P to TMEM; finally
+//                normalises O, stores it with a TMA store and writes the LSE.
 // tcgen05.mma operations issued by one thread execute in issue order, so an S
 // that overwrites P_h is issued after the PV that reads it.  Every mbarrier
 // wait is bounded; on a timeout the status word is set and all roles unwind to
@@ -59,7 +60,15 @@ constexpr int kStages = 2;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kColS = 0;    // S_h at kColS + 128 h (P_h over its first 64 columns)
 constexpr uint32_t kColO = 256;  // O_h at kColO + 128 h
-constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale when max grows by > 256x
+// Lazy rescale.  The fast path exponentiates a tile against the row's reference
+// max and keeps the result unless the row's sum of P over the tile exceeds 2^16
+// (then no P exceeds 2^16: bf16 P and the fp32 O and l stay far from overflow).
+// Checking the sum, which the row needs anyway, instead of a tile max saves one
+// instruction per pair of scores.  A tile that fails the check holds a P above
+// 2^9, so the general path, which moves the reference when the tile max is more
+// than 2^8 above it, always moves it there.
+constexpr float kRescaleThreshold = 8.0f;  // log2 units (general path)
+constexpr float kSumLimit = 65536.0f;      // fast path
 
 struct AttnArgs {
     CUtensorMap tm_q, tm_k, tm_v, tm_o, tm_ks, tm_vs;
@@ -577,17 +586,16 @@ __global__ void __launch_bounds__(threads_for<HALVES>(), 1) attn_fwd_kernel(cons
             if (!ok) break;
             tc_fence_after();
             // ---- fast path: every row of the warp already has a finite reference
-            // max.  One pass: exponentiate against the current reference while
-            // tracking the tile max (FULL tiles without any mask, boundary / padding
-            // tiles through their bitmask); the result is kept unless some row's max
-            // grew by more than 2^8 (then the tile is redone on the general path).
+            // max.  One pass: exponentiate against the current reference (FULL tiles
+            // without any mask, boundary / padding tiles through their bitmask); the
+            // result is kept unless some row's sum of P exceeds kSumLimit (then the
+            // tile is redone on the general path).
             bool done = false;
             // one pass over the four 32-column chunks; MASKED applies the tile's
             // retained-column bitmask (boundary / padding tiles)
             auto single_pass = [&](auto masked_tag, const uint32_t (&bits)[4]) -> bool {
                 constexpr bool MASKED = decltype(masked_tag)::value;
                 uint32_t pk[64];
-                float cm0 = -INFINITY, cm1 = -INFINITY;
                 uint64_t s2a = 0ull, s2b = 0ull;  // packed partial sums (two chains)
                 const uint64_t c2 = f2_pack(c, c);
                 const uint64_t nm2 = f2_pack(-m, -m);
@@ -603,10 +611,6 @@ __global__ void __launch_bounds__(threads_for<HALVES>(), 1) attn_fwd_kernel(cons
                             x0 = ((bits[cc] >> (2 * i)) & 1u) ? x0 : -INFINITY;
                             x1 = ((bits[cc] >> (2 * i + 1)) & 1u) ? x1 : -INFINITY;
                         }
-                        if (i & 1)
-                            cm1 = fmax3(cm1, x0, x1);
-                        else
-                            cm0 = fmax3(cm0, x0, x1);
                         float y0, y1;
                         f2_unpack(f2_fma(f2_pack(x0, x1), c2, nm2), y0, y1);
                         const float p0 = ex2_approx(y0), p1 = ex2_approx(y1);
@@ -618,12 +622,12 @@ __global__ void __launch_bounds__(threads_for<HALVES>(), 1) attn_fwd_kernel(cons
                         pk[16 * cc + i] = pack_bf16x2(p0, p1);
                     }
                 }
-                const float tmax_s = fmaxf(cm0, cm1) * c;
-                if (__any_sync(0xFFFFFFFFu, tmax_s > m + kRescaleThreshold)) return false;
                 float a0, a1, b0, b1;
                 f2_unpack(s2a, a0, a1);
                 f2_unpack(s2b, b0, b1);
-                l += (a0 + a1) + (b0 + b1);
+                const float tsum = (a0 + a1) + (b0 + b1);
+                if (__any_sync(0xFFFFFFFFu, tsum > kSumLimit)) return false;
+                l += tsum;
                 BSS_TMEM_ST32(t_s + 0, (pk + 0));
                 BSS_TMEM_ST32(t_s + 32, (pk + 32));
                 return true;
@@ -882,7 +886,8 @@ bss_status launch_d(const AttnLaunch& a, cudaStream_t stream) {
     const int64_t items = static_cast<int64_t>(a.H) * a.nq * (a.route ? 3 * a.splits : 1);
     if (items <= 0) return BSS_OK;
     if (items > 0x7FFFFFFF) return set_error(BSS_ERR_UNSUPPORTED, "too many work items");
-    kernel<<<static_cast<unsigned>(items), 128 * (1 + halves), smem, stream>>>(args);
+    const int threads = halves == 2 ? threads_for<2>() : threads_for<1>();
+    kernel<<<static_cast<unsigned>(items), threads, smem, stream>>>(args);
     return cuda_check(cudaGetLastError(), "attention launch");
 }
 
