@@ -31,6 +31,9 @@
 //                row's sum of P over the tile exceeds 2^16; only then are the
 //                max, O and l moved), writes bf16 P to TMEM; finally
 //                normalises O, stores it with a TMA store and writes the LSE.
+// With two halves, warpgroup 0 (warps 0..3) runs at 72 registers a thread and
+// the softmax warpgroups at 208 (setmaxnreg), so that the softmax keeps a
+// tile's P in registers without spilling.
 // tcgen05.mma operations issued by one thread execute in issue order, so an S
 // that overwrites P_h is issued after the PV that reads it.  Every mbarrier
 // wait is bounded; on a timeout the status word is set and all roles unwind to
@@ -69,6 +72,21 @@ constexpr uint32_t kColO = 256;  // O_h at kColO + 128 h
 // than 2^8 above it, always moves it there.
 constexpr float kRescaleThreshold = 8.0f;  // log2 units (general path)
 constexpr float kSumLimit = 65536.0f;      // fast path
+
+// Register split of the two-half CTA (384 threads launched at 168 registers a
+// thread = 64,512): warpgroup 0 (producer, MMA and the two spare warps) gives
+// registers back, the two softmax warpgroups take them, so that the softmax
+// keeps a whole tile of P in registers without spilling.  setmaxnreg.inc waits
+// until enough registers are free, so the split must fit in the launch's
+// allocation: 128 * 72 + 256 * 208 = 62,464 <= 64,512; per SM sub-partition
+// (one warp of each warpgroup) 72 + 2 * 208 = 488 <= 512 registers a lane.
+constexpr uint32_t kRegsControl = 72;
+constexpr uint32_t kRegsSoftmax = 208;
+constexpr uint32_t kRegsAtLaunch = 168;  // 65,536 / 384 rounded down to a multiple of 8
+static_assert(kRegsAtLaunch * 384 <= 65536, "launch allocation");
+static_assert(128 * kRegsControl + 256 * kRegsSoftmax <= 384 * kRegsAtLaunch,
+              "register split exceeds the launch allocation");
+static_assert(kRegsControl + 2 * kRegsSoftmax <= 512, "register split exceeds an SM sub-partition");
 
 struct AttnArgs {
     CUtensorMap tm_q, tm_k, tm_v, tm_o, tm_ks, tm_vs;
@@ -307,244 +325,249 @@ __global__ void __launch_bounds__(threads_for<HALVES>(), 1) attn_fwd_kernel(cons
     // temporal head whose (H,W,F) permutation is applied by the loads and stores
     const bool gather = !ROUTE && args.fused != 0 && code == MASK_TEMPORAL_VIRT;
 
-    if (warp == 0 && gather) {
-        // =========================== TMA producer, fused permutation: each lane
-        // gathers 4 permuted rows of every 128-row tile (tile::gather4 per 64-column
-        // chunk); frame-0 keys of the sink segment are contiguous, one box load.
-        if (lane == 0) {
-            tma_prefetch_desc(&args.tm_qg);
-            tma_prefetch_desc(&args.tm_kg);
-            tma_prefetch_desc(&args.tm_vg);
-            mbar_arrive_expect_tx(bar_q, HALVES * L::kTile);
-        }
-        __syncwarp();
-#pragma unroll
-        for (int hh = 0; hh < HALVES; ++hh) {
-            int r4[4];
-            fused_rows4(args, h, qt * kBQt + hh * kHalf + 4 * lane, r4);
-#pragma unroll
-            for (int c = 0; c < kChunks; ++c)
-                tma_gather4_2d(sQ + hh * L::kTile + c * kChunkBytesSw128 + lane * 512, &args.tm_qg, c * 64, r4[0],
-                               r4[1], r4[2], r4[3], bar_q);
-        }
-        bool ok = true;
-        int jk = 0, jv = 0;
-        for (; jv < n; ++jv) {
-            const int st = jv % kStages;
-            const uint32_t e = entry_at<ROUTE>(args, ents, jv, code, j0);
-            const int col0 = static_cast<int>(e & BSS_TILE_INDEX_MASK) * kBKV;
-            const bool sink = col0 < args.S_pad;
-            int r4[4] = {0, 0, 0, 0};
-            if (!sink) fused_rows4(args, h, col0 - args.S_pad + 4 * lane, r4);
-            if (jv >= kStages)
-                ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_k_empty + st, ((jv / kStages) - 1) & 1, status));
-            if (!ok) break;
-            if (lane == 0) mbar_arrive_expect_tx(bar_k_full + st, L::kTile);
-            __syncwarp();
-            if (sink) {
-                if (lane == 0) {
-#pragma unroll
-                    for (int c = 0; c < kChunks; ++c)
-                        tma_load_3d(sK + st * L::kTile + c * kChunkBytesSw128, &args.tm_ks, c * 64, col0, h,
-                                    bar_k_full + st);
-                }
-            } else {
-#pragma unroll
-                for (int c = 0; c < kChunks; ++c)
-                    tma_gather4_2d(sK + st * L::kTile + c * kChunkBytesSw128 + lane * 512, &args.tm_kg, c * 64, r4[0],
-                                   r4[1], r4[2], r4[3], bar_k_full + st);
+    if (warp < 4) {
+        // warpgroup 0: TMA producer, MMA issuer, two spare warps
+        if constexpr (HALVES == 2) setmaxnreg_dec<kRegsControl>();
+        if (warp == 0 && gather) {
+            // =========================== TMA producer, fused permutation: each lane
+            // gathers 4 permuted rows of every 128-row tile (tile::gather4 per 64-column
+            // chunk); frame-0 keys of the sink segment are contiguous, one box load.
+            if (lane == 0) {
+                tma_prefetch_desc(&args.tm_qg);
+                tma_prefetch_desc(&args.tm_kg);
+                tma_prefetch_desc(&args.tm_vg);
+                mbar_arrive_expect_tx(bar_q, HALVES * L::kTile);
             }
-            jk = jv + 1;
-            if (jv >= kStages)
-                ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_v_empty + st, ((jv / kStages) - 1) & 1, status));
-            if (!ok) break;
-            if (lane == 0) mbar_arrive_expect_tx(bar_v_full + st, L::kTile);
             __syncwarp();
-            if (sink) {
-                if (lane == 0) {
 #pragma unroll
-                    for (int c = 0; c < kChunks; ++c)
-                        tma_load_3d(sV + st * L::kTile + c * kChunkBytesSw128, &args.tm_vs, c * 64, col0, h,
-                                    bar_v_full + st);
-                }
-            } else {
+            for (int hh = 0; hh < HALVES; ++hh) {
+                int r4[4];
+                fused_rows4(args, h, qt * kBQt + hh * kHalf + 4 * lane, r4);
 #pragma unroll
                 for (int c = 0; c < kChunks; ++c)
-                    tma_gather4_2d(sV + st * L::kTile + c * kChunkBytesSw128 + lane * 512, &args.tm_vg, c * 64, r4[0],
-                                   r4[1], r4[2], r4[3], bar_v_full + st);
+                    tma_gather4_2d(sQ + hh * L::kTile + c * kChunkBytesSw128 + lane * 512, &args.tm_qg, c * 64, r4[0],
+                                   r4[1], r4[2], r4[3], bar_q);
             }
-        }
-        if (lane == 0) {
-            mbar_wait(bar_q, 0, status);
-            for (int jj = (jk - kStages > 0 ? jk - kStages : 0); jj < jk; ++jj)
-                mbar_wait(bar_k_full + jj % kStages, (jj / kStages) & 1, status);
-            for (int jj = (jv - kStages > 0 ? jv - kStages : 0); jj < jv; ++jj)
-                mbar_wait(bar_v_full + jj % kStages, (jj / kStages) & 1, status);
-        }
-    } else if (warp == 0) {
-        // =========================== TMA producer
-        if (lane == 0) {
-            const CUtensorMap* mq = tbuf ? &args.tm_qt : &args.tm_q;
-            const CUtensorMap* mk0 = tbuf ? &args.tm_kt : &args.tm_k;
-            const CUtensorMap* mv0 = tbuf ? &args.tm_vt : &args.tm_v;
-            tma_prefetch_desc(mq);
-            tma_prefetch_desc(mk0);
-            tma_prefetch_desc(mv0);
-            mbar_arrive_expect_tx(bar_q, HALVES * L::kTile);
-#pragma unroll
-            for (int hh = 0; hh < HALVES; ++hh)
-#pragma unroll
-                for (int c = 0; c < kChunks; ++c)
-                    tma_load_3d(sQ + hh * L::kTile + c * kChunkBytesSw128, mq, c * 64, qt * kBQt + hh * kHalf,
-                                h, bar_q);
             bool ok = true;
-            int jk = 0, jv = 0;  // K tiles and V tiles issued
+            int jk = 0, jv = 0;
             for (; jv < n; ++jv) {
                 const int st = jv % kStages;
                 const uint32_t e = entry_at<ROUTE>(args, ents, jv, code, j0);
                 const int col0 = static_cast<int>(e & BSS_TILE_INDEX_MASK) * kBKV;
-                const CUtensorMap* mk = mk0;
-                const CUtensorMap* mv = mv0;
-                int row = col0;
-                if (code == MASK_TEMPORAL_VIRT) {
-                    if (col0 < args.S_pad) {
-                        mk = &args.tm_ks;  // frame-0 keys: every F-th permuted row
-                        mv = &args.tm_vs;
-                    } else {
-                        row = col0 - args.S_pad;
+                const bool sink = col0 < args.S_pad;
+                int r4[4] = {0, 0, 0, 0};
+                if (!sink) fused_rows4(args, h, col0 - args.S_pad + 4 * lane, r4);
+                if (jv >= kStages)
+                    ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_k_empty + st, ((jv / kStages) - 1) & 1, status));
+                if (!ok) break;
+                if (lane == 0) mbar_arrive_expect_tx(bar_k_full + st, L::kTile);
+                __syncwarp();
+                if (sink) {
+                    if (lane == 0) {
+#pragma unroll
+                        for (int c = 0; c < kChunks; ++c)
+                            tma_load_3d(sK + st * L::kTile + c * kChunkBytesSw128, &args.tm_ks, c * 64, col0, h,
+                                        bar_k_full + st);
                     }
-                }
-                if (jv >= kStages) ok = mbar_wait(bar_k_empty + st, ((jv / kStages) - 1) & 1, status);
-                if (!ok) break;
-                mbar_arrive_expect_tx(bar_k_full + st, L::kTile);
+                } else {
 #pragma unroll
-                for (int c = 0; c < kChunks; ++c)
-                    tma_load_3d(sK + st * L::kTile + c * kChunkBytesSw128, mk, c * 64, row, h, bar_k_full + st);
+                    for (int c = 0; c < kChunks; ++c)
+                        tma_gather4_2d(sK + st * L::kTile + c * kChunkBytesSw128 + lane * 512, &args.tm_kg, c * 64, r4[0],
+                                       r4[1], r4[2], r4[3], bar_k_full + st);
+                }
                 jk = jv + 1;
-                if (jv >= kStages) ok = mbar_wait(bar_v_empty + st, ((jv / kStages) - 1) & 1, status);
+                if (jv >= kStages)
+                    ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_v_empty + st, ((jv / kStages) - 1) & 1, status));
                 if (!ok) break;
-                mbar_arrive_expect_tx(bar_v_full + st, L::kTile);
+                if (lane == 0) mbar_arrive_expect_tx(bar_v_full + st, L::kTile);
+                __syncwarp();
+                if (sink) {
+                    if (lane == 0) {
 #pragma unroll
-                for (int c = 0; c < kChunks; ++c)
-                    tma_load_3d(sV + st * L::kTile + c * kChunkBytesSw128, mv, c * 64, row, h, bar_v_full + st);
+                        for (int c = 0; c < kChunks; ++c)
+                            tma_load_3d(sV + st * L::kTile + c * kChunkBytesSw128, &args.tm_vs, c * 64, col0, h,
+                                        bar_v_full + st);
+                    }
+                } else {
+#pragma unroll
+                    for (int c = 0; c < kChunks; ++c)
+                        tma_gather4_2d(sV + st * L::kTile + c * kChunkBytesSw128 + lane * 512, &args.tm_vg, c * 64, r4[0],
+                                       r4[1], r4[2], r4[3], bar_v_full + st);
+                }
             }
-            // drain: no copy may still be landing in shared memory at exit
-            mbar_wait(bar_q, 0, status);
-            for (int jj = (jk - kStages > 0 ? jk - kStages : 0); jj < jk; ++jj)
-                mbar_wait(bar_k_full + jj % kStages, (jj / kStages) & 1, status);
-            for (int jj = (jv - kStages > 0 ? jv - kStages : 0); jj < jv; ++jj)
-                mbar_wait(bar_v_full + jj % kStages, (jj / kStages) & 1, status);
-        }
-    } else if (warp == 1) {
-        // =========================== MMA issuer: the whole warp runs the loop (so
-        // descriptors stay warp-uniform), one elected lane issues and commits.
-        if (n > 0) {
-            constexpr uint32_t idesc_qk = idesc_bf16_f32(kHalf, kBKV, 0);
-            constexpr uint32_t idesc_pv = idesc_bf16_f32(kHalf, D, 1);
-            const bool leader = elect_one();
-            // base descriptors; K step kk adds (kk / 4) * 16 KiB + (kk % 4) * 32 bytes
-            // (K-major) or kk * 2 KiB (MN-major) to the start-address field (>> 4)
-            const uint64_t dq0 = desc_kmajor_sw128(smem_u32(sQ), 0);
-            const uint64_t dq1 = desc_kmajor_sw128(smem_u32(sQ + L::kTile), 0);
-            const uint64_t dk0 = desc_kmajor_sw128(smem_u32(sK), 0);
-            const uint64_t dv0 = desc_mnmajor_sw128(smem_u32(sV), 0);
-            constexpr uint64_t kStageStep = L::kTile >> 4;
-            auto kstep = [](int kk) -> uint64_t {
-                return static_cast<uint64_t>((kk >> 2) * (kChunkBytesSw128 >> 4) + (kk & 3) * 2);
-            };
-            auto issue_s = [&](uint32_t d_col, uint64_t dq, uint64_t dk) {
-                if (leader) {
+            if (lane == 0) {
+                mbar_wait(bar_q, 0, status);
+                for (int jj = (jk - kStages > 0 ? jk - kStages : 0); jj < jk; ++jj)
+                    mbar_wait(bar_k_full + jj % kStages, (jj / kStages) & 1, status);
+                for (int jj = (jv - kStages > 0 ? jv - kStages : 0); jj < jv; ++jj)
+                    mbar_wait(bar_v_full + jj % kStages, (jj / kStages) & 1, status);
+            }
+        } else if (warp == 0) {
+            // =========================== TMA producer
+            if (lane == 0) {
+                const CUtensorMap* mq = tbuf ? &args.tm_qt : &args.tm_q;
+                const CUtensorMap* mk0 = tbuf ? &args.tm_kt : &args.tm_k;
+                const CUtensorMap* mv0 = tbuf ? &args.tm_vt : &args.tm_v;
+                tma_prefetch_desc(mq);
+                tma_prefetch_desc(mk0);
+                tma_prefetch_desc(mv0);
+                mbar_arrive_expect_tx(bar_q, HALVES * L::kTile);
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk)
-                        umma_ss(tmem + d_col, dq + kstep(kk), dk + kstep(kk), idesc_qk, kk > 0 ? 1u : 0u);
-                }
-            };
-            auto issue_pv = [&](uint32_t d_col, uint32_t p_col, uint64_t dv, bool acc) {
-                if (leader) {
+                for (int hh = 0; hh < HALVES; ++hh)
 #pragma unroll
-                    for (int kk = 0; kk < kBKV / 16; ++kk)
-                        umma_ts(tmem + d_col, tmem + p_col + kk * 8, dv + static_cast<uint64_t>(kk * 128), idesc_pv,
-                                (acc || kk > 0) ? 1u : 0u);
+                    for (int c = 0; c < kChunks; ++c)
+                        tma_load_3d(sQ + hh * L::kTile + c * kChunkBytesSw128, mq, c * 64, qt * kBQt + hh * kHalf,
+                                    h, bar_q);
+                bool ok = true;
+                int jk = 0, jv = 0;  // K tiles and V tiles issued
+                for (; jv < n; ++jv) {
+                    const int st = jv % kStages;
+                    const uint32_t e = entry_at<ROUTE>(args, ents, jv, code, j0);
+                    const int col0 = static_cast<int>(e & BSS_TILE_INDEX_MASK) * kBKV;
+                    const CUtensorMap* mk = mk0;
+                    const CUtensorMap* mv = mv0;
+                    int row = col0;
+                    if (code == MASK_TEMPORAL_VIRT) {
+                        if (col0 < args.S_pad) {
+                            mk = &args.tm_ks;  // frame-0 keys: every F-th permuted row
+                            mv = &args.tm_vs;
+                        } else {
+                            row = col0 - args.S_pad;
+                        }
+                    }
+                    if (jv >= kStages) ok = mbar_wait(bar_k_empty + st, ((jv / kStages) - 1) & 1, status);
+                    if (!ok) break;
+                    mbar_arrive_expect_tx(bar_k_full + st, L::kTile);
+#pragma unroll
+                    for (int c = 0; c < kChunks; ++c)
+                        tma_load_3d(sK + st * L::kTile + c * kChunkBytesSw128, mk, c * 64, row, h, bar_k_full + st);
+                    jk = jv + 1;
+                    if (jv >= kStages) ok = mbar_wait(bar_v_empty + st, ((jv / kStages) - 1) & 1, status);
+                    if (!ok) break;
+                    mbar_arrive_expect_tx(bar_v_full + st, L::kTile);
+#pragma unroll
+                    for (int c = 0; c < kChunks; ++c)
+                        tma_load_3d(sV + st * L::kTile + c * kChunkBytesSw128, mv, c * 64, row, h, bar_v_full + st);
                 }
-            };
-            auto commit = [&](uint64_t* bar) {
-                if (leader) tc_commit(bar);
-            };
-            bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_q, 0, status));
-            if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_k_full, 0, status));
-            if constexpr (HALVES == 1) {
-                // one half: S in two TMEM buffers (columns 0 / 128 by tile parity), so
-                // S(j+1) is issued before PV(j) and overlaps the softmax of tile j;
-                // the P-ready barrier is double-buffered the same way
+                // drain: no copy may still be landing in shared memory at exit
+                mbar_wait(bar_q, 0, status);
+                for (int jj = (jk - kStages > 0 ? jk - kStages : 0); jj < jk; ++jj)
+                    mbar_wait(bar_k_full + jj % kStages, (jj / kStages) & 1, status);
+                for (int jj = (jv - kStages > 0 ? jv - kStages : 0); jj < jv; ++jj)
+                    mbar_wait(bar_v_full + jj % kStages, (jj / kStages) & 1, status);
+            }
+        } else if (warp == 1) {
+            // =========================== MMA issuer: the whole warp runs the loop (so
+            // descriptors stay warp-uniform), one elected lane issues and commits.
+            if (n > 0) {
+                constexpr uint32_t idesc_qk = idesc_bf16_f32(kHalf, kBKV, 0);
+                constexpr uint32_t idesc_pv = idesc_bf16_f32(kHalf, D, 1);
+                const bool leader = elect_one();
+                // base descriptors; K step kk adds (kk / 4) * 16 KiB + (kk % 4) * 32 bytes
+                // (K-major) or kk * 2 KiB (MN-major) to the start-address field (>> 4)
+                const uint64_t dq0 = desc_kmajor_sw128(smem_u32(sQ), 0);
+                const uint64_t dq1 = desc_kmajor_sw128(smem_u32(sQ + L::kTile), 0);
+                const uint64_t dk0 = desc_kmajor_sw128(smem_u32(sK), 0);
+                const uint64_t dv0 = desc_mnmajor_sw128(smem_u32(sV), 0);
+                constexpr uint64_t kStageStep = L::kTile >> 4;
+                auto kstep = [](int kk) -> uint64_t {
+                    return static_cast<uint64_t>((kk >> 2) * (kChunkBytesSw128 >> 4) + (kk & 3) * 2);
+                };
+                auto issue_s = [&](uint32_t d_col, uint64_t dq, uint64_t dk) {
+                    if (leader) {
+#pragma unroll
+                        for (int kk = 0; kk < D / 16; ++kk)
+                            umma_ss(tmem + d_col, dq + kstep(kk), dk + kstep(kk), idesc_qk, kk > 0 ? 1u : 0u);
+                    }
+                };
+                auto issue_pv = [&](uint32_t d_col, uint32_t p_col, uint64_t dv, bool acc) {
+                    if (leader) {
+#pragma unroll
+                        for (int kk = 0; kk < kBKV / 16; ++kk)
+                            umma_ts(tmem + d_col, tmem + p_col + kk * 8, dv + static_cast<uint64_t>(kk * 128), idesc_pv,
+                                    (acc || kk > 0) ? 1u : 0u);
+                    }
+                };
+                auto commit = [&](uint64_t* bar) {
+                    if (leader) tc_commit(bar);
+                };
+                bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_q, 0, status));
+                if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_k_full, 0, status));
+                if constexpr (HALVES == 1) {
+                    // one half: S in two TMEM buffers (columns 0 / 128 by tile parity), so
+                    // S(j+1) is issued before PV(j) and overlaps the softmax of tile j;
+                    // the P-ready barrier is double-buffered the same way
+                    if (ok) {
+                        tc_fence_after();
+                        issue_s(kColS, dq0, dk0);
+                        commit(bar_s_full + 0);
+                        commit(bar_k_empty + 0);
+                    }
+                    for (int j = 0; ok && j < n; ++j) {
+                        const int st = j % kStages;
+                        if (j + 1 < n) {
+                            const int st1 = (j + 1) % kStages;
+                            ok = __all_sync(0xFFFFFFFFu,
+                                            mbar_wait(bar_k_full + st1, ((j + 1) / kStages) & 1, status));
+                            if (!ok) break;
+                            tc_fence_after();
+                            issue_s(kColS + 128 * ((j + 1) & 1), dq0, dk0 + st1 * kStageStep);
+                            commit(bar_s_full + ((j + 1) & 1));
+                            commit(bar_k_empty + st1);
+                        }
+                        ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_v_full + st, (j / kStages) & 1, status));
+                        if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_p_full + (j & 1), (j >> 1) & 1, status));
+                        if (!ok) break;
+                        tc_fence_after();
+                        issue_pv(kColO, kColS + 128 * (j & 1), dv0 + st * kStageStep, j > 0);
+                        commit(bar_o_done + 0);
+                        commit(bar_v_empty + st);
+                    }
+                } else {
                 if (ok) {
                     tc_fence_after();
                     issue_s(kColS, dq0, dk0);
                     commit(bar_s_full + 0);
-                    commit(bar_k_empty + 0);
                 }
                 for (int j = 0; ok && j < n; ++j) {
                     const int st = j % kStages;
+                    const uint64_t dk = dk0 + st * kStageStep;
+                    const uint64_t dv = dv0 + st * kStageStep;
+                    // S_1(j): K_j is resident (waited before S_0(j))
+                    issue_s(kColS + 128, dq1, dk);
+                    commit(bar_s_full + 1);
+                    commit(bar_k_empty + st);  // K_j is free once S_0(j) and S_1(j) complete
+                    // PV_0(j)
+                    ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_v_full + st, (j / kStages) & 1, status));
+                    if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_p_full + 0, j & 1, status));
+                    if (!ok) break;
+                    tc_fence_after();
+                    issue_pv(kColO, kColS, dv, j > 0);
+                    commit(bar_o_done + 0);
+                    // S_0(j+1)
                     if (j + 1 < n) {
                         const int st1 = (j + 1) % kStages;
-                        ok = __all_sync(0xFFFFFFFFu,
-                                        mbar_wait(bar_k_full + st1, ((j + 1) / kStages) & 1, status));
+                        ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_k_full + st1, ((j + 1) / kStages) & 1, status));
                         if (!ok) break;
                         tc_fence_after();
-                        issue_s(kColS + 128 * ((j + 1) & 1), dq0, dk0 + st1 * kStageStep);
-                        commit(bar_s_full + ((j + 1) & 1));
-                        commit(bar_k_empty + st1);
+                        issue_s(kColS, dq0, dk0 + st1 * kStageStep);
+                        commit(bar_s_full + 0);
                     }
-                    ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_v_full + st, (j / kStages) & 1, status));
-                    if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_p_full + (j & 1), (j >> 1) & 1, status));
+                    // PV_1(j)
+                    ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_p_full + 1, j & 1, status));
                     if (!ok) break;
                     tc_fence_after();
-                    issue_pv(kColO, kColS + 128 * (j & 1), dv0 + st * kStageStep, j > 0);
-                    commit(bar_o_done + 0);
+                    issue_pv(kColO + 128, kColS + 128, dv, j > 0);
+                    commit(bar_o_done + 1);
                     commit(bar_v_empty + st);
                 }
-            } else {
-            if (ok) {
-                tc_fence_after();
-                issue_s(kColS, dq0, dk0);
-                commit(bar_s_full + 0);
-            }
-            for (int j = 0; ok && j < n; ++j) {
-                const int st = j % kStages;
-                const uint64_t dk = dk0 + st * kStageStep;
-                const uint64_t dv = dv0 + st * kStageStep;
-                // S_1(j): K_j is resident (waited before S_0(j))
-                issue_s(kColS + 128, dq1, dk);
-                commit(bar_s_full + 1);
-                commit(bar_k_empty + st);  // K_j is free once S_0(j) and S_1(j) complete
-                // PV_0(j)
-                ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_v_full + st, (j / kStages) & 1, status));
-                if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_p_full + 0, j & 1, status));
-                if (!ok) break;
-                tc_fence_after();
-                issue_pv(kColO, kColS, dv, j > 0);
-                commit(bar_o_done + 0);
-                // S_0(j+1)
-                if (j + 1 < n) {
-                    const int st1 = (j + 1) % kStages;
-                    ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_k_full + st1, ((j + 1) / kStages) & 1, status));
-                    if (!ok) break;
-                    tc_fence_after();
-                    issue_s(kColS, dq0, dk0 + st1 * kStageStep);
-                    commit(bar_s_full + 0);
                 }
-                // PV_1(j)
-                ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_p_full + 1, j & 1, status));
-                if (!ok) break;
-                tc_fence_after();
-                issue_pv(kColO + 128, kColS + 128, dv, j > 0);
-                commit(bar_o_done + 1);
-                commit(bar_v_empty + st);
+                commit(bar_mma_done);
+                mbar_wait(bar_mma_done, 0, status);
             }
-            }
-            commit(bar_mma_done);
-            mbar_wait(bar_mma_done, 0, status);
         }
-    } else if (warp >= 4) {
+    } else {
+        if constexpr (HALVES == 2) setmaxnreg_inc<kRegsSoftmax>();
         // =========================== softmax + epilogue (one thread per row)
         const int hf = (warp - 4) >> 2;  // half
         const int r = threadIdx.x - 128 - hf * 128;
