@@ -614,7 +614,7 @@ __global__ void __launch_bounds__(threads_for<HALVES>(), 1) attn_fwd_kernel(cons
             // result is kept unless some row's sum of P exceeds kSumLimit (then the
             // tile is redone on the general path).
             bool done = false;
-            // one pass over the four 32-column chunks; MASKED applies the tile's
+            // one pass over the row's 128 scores; MASKED applies the tile's
             // retained-column bitmask (boundary / padding tiles)
             auto single_pass = [&](auto masked_tag, const uint32_t (&bits)[4]) -> bool {
                 constexpr bool MASKED = decltype(masked_tag)::value;
@@ -622,11 +622,16 @@ __global__ void __launch_bounds__(threads_for<HALVES>(), 1) attn_fwd_kernel(cons
                 uint64_t s2a = 0ull, s2b = 0ull;  // packed partial sums (two chains)
                 const uint64_t c2 = f2_pack(c, c);
                 const uint64_t nm2 = f2_pack(-m, -m);
+                // the row's 128 scores in one wait, so that the scheduler has 64
+                // independent pairs to interleave with the exponentials (measured:
+                // 1.9% faster than a wait per 32-column chunk)
+                uint32_t sb[4][32];
+#pragma unroll
+                for (int cc = 0; cc < 4; ++cc) BSS_TMEM_LD32(t_s + 32 * cc, sb[cc]);
+                tmem_wait_ld();
 #pragma unroll
                 for (int cc = 0; cc < 4; ++cc) {
-                    uint32_t sr[32];
-                    BSS_TMEM_LD32(t_s + 32 * cc, sr);
-                    tmem_wait_ld();
+                    const uint32_t (&sr)[32] = sb[cc];
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
                         float x0 = __uint_as_float(sr[2 * i]), x1 = __uint_as_float(sr[2 * i + 1]);
