@@ -656,8 +656,10 @@ __global__ void __launch_bounds__(threads_for<HALVES>(), 1) attn_fwd_kernel(cons
                 const float tsum = (a0 + a1) + (b0 + b1);
                 if (__any_sync(0xFFFFFFFFu, tsum > kSumLimit)) return false;
                 l += tsum;
-                BSS_TMEM_ST32(t_s + 0, (pk + 0));
-                BSS_TMEM_ST32(t_s + 32, (pk + 32));
+                // P in 16-column stores (measured: 1.6% faster than 32-column ones,
+                // 1% slower with 8-column ones)
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4) BSS_TMEM_ST16(t_s + 16 * q4, (pk + 16 * q4));
                 return true;
             };
             if (__all_sync(0xFFFFFFFFu, m != -INFINITY)) {
