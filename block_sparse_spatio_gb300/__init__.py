@@ -287,14 +287,18 @@ def sparse_attention(Q, K, V, O, tile_map: TileMap, head_is_temporal=None, lse=N
 def sparse_attention_split(Q, K, V, O, Qt, Kt, Vt, Ot, tile_map: TileMap, head_is_temporal, lse=None,
                            softmax_scale: float = 0.0, stream=None):
     """Block-sparse attention with spatial heads in Q, K, V -> O and temporal
-    heads (flag 1) in the permuted buffers Qt, Kt, Vt -> Ot."""
+    heads (flag 1) in the permuted buffers Qt, Kt, Vt -> Ot.  Ot=None writes the
+    temporal heads' output rows straight to O in (F,H,W) order (no inverse
+    permutation needed)."""
     import torch
-    for t, n in ((Q, "Q"), (K, "K"), (V, "V"), (O, "O"), (Qt, "Qt"), (Kt, "Kt"), (Vt, "Vt"), (Ot, "Ot")):
+    named = [(Q, "Q"), (K, "K"), (V, "V"), (O, "O"), (Qt, "Qt"), (Kt, "Kt"), (Vt, "Vt")]
+    if Ot is not None:
+        named.append((Ot, "Ot"))
+    for t, n in named:
         _dev_tensor(t, n, torch.bfloat16)
     _dev_tensor(head_is_temporal, "head_is_temporal", torch.uint8)
     _dev_tensor(lse, "lse", torch.float32)
-    _check_shapes(tile_map, lse, (Q, "Q"), (K, "K"), (V, "V"), (O, "O"), (Qt, "Qt"), (Kt, "Kt"), (Vt, "Vt"),
-                  (Ot, "Ot"))
+    _check_shapes(tile_map, lse, *named)
     _check(load().bss_sparse_attention_split(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(Qt), _ptr(Kt), _ptr(Vt),
                                              _ptr(Ot), _ptr(lse), tile_map.handle, _ptr(head_is_temporal),
                                              Q.shape[0], float(softmax_scale), _stream(stream)))
@@ -388,19 +392,21 @@ def route_heads(Q, K, V, params: MaskParams, rows, head_is_temporal, errors, str
     return head_is_temporal, errors
 
 
-def attention_step(Q, K, V, O, tile_map: TileMap, head_is_temporal, Qp, Kp, Vp, Op, lse=None, stream=None):
+def attention_step(Q, K, V, O, tile_map: TileMap, head_is_temporal, Qp, Kp, Vp, Op=None, lse=None, stream=None):
     """The per-layer path of the blog's Figure 8 on one GPU: permute the temporal
     heads' Q, K, V to (H,W,F), run block-sparse attention, restore O's order.
-    Q, K, V, O are in (F,H,W) order; Qp, Kp, Vp, Op are caller-owned workspaces."""
+    Q, K, V, O are in (F,H,W) order; Qp, Kp, Vp are caller-owned workspaces (Op
+    is not needed: the attention writes the temporal heads' O rows straight to
+    their (F,H,W) positions; it is accepted for callers that pass four
+    workspaces).  lse, if given, is in each head's own layout."""
     p = tile_map.params
     if p.temporal_permuted:
         # only the temporal heads are permuted; spatial heads are read from Q, K, V
-        # and written to O in place
+        # and written to O in place, temporal heads' rows are stored back in order
         permute(Q, Qp, head_is_temporal, p, False, stream, only_flagged=True)
         permute(K, Kp, head_is_temporal, p, False, stream, only_flagged=True)
         permute(V, Vp, head_is_temporal, p, False, stream, only_flagged=True)
-        sparse_attention_split(Q, K, V, O, Qp, Kp, Vp, Op, tile_map, head_is_temporal, lse, stream=stream)
-        permute(Op, O, head_is_temporal, p, True, stream, only_flagged=True)
+        sparse_attention_split(Q, K, V, O, Qp, Kp, Vp, None, tile_map, head_is_temporal, lse, stream=stream)
     else:
         sparse_attention(Q, K, V, O, tile_map, head_is_temporal, lse, stream=stream)
     return O
@@ -409,7 +415,7 @@ def attention_step(Q, K, V, O, tile_map: TileMap, head_is_temporal, Qp, Kp, Vp, 
 def attention_step_host(hQ, hK, hV, hO, tile_map: TileMap, head_is_temporal, workspace, heads_per_chunk: int = 1,
                         stream=None):
     """The per-layer path from pinned HOST buffers: H2D copies of Q, K, V, the
-    permute -> block-sparse attention -> unpermute path, and the D2H copy of O,
+    permute -> block-sparse attention path of ``attention_step``, and the D2H copy of O,
     pipelined over groups of heads (heads are independent) on three streams.
 
     hQ, hK, hV, hO: pinned CPU bf16 [H][N][d]; head_is_temporal: device uint8[H],
@@ -428,7 +434,7 @@ def attention_step_host(hQ, hK, hV, hO, tile_map: TileMap, head_is_temporal, wor
     workspace["next"] = (k + 1) % len(workspace["sets"])
     buf = workspace["sets"][k]
     Q, K, V, O = buf["Q"], buf["K"], buf["V"], buf["O"]
-    Qp, Kp, Vp, Op = buf["Qp"], buf["Kp"], buf["Vp"], buf["Op"]
+    Qp, Kp, Vp = buf["Qp"], buf["Kp"], buf["Vp"]
     free = workspace["free"][k]
     if free is not None:
         cs.wait_event(free)
@@ -447,7 +453,7 @@ def attention_step_host(hQ, hK, hV, hO, tile_map: TileMap, head_is_temporal, wor
         main.wait_event(ready)
         with torch.cuda.stream(main):
             attention_step(Q[h0:h1], K[h0:h1], V[h0:h1], O[h0:h1], tile_map, flags[h0:h1],
-                           Qp[h0:h1], Kp[h0:h1], Vp[h0:h1], Op[h0:h1], stream=main)
+                           Qp[h0:h1], Kp[h0:h1], Vp[h0:h1], stream=main)
         done = torch.cuda.Event()
         done.record(main)
         os_.wait_event(done)
@@ -464,7 +470,7 @@ def step_workspace(H: int, N: int, d: int, device=None, depth: int = 2):
     import torch
     device = device or torch.device("cuda")
     sets = [{k: torch.empty(H, N, d, dtype=torch.bfloat16, device=device)
-             for k in ("Q", "K", "V", "O", "Qp", "Kp", "Vp", "Op")} for _ in range(depth)]
+             for k in ("Q", "K", "V", "O", "Qp", "Kp", "Vp")} for _ in range(depth)]
     for st in sets:
         st["flags"] = torch.empty(H, dtype=torch.uint8, device=device)
     return {"sets": sets, "free": [None] * depth, "next": 0,

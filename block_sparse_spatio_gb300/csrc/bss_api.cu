@@ -365,11 +365,13 @@ bss_status bss_sparse_attention_split(const void* Q, const void* K, const void* 
                                       const uint8_t* head_is_temporal, int32_t H, float softmax_scale,
                                       cudaStream_t stream) {
     using namespace bss;
-    if (Qt == nullptr || Kt == nullptr || Vt == nullptr || Ot == nullptr)
+    if (Qt == nullptr || Kt == nullptr || Vt == nullptr)
         return set_error(BSS_ERR_INVALID_ARG, "NULL temporal-head tensor");
-    if (!aligned16(Qt) || !aligned16(Kt) || !aligned16(Vt) || !aligned16(Ot))
+    if (!aligned16(Qt) || !aligned16(Kt) || !aligned16(Vt) || (Ot != nullptr && !aligned16(Ot)))
         return set_error(BSS_ERR_INVALID_ARG, "tensors must be 16-byte aligned");
-    return sparse_attention_impl(Q, K, V, O, lse, map, head_is_temporal, H, softmax_scale, 0, stream, Qt, Kt, Vt, Ot);
+    // Ot == NULL: the temporal heads' O rows are written straight to O in (F,H,W) order
+    return sparse_attention_impl(Q, K, V, O, lse, map, head_is_temporal, H, softmax_scale, Ot == nullptr ? 2 : 0,
+                                 stream, Qt, Kt, Vt, Ot);
 }
 
 bss_status bss_sparse_attention_fused(const void* Q, const void* K, const void* V, void* O, float* lse,

@@ -103,7 +103,8 @@ struct AttnArgs {
     float* lse;
     int* status;
     int32_t code[2];
-    int32_t H, N, nq, F, S, S_pad, wf, ws, dense, nkv_dense, fused;
+    int32_t H, N, nq, F, S, S_pad, wf, ws, dense, nkv_dense;
+    int32_t fused;  // 0: none, 1: permutation in loads and stores, 2: in the O stores only
     int32_t route, Nq, splits;  // routing mode: query rows per head, kv splits
     float scale_log2;
 };
@@ -323,7 +324,10 @@ __global__ void __launch_bounds__(threads_for<HALVES>(), 1) attn_fwd_kernel(cons
     const uint32_t tmem = *tmem_slot;
 
     // temporal head whose (H,W,F) permutation is applied by the loads and stores
-    const bool gather = !ROUTE && args.fused != 0 && code == MASK_TEMPORAL_VIRT;
+    // (fused mode 1), or by the output stores only (mode 2: Q, K, V come permuted,
+    // O rows go straight to their (F,H,W) positions)
+    const bool gather = !ROUTE && args.fused == 1 && code == MASK_TEMPORAL_VIRT;
+    const bool scatter = gather || (!ROUTE && args.fused == 2 && code == MASK_TEMPORAL_VIRT);
 
     if (warp < 4) {
         // warpgroup 0: TMA producer, MMA issuer, two spare warps
@@ -586,7 +590,7 @@ __global__ void __launch_bounds__(threads_for<HALVES>(), 1) attn_fwd_kernel(cons
         const RowPred rp = row_pred(args, code, qo);
         // output row of this query: its own index, or its (F,H,W) position when the
         // kernel applies the permutation
-        const int orow = (gather && q < args.N) ? (q % args.F) * args.S + q / args.F : q;
+        const int orow = (scatter && q < args.N) ? (q % args.F) * args.S + q / args.F : q;
         const float c = args.scale_log2;
         float m = -INFINITY;
         float l = 0.0f;
@@ -787,8 +791,9 @@ __global__ void __launch_bounds__(threads_for<HALVES>(), 1) attn_fwd_kernel(cons
                                                  __uint_as_float(o[4 * u + 2]) * inv_l,
                                                  __uint_as_float(o[4 * u + 3]) * inv_l);
                     }
-                } else if (gather) {
-                    // fused permutation: the row goes straight to its (F,H,W) position
+                } else if (scatter) {
+                    // permutation applied by the store: the row goes straight to its
+                    // (F,H,W) position
                     if (q < args.N) {
                         uint4* dst = reinterpret_cast<uint4*>(args.o_rows + (static_cast<int64_t>(h) * args.N + orow) * D) +
                                      cc * 4;
@@ -813,13 +818,14 @@ __global__ void __launch_bounds__(threads_for<HALVES>(), 1) attn_fwd_kernel(cons
                 }
             } else if (args.lse != nullptr && q < args.N) {
                 const float lse = l > 0.0f ? (m + log2f(l)) * 0.69314718055994530942f : -INFINITY;
-                args.lse[static_cast<int64_t>(h) * args.N + orow] = lse;
+                // fused mode: LSE in (F,H,W) order like O; otherwise in layout order
+                args.lse[static_cast<int64_t>(h) * args.N + (gather ? orow : q)] = lse;
             }
             fence_proxy_async_smem();
         }
         named_barrier_sync(1 + hf, 128);
         const int row0 = qt * kBQt + hf * kHalf;
-        if (r == 0 && ok && row0 < args.N && !gather && !ROUTE) {
+        if (r == 0 && ok && row0 < args.N && !scatter && !ROUTE) {
 #pragma unroll
             for (int cc = 0; cc < kChunks; ++cc)
                 tma_store_3d(tbuf ? &args.tm_ot : &args.tm_o, stage + cc * kChunkBytesSw128, cc * 64, row0, h);
@@ -854,7 +860,7 @@ bss_status launch_d(const AttnLaunch& a, cudaStream_t stream) {
         return st;
     // frame-0 keys of a temporal head: row s of this view is key (f = 0, s), which
     // is permuted row s*F of a permuted tensor, or row s of an (F,H,W) tensor
-    const uint64_t sink_rs = a.fused ? rs : rs * a.F;
+    const uint64_t sink_rs = a.fused == 1 ? rs : rs * a.F;
     // heads with flag 1: split buffers if given
     const void* Qt = a.Qt ? a.Qt : a.Q;
     const void* Kt = a.Kt ? a.Kt : a.K;
@@ -866,7 +872,7 @@ bss_status launch_d(const AttnLaunch& a, cudaStream_t stream) {
     if ((st = encode_tmap_3d(&args.tm_ot, Ot, a.d, nq_rows, a.H, rs, rs * nq_rows, 64, kHalf)) != BSS_OK) return st;
     if ((st = encode_tmap_3d(&args.tm_ks, Kt, a.d, a.S, a.H, sink_rs, hs, 64, kBKV)) != BSS_OK) return st;
     if ((st = encode_tmap_3d(&args.tm_vs, Vt, a.d, a.S, a.H, sink_rs, hs, 64, kBKV)) != BSS_OK) return st;
-    if (a.fused) {
+    if (a.fused == 1) {
         const uint64_t rows = static_cast<uint64_t>(a.H) * static_cast<uint64_t>(a.N);
         if (rows > 0x7FFFFFFFull) return set_error(BSS_ERR_UNSUPPORTED, "H*N too large for the fused permutation");
         if ((st = encode_tmap_rows_2d(&args.tm_qg, a.Q, a.d, rows, rs, 64)) != BSS_OK) return st;

@@ -68,7 +68,9 @@ struct AttnLaunch {
     float softmax_scale;
     // 1: Q, K, V, O and lse are in (F,H,W) token order for every head; the
     // temporal kind's (H,W,F) permutation is applied by the kernel's loads and
-    // stores instead of separate permute passes
+    // stores instead of separate permute passes.  2: temporal heads' Q, K, V come
+    // permuted (Qt, Kt, Vt) and only their O rows are written straight to their
+    // (F,H,W) positions in O (lse stays in layout order).
     int32_t fused;
     // routing mode: 3 x H output heads (dense, spatial, temporal in (F,H,W)
     // order) over Nq sampled query rows per head whose tokens are qmap[r]; every

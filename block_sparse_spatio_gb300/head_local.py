@@ -67,17 +67,17 @@ def head_local_attention(Q, K, V, head_is_temporal, step, group=None):
 
 def make_attention_step(tile_map, heads_local: int, N: int, d: int, device=None):
     """A ``step`` for ``head_local_attention``: the library's permute -> sparse
-    attention -> unpermute path on the local heads, with its workspaces
+    attention path (``attention_step``) on the local heads, with its workspaces
     allocated once ([H/P][N][d] bf16 each)."""
     import torch
 
     from . import attention_step
     device = device or torch.device("cuda")
-    ws = [torch.empty(heads_local, N, d, dtype=torch.bfloat16, device=device) for _ in range(5)]
+    ws = [torch.empty(heads_local, N, d, dtype=torch.bfloat16, device=device) for _ in range(4)]
 
     def step(Qh, Kh, Vh, flags):
-        Oh = ws[4]
-        attention_step(Qh, Kh, Vh, Oh, tile_map, flags, ws[0], ws[1], ws[2], ws[3])
+        Oh = ws[3]
+        attention_step(Qh, Kh, Vh, Oh, tile_map, flags, ws[0], ws[1], ws[2])
         return Oh
 
     return step

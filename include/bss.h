@@ -180,8 +180,14 @@ bss_status bss_sparse_attention(const void* Q, const void* K, const void* V, voi
  * Kt, Vt and write Ot (all device [H][N][d] bf16, only each kind's heads are
  * touched).  With Qt, Kt, Vt the bss_permute_flagged images of Q, K, V and O
  * restored by the inverse bss_permute_flagged of Ot, the step permutes only
- * the temporal heads.  lse as in bss_sparse_attention (each head in its own
- * layout).  Errors as bss_sparse_attention. */
+ * the temporal heads.  Ot may be NULL: the temporal heads' output rows are
+ * then written straight to O at their (F,H,W) positions (row s*F + f of the
+ * permuted layout goes to row f*S + s), so no inverse permutation is needed
+ * and O holds every head in (F,H,W) order (bit for bit what the inverse
+ * bss_permute_flagged of Ot would give); this needs a map built with
+ * temporal_permuted = 1, else Ot = NULL writes O in the heads' own layout.
+ * lse as in bss_sparse_attention (each head in its own layout, also with
+ * Ot = NULL).  Errors as bss_sparse_attention. */
 bss_status bss_sparse_attention_split(const void* Q, const void* K, const void* V, void* O, const void* Qt,
                                       const void* Kt, const void* Vt, void* Ot, float* lse, bss_tile_map map,
                                       const uint8_t* head_is_temporal, int32_t H, float softmax_scale,

@@ -255,7 +255,18 @@ def test_split_step_equals_full_permutation_step(bss, wl_name):
         bss.permute(V, Vp, fl, p, False)
         bss.sparse_attention(Qp, Kp, Vp, Op, tm, fl, lse=l2)
         bss.permute(Op, O2, fl, p, True)
+        # the split call with an explicit Ot, then the inverse permute of Ot (the
+        # step stores the temporal heads' rows in (F,H,W) order itself, Ot = None)
+        O3, Ot = torch.empty_like(Q), torch.empty_like(Q)
+        l3 = torch.empty(H, wl.N, device=dev)
+        bss.permute(Q, Qp, fl, p, False, only_flagged=True)
+        bss.permute(K, Kp, fl, p, False, only_flagged=True)
+        bss.permute(V, Vp, fl, p, False, only_flagged=True)
+        bss.sparse_attention_split(Q, K, V, O3, Qp, Kp, Vp, Ot, tm, fl, lse=l3)
+        bss.permute(Ot, O3, fl, p, True, only_flagged=True)
         torch.cuda.synchronize()
     assert bss.get_device_status() == 0
     assert torch.equal(O1.view(torch.int16), O2.view(torch.int16))
     assert torch.equal(l1.view(torch.int32), l2.view(torch.int32))
+    assert torch.equal(O3.view(torch.int16), O1.view(torch.int16))
+    assert torch.equal(l3.view(torch.int32), l1.view(torch.int32))
