@@ -528,43 +528,43 @@ __global__ void __launch_bounds__(threads_for<HALVES>(), 1) attn_fwd_kernel(cons
                         commit(bar_v_empty + st);
                     }
                 } else {
-                if (ok) {
-                    tc_fence_after();
-                    issue_s(kColS, dq0, dk0);
-                    commit(bar_s_full + 0);
-                }
-                for (int j = 0; ok && j < n; ++j) {
-                    const int st = j % kStages;
-                    const uint64_t dk = dk0 + st * kStageStep;
-                    const uint64_t dv = dv0 + st * kStageStep;
-                    // S_1(j): K_j is resident (waited before S_0(j))
-                    issue_s(kColS + 128, dq1, dk);
-                    commit(bar_s_full + 1);
-                    commit(bar_k_empty + st);  // K_j is free once S_0(j) and S_1(j) complete
-                    // PV_0(j)
-                    ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_v_full + st, (j / kStages) & 1, status));
-                    if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_p_full + 0, j & 1, status));
-                    if (!ok) break;
-                    tc_fence_after();
-                    issue_pv(kColO, kColS, dv, j > 0);
-                    commit(bar_o_done + 0);
-                    // S_0(j+1)
-                    if (j + 1 < n) {
-                        const int st1 = (j + 1) % kStages;
-                        ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_k_full + st1, ((j + 1) / kStages) & 1, status));
-                        if (!ok) break;
+                    if (ok) {
                         tc_fence_after();
-                        issue_s(kColS, dq0, dk0 + st1 * kStageStep);
+                        issue_s(kColS, dq0, dk0);
                         commit(bar_s_full + 0);
                     }
-                    // PV_1(j)
-                    ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_p_full + 1, j & 1, status));
-                    if (!ok) break;
-                    tc_fence_after();
-                    issue_pv(kColO + 128, kColS + 128, dv, j > 0);
-                    commit(bar_o_done + 1);
-                    commit(bar_v_empty + st);
-                }
+                    for (int j = 0; ok && j < n; ++j) {
+                        const int st = j % kStages;
+                        const uint64_t dk = dk0 + st * kStageStep;
+                        const uint64_t dv = dv0 + st * kStageStep;
+                        // S_1(j): K_j is resident (waited before S_0(j))
+                        issue_s(kColS + 128, dq1, dk);
+                        commit(bar_s_full + 1);
+                        commit(bar_k_empty + st);  // K_j is free once S_0(j) and S_1(j) complete
+                        // PV_0(j)
+                        ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_v_full + st, (j / kStages) & 1, status));
+                        if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_p_full + 0, j & 1, status));
+                        if (!ok) break;
+                        tc_fence_after();
+                        issue_pv(kColO, kColS, dv, j > 0);
+                        commit(bar_o_done + 0);
+                        // S_0(j+1)
+                        if (j + 1 < n) {
+                            const int st1 = (j + 1) % kStages;
+                            ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_k_full + st1, ((j + 1) / kStages) & 1, status));
+                            if (!ok) break;
+                            tc_fence_after();
+                            issue_s(kColS, dq0, dk0 + st1 * kStageStep);
+                            commit(bar_s_full + 0);
+                        }
+                        // PV_1(j)
+                        ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_p_full + 1, j & 1, status));
+                        if (!ok) break;
+                        tc_fence_after();
+                        issue_pv(kColO + 128, kColS + 128, dv, j > 0);
+                        commit(bar_o_done + 1);
+                        commit(bar_v_empty + st);
+                    }
                 }
                 commit(bar_mma_done);
                 mbar_wait(bar_mma_done, 0, status);
