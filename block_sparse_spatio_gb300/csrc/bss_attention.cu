@@ -30,7 +30,9 @@
 //                tile is exponentiated against the reference and kept unless a
 //                row's sum of P over the tile exceeds 2^16; only then are the
 //                max, O and l moved), writes bf16 P to TMEM; finally
-//                normalises O, stores it with a TMA store and writes the LSE.
+//                normalises O, stores it with a TMA store (or, for a permuted
+//                temporal head whose permutation the stores undo, row by row
+//                to the rows' (F,H,W) positions) and writes the LSE.
 // With two halves, warpgroup 0 (warps 0..3) runs at 72 registers a thread and
 // the softmax warpgroups at 208 (setmaxnreg), so that the softmax keeps a
 // tile's P in registers without spilling.
