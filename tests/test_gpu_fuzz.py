@@ -51,3 +51,26 @@ def test_random_geometry_matches_oracle(bss, case):
     for h, fl in enumerate(flags):
         Oref, lref = oracle_rows(q, k, v, h, oracle_kind(fl, tperm), g, None, rounding == 1, BQ=BQ)
         compare(out[h].numpy(), lse[h].numpy(), Oref, lref, f"{name} head {h} rounding {rounding} BQ {BQ}")
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
+def test_random_geometry_fused_equals_step(bss, case):
+    # the permutation applied by the kernel's loads and stores gives the same bits
+    # as the permute -> attention step (LSE compared in (F,H,W) order)
+    name, F, Hs, Ws, wf, ws, d, flags, rounding, tperm, BQ = case
+    N = F * Hs * Ws
+    p = bss.MaskParams(F, Hs, Ws, d, wf, ws, temporal_permuted=tperm, rounding=rounding)
+    q, k, v = W.qkv(W.SMALL, H=len(flags), N=N, d=d, seed=len(name) + N)
+    out, lse, _ = run_gpu(bss, q, k, v, flags, p, BQ=BQ)
+    dev = torch.device("cuda")
+    Q, K, V = (x.to(dev) for x in (q, k, v))
+    O = torch.empty_like(Q)
+    L = torch.empty(len(flags), N, dtype=torch.float32, device=dev)
+    fl = torch.tensor(flags, dtype=torch.uint8, device=dev)
+    with bss.build_tile_map(p, BQ, 128) as tm:
+        bss.sparse_attention_fused(Q, K, V, O, tm, fl, lse=L)
+        torch.cuda.synchronize()
+    assert bss.get_device_status() == 0
+    assert torch.equal(O.float().cpu().view(torch.int32), out.view(torch.int32)), name
+    assert torch.equal(L.cpu().view(torch.int32), lse.view(torch.int32)), name
