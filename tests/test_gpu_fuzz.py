@@ -1,7 +1,9 @@
 """Seeded random small geometries: the tile map bit for bit and the attention
 step (all rows, both layouts of the temporal mask, all three traversal modes,
-both query-tile heights) against the fp64 oracle.  The geometries are drawn from
-a fixed seed, so a failure names a reproducible case."""
+both query-tile heights) against the fp64 oracle; the fused permutation against
+the step bit for bit; routing against the oracle's routing.  The geometries are
+drawn from a fixed seed, so a failure names a reproducible case."""
+import numpy as np
 import pytest
 import torch
 
@@ -74,3 +76,32 @@ def test_random_geometry_fused_equals_step(bss, case):
     assert bss.get_device_status() == 0
     assert torch.equal(O.float().cpu().view(torch.int32), out.view(torch.int32)), name
     assert torch.equal(L.cpu().view(torch.int32), lse.view(torch.int32)), name
+
+
+ROUTE_CASES = CASES[:16]
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("case", ROUTE_CASES, ids=[c[0] for c in ROUTE_CASES])
+def test_random_geometry_routing_matches_oracle(bss, case):
+    name, F, Hs, Ws, wf, ws, d, flags, _, _, _ = case
+    N = F * Hs * Ws
+    H = len(flags)
+    g = torch.Generator().manual_seed(N + H)
+    R = int(torch.randint(1, 301, (1,), generator=g))
+    rows = torch.randint(0, N, (R,), generator=g).tolist()
+    q, k, v = W.qkv(W.SMALL, H=H, N=N, d=d, seed=len(name) + 7)
+    dev = torch.device("cuda")
+    Q, K, V = (x.to(dev) for x in (q, k, v))
+    fl = torch.empty(H, dtype=torch.uint8, device=dev)
+    err = torch.empty(H, 2, dtype=torch.float32, device=dev)
+    bss.route_heads(Q, K, V, bss.MaskParams(F, Hs, Ws, d, wf, ws), torch.tensor(rows, dtype=torch.int32, device=dev),
+                    fl, err)
+    torch.cuda.synchronize()
+    assert bss.get_device_status() == 0
+    oflags, oerr = oracle.route(W.bf16_bits(q), W.bf16_bits(k), W.bf16_bits(v),
+                                oracle.Geometry(F, Hs, Ws, wf=wf, ws=ws), rows)
+    e = err.cpu().numpy()
+    np.testing.assert_allclose(e, oerr, rtol=5e-3, atol=1e-6)
+    clear = np.abs(oerr[:, 0] - oerr[:, 1]) > 1e-2 * np.maximum(oerr[:, 0], oerr[:, 1])
+    assert np.array_equal(fl.cpu().numpy()[clear], oflags[clear])
