@@ -508,16 +508,17 @@ def variants(bss, torch, W, w, H, Q, K, V, dev, peaks, flags):
     pe = bss.MaskParams(w.F, w.Hs, w.Ws, w.d, w.wf, w.ws, temporal_permuted=1, rounding=0)
     zeros_ = torch.zeros(H, dtype=torch.uint8, device=dev)
     lat = {}
-    qmaps = {bq: bss.build_tile_map(pe, BQ=bq) for bq in bss.ATTN_BQ_SUPPORTED}
+    qmaps = {(bq, bkv): bss.build_tile_map(pe, BQ=bq, BKV=bkv)
+             for bq in bss.ATTN_BQ_SUPPORTED for bkv in bss.ATTN_BKV_SUPPORTED}
     try:
-        qms = _time_interleaved(torch, {bq: (lambda tmq=tmq: bss.sparse_attention(Q, K, V, O, tmq, zeros_))
-                                        for bq, tmq in qmaps.items()})
-        for bq, tmq in qmaps.items():
+        qms = _time_interleaved(torch, {key: (lambda tmq=tmq: bss.sparse_attention(Q, K, V, O, tmq, zeros_))
+                                        for key, tmq in qmaps.items()})
+        for (bq, bkv), tmq in qmaps.items():
             st0 = tmq.stats(0)
-            ms = qms[bq]
+            ms = qms[(bq, bkv)]
             ex = st0["full"] + st0["boundary"] + st0["pad"]
-            lat[f"BQ{bq}_BKV128"] = {"ms": ms, "tflops": 4.0 * w.d * H * st0["retained_pairs"] / ms / 1e9,
-                                     "masked_share": (st0["boundary"] + st0["pad"]) / ex}
+            lat[f"BQ{bq}_BKV{bkv}"] = {"ms": ms, "tflops": 4.0 * w.d * H * st0["retained_pairs"] / ms / 1e9,
+                                       "masked_share": (st0["boundary"] + st0["pad"]) / ex}
     finally:
         for tmq in qmaps.values():
             tmq.destroy()

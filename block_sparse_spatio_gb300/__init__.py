@@ -25,6 +25,7 @@ KIND_SPATIAL, KIND_TEMPORAL = 0, 1
 CLASS_FULL, CLASS_BOUNDARY, CLASS_PAD = 0, 1, 2
 ATTN_BQ, ATTN_BKV = 256, 128   # default tile shape of bss_sparse_attention's map
 ATTN_BQ_SUPPORTED = (128, 256)  # query rows per tile it runs (one or two 128-row MMA halves)
+ATTN_BKV_SUPPORTED = (64, 128)  # keys per tile it runs (routing, dense control and fused permutation: 128)
 CLASS_SHIFT = 30
 TILE_INDEX_MASK = (1 << 30) - 1
 STAT_NAMES = ("full", "boundary", "pad", "skip", "retained_pairs", "exact_retained_pairs")

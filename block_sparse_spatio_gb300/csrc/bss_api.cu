@@ -311,10 +311,10 @@ bss_status sparse_attention_impl(const void* Q, const void* K, const void* V, vo
     if (!aligned16(Q) || !aligned16(K) || !aligned16(V) || !aligned16(O) || (lse && (reinterpret_cast<uintptr_t>(lse) & 3u)))
         return set_error(BSS_ERR_INVALID_ARG, "tensors must be 16-byte aligned");
     if (H <= 0) return set_error(BSS_ERR_INVALID_ARG, "H must be positive");
-    if (!attention_supports_block_q(map->BQ) || map->BKV != attention_block_kv())
+    if (!attention_supports_block_q(map->BQ) || !attention_supports_block_kv(map->BKV))
         return set_error(BSS_ERR_UNSUPPORTED,
-                         "attention needs a map built with BQ = 128 or 256 and BKV = %d (got %d x %d)",
-                         attention_block_kv(), map->BQ, map->BKV);
+                         "attention needs a map built with BQ = 128 or 256 and BKV = 64 or 128 (got %d x %d)",
+                         map->BQ, map->BKV);
     if (!std::isfinite(softmax_scale)) return set_error(BSS_ERR_INVALID_ARG, "softmax_scale is not finite");
     int dev = 0;
     cudaGetDevice(&dev);
@@ -346,6 +346,7 @@ bss_status sparse_attention_impl(const void* Q, const void* K, const void* V, vo
     a.softmax_scale = softmax_scale;
     a.fused = fused;
     a.bq = map->BQ;
+    a.bkv = map->BKV;
     a.Qt = Qt;
     a.Kt = Kt;
     a.Vt = Vt;

@@ -130,13 +130,15 @@ __device__ __forceinline__ void fused_rows4(const AttnArgs& a, int h, int p0, in
     }
 }
 
-template <int D, int HALVES = 2>
+template <int D, int HALVES = 2, int BKV = kBKV>
 struct Smem {
-    static constexpr uint32_t kTile = kHalf * D * 2;  // bytes of one 128-row bf16 tile
-    static constexpr uint32_t kQ = 0;                 // the q halves
+    static constexpr uint32_t kTile = kHalf * D * 2;   // bytes of one 128-row bf16 tile (a q half)
+    static constexpr uint32_t kTileKV = BKV * D * 2;   // bytes of one K or V tile
+    static constexpr uint32_t kChunkKV = BKV * 128u;  // one 64-column (128-byte) chunk of a K or V tile
+    static constexpr uint32_t kQ = 0;                  // the q halves
     static constexpr uint32_t kK = HALVES * kTile;
-    static constexpr uint32_t kV = kK + kStages * kTile;
-    static constexpr uint32_t kBar = kV + kStages * kTile;
+    static constexpr uint32_t kV = kK + kStages * kTileKV;
+    static constexpr uint32_t kBar = kV + kStages * kTileKV;
     // q, k_full[S], v_full[S], k_empty[S], v_empty[S], s_full[2], p_full[2], o_done[2], mma_done
     static constexpr uint32_t kNumBars = 1 + 4 * kStages + 2 + 2 + 2 + 1;
     static constexpr uint32_t kBytes = kBar + kNumBars * 8 + 16;
@@ -148,14 +150,16 @@ __device__ __forceinline__ uint32_t bits_range(int lo, int hi) {  // 0 <= lo < h
     return h & ~((1u << lo) - 1u);
 }
 
-// OR the columns of [lo, hi) that fall inside the tile starting at column c0.
-__device__ __forceinline__ void add_interval(uint32_t (&bits)[4], int lo, int hi, int c0) {
+// OR the columns of [lo, hi) that fall inside the tile of NW * 32 columns
+// starting at column c0.
+template <int NW>
+__device__ __forceinline__ void add_interval(uint32_t (&bits)[NW], int lo, int hi, int c0) {
     int l = lo - c0, h = hi - c0;
     l = l < 0 ? 0 : l;
-    h = h > kBKV ? kBKV : h;
+    h = h > NW * 32 ? NW * 32 : h;
     if (h <= l) return;
 #pragma unroll
-    for (int w = 0; w < 4; ++w) {
+    for (int w = 0; w < NW; ++w) {
         int lw = l - 32 * w, hw = h - 32 * w;
         lw = lw < 0 ? 0 : lw;
         hw = hw > 32 ? 32 : hw;
@@ -188,9 +192,11 @@ __device__ __forceinline__ RowPred row_pred(const AttnArgs& a, int code, int q) 
 //   boundary tile: the coordinate predicate (all masks are unions of <= 3
 //   intervals except the striped (F,H,W) temporal mask, one interval per frame);
 //   padding tile: the real-column predicate only.
-__device__ __forceinline__ void tile_bits(uint32_t (&bits)[4], const AttnArgs& a, int code, int cls, int c0,
+template <int NW>
+__device__ __forceinline__ void tile_bits(uint32_t (&bits)[NW], const AttnArgs& a, int code, int cls, int c0,
                                           const RowPred& rp) {
-    bits[0] = bits[1] = bits[2] = bits[3] = 0u;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) bits[w] = 0u;
     if (cls == BSS_CLASS_PAD) {
         if (code == MASK_TEMPORAL_VIRT) {
             add_interval(bits, 0, a.S, c0);
@@ -211,7 +217,7 @@ __device__ __forceinline__ void tile_bits(uint32_t (&bits)[4], const AttnArgs& a
         add_interval(bits, 0, a.S, c0);  // frame 0 entirely
         int f_lo = c0 / a.S;
         f_lo = f_lo < 1 ? 1 : f_lo;
-        int f_hi = (c0 + kBKV - 1) / a.S;
+        int f_hi = (c0 + NW * 32 - 1) / a.S;
         f_hi = f_hi > a.F - 1 ? a.F - 1 : f_hi;
         for (int f = f_lo; f <= f_hi; ++f) add_interval(bits, f * a.S + rp.lo, f * a.S + rp.hi, c0);
     } else {
@@ -222,26 +228,28 @@ __device__ __forceinline__ void tile_bits(uint32_t (&bits)[4], const AttnArgs& a
 // j-th kv tile of the work item: from the tile map, or every tile from j0 on
 // (dense control and routing: FULL, PAD for a ragged last tile; BOUNDARY for a
 // masked routing kind, whose rows are scattered sampled queries)
-template <bool ROUTE>
+template <bool ROUTE, int BKV = kBKV>
 __device__ __forceinline__ uint32_t entry_at(const AttnArgs& a, const int32_t* ents, int j, int code, int j0) {
     if constexpr (ROUTE) {
         const int t = j0 + j;
-        uint32_t cls = (t == a.nkv_dense - 1 && (a.N % kBKV) != 0) ? BSS_CLASS_PAD : BSS_CLASS_FULL;
+        uint32_t cls = (t == a.nkv_dense - 1 && (a.N % BKV) != 0) ? BSS_CLASS_PAD : BSS_CLASS_FULL;
         if (code != MASK_DENSE) cls = BSS_CLASS_BOUNDARY;
         return static_cast<uint32_t>(t) | (cls << BSS_CLASS_SHIFT);
     } else {
         if (a.dense) {
-            const uint32_t cls = (j == a.nkv_dense - 1 && (a.N % kBKV) != 0) ? BSS_CLASS_PAD : BSS_CLASS_FULL;
+            const uint32_t cls = (j == a.nkv_dense - 1 && (a.N % BKV) != 0) ? BSS_CLASS_PAD : BSS_CLASS_FULL;
             return static_cast<uint32_t>(j) | (cls << BSS_CLASS_SHIFT);
         }
         return static_cast<uint32_t>(__ldg(ents + j));
     }
 }
 
-template <int D, bool ROUTE, int HALVES>
+template <int D, bool ROUTE, int HALVES, int BKV = kBKV>
 __global__ void __launch_bounds__(threads_for<HALVES>(), 1) attn_fwd_kernel(const __grid_constant__ AttnArgs args) {
     static_assert(HALVES == 1 || HALVES == 2, "one or two 128-row halves per CTA");
-    using L = Smem<D, HALVES>;
+    static_assert(BKV == 64 || BKV == 128, "kv tiles of 64 or 128 keys");
+    using L = Smem<D, HALVES, BKV>;
+    constexpr int kNW = BKV / 32;  // 32-column chunks of a kv tile (words of its row bitmask)
     constexpr int kBQt = HALVES * kHalf;  // query rows per CTA
     constexpr int kChunks = D / 64;  // 64-column (128-byte) swizzle atoms per row
 
@@ -328,7 +336,7 @@ __global__ void __launch_bounds__(threads_for<HALVES>(), 1) attn_fwd_kernel(cons
     // temporal head whose (H,W,F) permutation is applied by the loads and stores
     // (fused mode 1), or by the output stores only (mode 2: Q, K, V come permuted,
     // O rows go straight to their (F,H,W) positions)
-    const bool gather = !ROUTE && args.fused == 1 && code == MASK_TEMPORAL_VIRT;
+    const bool gather = BKV == 128 && !ROUTE && args.fused == 1 && code == MASK_TEMPORAL_VIRT;
     const bool scatter = gather || (!ROUTE && args.fused == 2 && code == MASK_TEMPORAL_VIRT);
 
     if (warp < 4) {
@@ -358,46 +366,46 @@ __global__ void __launch_bounds__(threads_for<HALVES>(), 1) attn_fwd_kernel(cons
             int jk = 0, jv = 0;
             for (; jv < n; ++jv) {
                 const int st = jv % kStages;
-                const uint32_t e = entry_at<ROUTE>(args, ents, jv, code, j0);
-                const int col0 = static_cast<int>(e & BSS_TILE_INDEX_MASK) * kBKV;
+                const uint32_t e = entry_at<ROUTE, BKV>(args, ents, jv, code, j0);
+                const int col0 = static_cast<int>(e & BSS_TILE_INDEX_MASK) * BKV;
                 const bool sink = col0 < args.S_pad;
                 int r4[4] = {0, 0, 0, 0};
                 if (!sink) fused_rows4(args, h, col0 - args.S_pad + 4 * lane, r4);
                 if (jv >= kStages)
                     ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_k_empty + st, ((jv / kStages) - 1) & 1, status));
                 if (!ok) break;
-                if (lane == 0) mbar_arrive_expect_tx(bar_k_full + st, L::kTile);
+                if (lane == 0) mbar_arrive_expect_tx(bar_k_full + st, L::kTileKV);
                 __syncwarp();
                 if (sink) {
                     if (lane == 0) {
 #pragma unroll
                         for (int c = 0; c < kChunks; ++c)
-                            tma_load_3d(sK + st * L::kTile + c * kChunkBytesSw128, &args.tm_ks, c * 64, col0, h,
+                            tma_load_3d(sK + st * L::kTileKV + c * L::kChunkKV, &args.tm_ks, c * 64, col0, h,
                                         bar_k_full + st);
                     }
                 } else {
 #pragma unroll
                     for (int c = 0; c < kChunks; ++c)
-                        tma_gather4_2d(sK + st * L::kTile + c * kChunkBytesSw128 + lane * 512, &args.tm_kg, c * 64, r4[0],
+                        tma_gather4_2d(sK + st * L::kTileKV + c * L::kChunkKV + lane * 512, &args.tm_kg, c * 64, r4[0],
                                        r4[1], r4[2], r4[3], bar_k_full + st);
                 }
                 jk = jv + 1;
                 if (jv >= kStages)
                     ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_v_empty + st, ((jv / kStages) - 1) & 1, status));
                 if (!ok) break;
-                if (lane == 0) mbar_arrive_expect_tx(bar_v_full + st, L::kTile);
+                if (lane == 0) mbar_arrive_expect_tx(bar_v_full + st, L::kTileKV);
                 __syncwarp();
                 if (sink) {
                     if (lane == 0) {
 #pragma unroll
                         for (int c = 0; c < kChunks; ++c)
-                            tma_load_3d(sV + st * L::kTile + c * kChunkBytesSw128, &args.tm_vs, c * 64, col0, h,
+                            tma_load_3d(sV + st * L::kTileKV + c * L::kChunkKV, &args.tm_vs, c * 64, col0, h,
                                         bar_v_full + st);
                     }
                 } else {
 #pragma unroll
                     for (int c = 0; c < kChunks; ++c)
-                        tma_gather4_2d(sV + st * L::kTile + c * kChunkBytesSw128 + lane * 512, &args.tm_vg, c * 64, r4[0],
+                        tma_gather4_2d(sV + st * L::kTileKV + c * L::kChunkKV + lane * 512, &args.tm_vg, c * 64, r4[0],
                                        r4[1], r4[2], r4[3], bar_v_full + st);
                 }
             }
@@ -428,8 +436,8 @@ __global__ void __launch_bounds__(threads_for<HALVES>(), 1) attn_fwd_kernel(cons
                 int jk = 0, jv = 0;  // K tiles and V tiles issued
                 for (; jv < n; ++jv) {
                     const int st = jv % kStages;
-                    const uint32_t e = entry_at<ROUTE>(args, ents, jv, code, j0);
-                    const int col0 = static_cast<int>(e & BSS_TILE_INDEX_MASK) * kBKV;
+                    const uint32_t e = entry_at<ROUTE, BKV>(args, ents, jv, code, j0);
+                    const int col0 = static_cast<int>(e & BSS_TILE_INDEX_MASK) * BKV;
                     const CUtensorMap* mk = mk0;
                     const CUtensorMap* mv = mv0;
                     int row = col0;
@@ -443,17 +451,17 @@ __global__ void __launch_bounds__(threads_for<HALVES>(), 1) attn_fwd_kernel(cons
                     }
                     if (jv >= kStages) ok = mbar_wait(bar_k_empty + st, ((jv / kStages) - 1) & 1, status);
                     if (!ok) break;
-                    mbar_arrive_expect_tx(bar_k_full + st, L::kTile);
+                    mbar_arrive_expect_tx(bar_k_full + st, L::kTileKV);
 #pragma unroll
                     for (int c = 0; c < kChunks; ++c)
-                        tma_load_3d(sK + st * L::kTile + c * kChunkBytesSw128, mk, c * 64, row, h, bar_k_full + st);
+                        tma_load_3d(sK + st * L::kTileKV + c * L::kChunkKV, mk, c * 64, row, h, bar_k_full + st);
                     jk = jv + 1;
                     if (jv >= kStages) ok = mbar_wait(bar_v_empty + st, ((jv / kStages) - 1) & 1, status);
                     if (!ok) break;
-                    mbar_arrive_expect_tx(bar_v_full + st, L::kTile);
+                    mbar_arrive_expect_tx(bar_v_full + st, L::kTileKV);
 #pragma unroll
                     for (int c = 0; c < kChunks; ++c)
-                        tma_load_3d(sV + st * L::kTile + c * kChunkBytesSw128, mv, c * 64, row, h, bar_v_full + st);
+                        tma_load_3d(sV + st * L::kTileKV + c * L::kChunkKV, mv, c * 64, row, h, bar_v_full + st);
                 }
                 // drain: no copy may still be landing in shared memory at exit
                 mbar_wait(bar_q, 0, status);
@@ -466,30 +474,33 @@ __global__ void __launch_bounds__(threads_for<HALVES>(), 1) attn_fwd_kernel(cons
             // =========================== MMA issuer: the whole warp runs the loop (so
             // descriptors stay warp-uniform), one elected lane issues and commits.
             if (n > 0) {
-                constexpr uint32_t idesc_qk = idesc_bf16_f32(kHalf, kBKV, 0);
+                constexpr uint32_t idesc_qk = idesc_bf16_f32(kHalf, BKV, 0);
                 constexpr uint32_t idesc_pv = idesc_bf16_f32(kHalf, D, 1);
                 const bool leader = elect_one();
                 // base descriptors; K step kk adds (kk / 4) * 16 KiB + (kk % 4) * 32 bytes
                 // (K-major) or kk * 2 KiB (MN-major) to the start-address field (>> 4)
                 const uint64_t dq0 = desc_kmajor_sw128(smem_u32(sQ), 0);
                 const uint64_t dq1 = desc_kmajor_sw128(smem_u32(sQ + L::kTile), 0);
-                const uint64_t dk0 = desc_kmajor_sw128(smem_u32(sK), 0);
-                const uint64_t dv0 = desc_mnmajor_sw128(smem_u32(sV), 0);
-                constexpr uint64_t kStageStep = L::kTile >> 4;
-                auto kstep = [](int kk) -> uint64_t {
+                const uint64_t dk0 = desc_kmajor_sw128(smem_u32(sK), 0, L::kChunkKV);
+                const uint64_t dv0 = desc_mnmajor_sw128(smem_u32(sV), 0, L::kChunkKV);
+                constexpr uint64_t kStageStep = L::kTileKV >> 4;  // one K or V stage
+                auto kstep = [](int kk) -> uint64_t {  // Q: 128-row chunks
                     return static_cast<uint64_t>((kk >> 2) * (kChunkBytesSw128 >> 4) + (kk & 3) * 2);
+                };
+                auto kstep_kv = [](int kk) -> uint64_t {  // K: BKV-row chunks
+                    return static_cast<uint64_t>((kk >> 2) * (L::kChunkKV >> 4) + (kk & 3) * 2);
                 };
                 auto issue_s = [&](uint32_t d_col, uint64_t dq, uint64_t dk) {
                     if (leader) {
 #pragma unroll
                         for (int kk = 0; kk < D / 16; ++kk)
-                            umma_ss(tmem + d_col, dq + kstep(kk), dk + kstep(kk), idesc_qk, kk > 0 ? 1u : 0u);
+                            umma_ss(tmem + d_col, dq + kstep(kk), dk + kstep_kv(kk), idesc_qk, kk > 0 ? 1u : 0u);
                     }
                 };
                 auto issue_pv = [&](uint32_t d_col, uint32_t p_col, uint64_t dv, bool acc) {
                     if (leader) {
 #pragma unroll
-                        for (int kk = 0; kk < kBKV / 16; ++kk)
+                        for (int kk = 0; kk < BKV / 16; ++kk)
                             umma_ts(tmem + d_col, tmem + p_col + kk * 8, dv + static_cast<uint64_t>(kk * 128), idesc_pv,
                                     (acc || kk > 0) ? 1u : 0u);
                     }
@@ -598,9 +609,9 @@ __global__ void __launch_bounds__(threads_for<HALVES>(), 1) attn_fwd_kernel(cons
         float l = 0.0f;
         bool ok = true;
         for (int j = 0; j < n; ++j) {
-            const uint32_t e = entry_at<ROUTE>(args, ents, j, code, j0);
+            const uint32_t e = entry_at<ROUTE, BKV>(args, ents, j, code, j0);
             const int cls = static_cast<int>(e >> BSS_CLASS_SHIFT);
-            const int c0 = static_cast<int>(e & BSS_TILE_INDEX_MASK) * kBKV;
+            const int c0 = static_cast<int>(e & BSS_TILE_INDEX_MASK) * BKV;
             // one half: the four softmax warps start every tile together.  S(j+1) is
             // issued before PV(j), so without this a warp could run a tile ahead of
             // another; the outputs then came out wrong when rows rescaled O after
@@ -620,23 +631,26 @@ __global__ void __launch_bounds__(threads_for<HALVES>(), 1) attn_fwd_kernel(cons
             // result is kept unless some row's sum of P exceeds kSumLimit (then the
             // tile is redone on the general path).
             bool done = false;
-            // one pass over the row's 128 scores; MASKED applies the tile's
-            // retained-column bitmask (boundary / padding tiles)
+            // one pass over the row's BKV scores; MASKED applies the tile's
+            // retained-column bitmask (boundary / padding tiles; a 64-key tile uses
+            // the first two words: the parameter has a fixed size because nvcc 13.0
+            // crashes on a generic lambda taking an array of a template-dependent
+            // size by reference)
             auto single_pass = [&](auto masked_tag, const uint32_t (&bits)[4]) -> bool {
                 constexpr bool MASKED = decltype(masked_tag)::value;
-                uint32_t pk[64];
+                uint32_t pk[BKV / 2];
                 uint64_t s2a = 0ull, s2b = 0ull;  // packed partial sums (two chains)
                 const uint64_t c2 = f2_pack(c, c);
                 const uint64_t nm2 = f2_pack(-m, -m);
                 // the row's 128 scores in one wait, so that the scheduler has 64
                 // independent pairs to interleave with the exponentials (measured:
                 // 1.9% faster than a wait per 32-column chunk)
-                uint32_t sb[4][32];
+                uint32_t sb[kNW][32];
 #pragma unroll
-                for (int cc = 0; cc < 4; ++cc) BSS_TMEM_LD32(t_s + 32 * cc, sb[cc]);
+                for (int cc = 0; cc < kNW; ++cc) BSS_TMEM_LD32(t_s + 32 * cc, sb[cc]);
                 tmem_wait_ld();
 #pragma unroll
-                for (int cc = 0; cc < 4; ++cc) {
+                for (int cc = 0; cc < kNW; ++cc) {
                     const uint32_t (&sr)[32] = sb[cc];
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
@@ -665,7 +679,7 @@ __global__ void __launch_bounds__(threads_for<HALVES>(), 1) attn_fwd_kernel(cons
                 // P in 16-column stores (measured: 1.6% faster than 32-column ones,
                 // 1% slower with 8-column ones)
 #pragma unroll
-                for (int q4 = 0; q4 < 4; ++q4) BSS_TMEM_ST16(t_s + 16 * q4, (pk + 16 * q4));
+                for (int q4 = 0; q4 < kNW; ++q4) BSS_TMEM_ST16(t_s + 16 * q4, (pk + 16 * q4));
                 return true;
             };
             if (__all_sync(0xFFFFFFFFu, m != -INFINITY)) {
@@ -674,7 +688,7 @@ __global__ void __launch_bounds__(threads_for<HALVES>(), 1) attn_fwd_kernel(cons
                     done = single_pass(std::integral_constant<bool, false>(), none);
                 } else {
                     uint32_t bits[4];
-                    tile_bits(bits, args, code, cls, c0, rp);
+                    tile_bits<kNW>(*reinterpret_cast<uint32_t(*)[kNW]>(bits), args, code, cls, c0, rp);
                     done = single_pass(std::integral_constant<bool, true>(), bits);
                 }
             }
@@ -683,12 +697,13 @@ __global__ void __launch_bounds__(threads_for<HALVES>(), 1) attn_fwd_kernel(cons
                 // a row, or a reference max that must move.  Pass 1 finds the row max,
                 // pass 2 exponentiates and writes P chunk by chunk.
                 uint32_t bits[4] = {0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu};
-                if (cls != BSS_CLASS_FULL) tile_bits(bits, args, code, cls, c0, rp);
+                if (cls != BSS_CLASS_FULL)
+                    tile_bits<kNW>(*reinterpret_cast<uint32_t(*)[kNW]>(bits), args, code, cls, c0, rp);
                 float mx[8];
 #pragma unroll
                 for (int t = 0; t < 8; ++t) mx[t] = -INFINITY;
 #pragma unroll
-                for (int cc = 0; cc < 4; ++cc) {
+                for (int cc = 0; cc < kNW; ++cc) {
                     uint32_t sr[32];
                     BSS_TMEM_LD32(t_s + 32 * cc, sr);
                     tmem_wait_ld();
@@ -727,7 +742,7 @@ __global__ void __launch_bounds__(threads_for<HALVES>(), 1) attn_fwd_kernel(cons
                 // which chunks <= cc have already been read from.
                 float sm[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-                for (int cc = 0; cc < 4; ++cc) {
+                for (int cc = 0; cc < kNW; ++cc) {
                     uint32_t sr[32];
                     BSS_TMEM_LD32(t_s + 32 * cc, sr);
                     tmem_wait_ld();
@@ -854,9 +869,15 @@ bss_status launch_d(const AttnLaunch& a, cudaStream_t stream) {
     bss_status st;
     // query rows per head: N, or the sampled rows in routing mode
     const int64_t nq_rows = a.route ? a.Nq : a.N;
+    // keys per kv tile: the map's BKV (routing, the dense control and the fused
+    // permutation use 128)
+    const int bkv = (a.route || a.dense || a.bkv == 0) ? kBKV : a.bkv;
+    if (bkv != 64 && bkv != kBKV) return set_error(BSS_ERR_UNSUPPORTED, "kv tile of %d keys", bkv);
+    if (a.fused == 1 && bkv != kBKV)
+        return set_error(BSS_ERR_UNSUPPORTED, "the fused permutation needs %d-key tiles", kBKV);
     if ((st = encode_tmap_3d(&args.tm_q, a.Q, a.d, nq_rows, a.H, rs, rs * nq_rows, 64, kHalf)) != BSS_OK) return st;
-    if ((st = encode_tmap_3d(&args.tm_k, a.K, a.d, a.N, a.H, rs, hs, 64, kBKV)) != BSS_OK) return st;
-    if ((st = encode_tmap_3d(&args.tm_v, a.V, a.d, a.N, a.H, rs, hs, 64, kBKV)) != BSS_OK) return st;
+    if ((st = encode_tmap_3d(&args.tm_k, a.K, a.d, a.N, a.H, rs, hs, 64, bkv)) != BSS_OK) return st;
+    if ((st = encode_tmap_3d(&args.tm_v, a.V, a.d, a.N, a.H, rs, hs, 64, bkv)) != BSS_OK) return st;
     if ((st = encode_tmap_3d(&args.tm_o, a.route ? a.Q : a.O, a.d, nq_rows, a.H, rs, rs * nq_rows, 64, kHalf)) !=
         BSS_OK)
         return st;
@@ -869,11 +890,11 @@ bss_status launch_d(const AttnLaunch& a, cudaStream_t stream) {
     const void* Vt = a.Vt ? a.Vt : a.V;
     void* Ot = a.Ot ? a.Ot : (a.route ? const_cast<void*>(a.Q) : a.O);
     if ((st = encode_tmap_3d(&args.tm_qt, Qt, a.d, nq_rows, a.H, rs, rs * nq_rows, 64, kHalf)) != BSS_OK) return st;
-    if ((st = encode_tmap_3d(&args.tm_kt, Kt, a.d, a.N, a.H, rs, hs, 64, kBKV)) != BSS_OK) return st;
-    if ((st = encode_tmap_3d(&args.tm_vt, Vt, a.d, a.N, a.H, rs, hs, 64, kBKV)) != BSS_OK) return st;
+    if ((st = encode_tmap_3d(&args.tm_kt, Kt, a.d, a.N, a.H, rs, hs, 64, bkv)) != BSS_OK) return st;
+    if ((st = encode_tmap_3d(&args.tm_vt, Vt, a.d, a.N, a.H, rs, hs, 64, bkv)) != BSS_OK) return st;
     if ((st = encode_tmap_3d(&args.tm_ot, Ot, a.d, nq_rows, a.H, rs, rs * nq_rows, 64, kHalf)) != BSS_OK) return st;
-    if ((st = encode_tmap_3d(&args.tm_ks, Kt, a.d, a.S, a.H, sink_rs, hs, 64, kBKV)) != BSS_OK) return st;
-    if ((st = encode_tmap_3d(&args.tm_vs, Vt, a.d, a.S, a.H, sink_rs, hs, 64, kBKV)) != BSS_OK) return st;
+    if ((st = encode_tmap_3d(&args.tm_ks, Kt, a.d, a.S, a.H, sink_rs, hs, 64, bkv)) != BSS_OK) return st;
+    if ((st = encode_tmap_3d(&args.tm_vs, Vt, a.d, a.S, a.H, sink_rs, hs, 64, bkv)) != BSS_OK) return st;
     if (a.fused == 1) {
         const uint64_t rows = static_cast<uint64_t>(a.H) * static_cast<uint64_t>(a.N);
         if (rows > 0x7FFFFFFFull) return set_error(BSS_ERR_UNSUPPORTED, "H*N too large for the fused permutation");
@@ -916,9 +937,16 @@ bss_status launch_d(const AttnLaunch& a, cudaStream_t stream) {
     // choice (the dense control uses two)
     const int halves = a.dense ? 2 : a.bq / kHalf;
     if (halves != 1 && halves != 2) return set_error(BSS_ERR_UNSUPPORTED, "query tile of %d rows", a.bq);
-    const uint32_t smem = halves == 2 ? Smem<D, 2>::kAlloc : Smem<D, 1>::kAlloc;
-    auto kernel = a.route ? (halves == 2 ? attn_fwd_kernel<D, true, 2> : attn_fwd_kernel<D, true, 1>)
-                          : (halves == 2 ? attn_fwd_kernel<D, false, 2> : attn_fwd_kernel<D, false, 1>);
+    uint32_t smem;
+    void (*kernel)(AttnArgs);
+    if (bkv == 64) {  // the tile-shape comparison's 64-key tiles (not in routing)
+        smem = halves == 2 ? Smem<D, 2, 64>::kAlloc : Smem<D, 1, 64>::kAlloc;
+        kernel = halves == 2 ? attn_fwd_kernel<D, false, 2, 64> : attn_fwd_kernel<D, false, 1, 64>;
+    } else {
+        smem = halves == 2 ? Smem<D, 2>::kAlloc : Smem<D, 1>::kAlloc;
+        kernel = a.route ? (halves == 2 ? attn_fwd_kernel<D, true, 2> : attn_fwd_kernel<D, true, 1>)
+                         : (halves == 2 ? attn_fwd_kernel<D, false, 2> : attn_fwd_kernel<D, false, 1>);
+    }
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return cuda_check(e, "cudaFuncSetAttribute(attention)");
     const int64_t items = static_cast<int64_t>(a.H) * a.nq * (a.route ? 3 * a.splits : 1);
@@ -934,6 +962,7 @@ bss_status launch_d(const AttnLaunch& a, cudaStream_t stream) {
 int attention_block_q() { return kBQ; }
 bool attention_supports_block_q(int bq) { return bq == kHalf || bq == 2 * kHalf; }
 int attention_block_kv() { return kBKV; }
+bool attention_supports_block_kv(int bkv) { return bkv == 64 || bkv == kBKV; }
 
 bss_status launch_attention(const AttnLaunch& a, cudaStream_t stream) {
     if (a.d == 128) return launch_d<128>(a, stream);

@@ -76,7 +76,8 @@ struct AttnLaunch {
     // order) over Nq sampled query rows per head whose tokens are qmap[r]; every
     // kv tile, split into `splits` ranges; normalised fp32 O and LSE per split
     int32_t route, Nq, splits;
-    int32_t bq;  // query rows per CTA: the map's BQ (128 or 256)
+    int32_t bq;   // query rows per CTA: the map's BQ (128 or 256)
+    int32_t bkv;  // keys per kv tile: the map's BKV (64 or 128; 0 = 128)
     // split buffers: heads with flag 1 read Qt, Kt, Vt and write Ot (NULL: Q, K, V, O)
     const void *Qt, *Kt, *Vt;
     void* Ot;
@@ -87,7 +88,8 @@ struct AttnLaunch {
 bss_status launch_attention(const AttnLaunch& a, cudaStream_t stream);
 int attention_block_q();   // query rows per attention tile of the default shape (the map's BQ)
 bool attention_supports_block_q(int bq);  // 128 (one MMA half per CTA) or 256 (two)
-int attention_block_kv();  // key columns per attention tile (the map's BKV)
+int attention_block_kv();  // key columns per attention tile of routing and the dense control
+bool attention_supports_block_kv(int bkv);  // 64 or 128 for a map-driven call
 
 // helpers (bss_api.cu)
 bss_status set_error(bss_status st, const char* fmt, ...);

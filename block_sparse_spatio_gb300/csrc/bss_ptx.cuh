@@ -250,17 +250,19 @@ constexpr uint32_t kChunkBytesSw128 = 128u * 128u;
 // K-major operand (Q or K: contraction over the D columns), K step kk of 16
 // columns: 32 bytes further inside the 128-byte swizzle row, next chunk every
 // 4 steps; 8-row groups are 1024 bytes apart.
-__device__ __forceinline__ uint64_t desc_kmajor_sw128(uint32_t tile_base, int kk) {
-    return smem_desc_sw128(tile_base + static_cast<uint32_t>(kk >> 2) * kChunkBytesSw128 +
-                               static_cast<uint32_t>(kk & 3) * 32u,
+__device__ __forceinline__ uint64_t desc_kmajor_sw128(uint32_t tile_base, int kk,
+                                                      uint32_t chunk_bytes = kChunkBytesSw128) {
+    return smem_desc_sw128(tile_base + static_cast<uint32_t>(kk >> 2) * chunk_bytes + static_cast<uint32_t>(kk & 3) * 32u,
                            16, 1024);
 }
 
-// MN-major operand (V: contraction over the 128 rows, N = D columns), K step kk
-// of 16 rows = 2048 bytes; 64-column chunks are 16 KiB apart (leading offset),
-// 8-row groups 1024 bytes apart (stride offset).
-__device__ __forceinline__ uint64_t desc_mnmajor_sw128(uint32_t tile_base, int kk) {
-    return smem_desc_sw128(tile_base + static_cast<uint32_t>(kk) * 2048u, kChunkBytesSw128, 1024);
+// MN-major operand (V: contraction over the tile's rows, N = D columns), K step
+// kk of 16 rows = 2048 bytes; 64-column chunks are chunk_bytes apart (leading
+// offset: 16 KiB for 128-row tiles), 8-row groups 1024 bytes apart (stride
+// offset).
+__device__ __forceinline__ uint64_t desc_mnmajor_sw128(uint32_t tile_base, int kk,
+                                                       uint32_t chunk_bytes = kChunkBytesSw128) {
+    return smem_desc_sw128(tile_base + static_cast<uint32_t>(kk) * 2048u, chunk_bytes, 1024);
 }
 
 // Instruction descriptor for kind::f16 with bf16 inputs and fp32 accumulate.

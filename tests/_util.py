@@ -20,7 +20,7 @@ def oracle_kind(flag: int, temporal_permuted: int) -> int:
     return oracle.TEMPORAL_PERMUTED if temporal_permuted else oracle.TEMPORAL_FHW
 
 
-def run_gpu(bss, q, k, v, flags, params, want_lse=True, dense=False, BQ=None):
+def run_gpu(bss, q, k, v, flags, params, want_lse=True, dense=False, BQ=None, BKV=None):
     """(F,H,W)-order CPU bf16 q, k, v -> (O [H][N][d] float32 CPU in (F,H,W) order,
     lse [H][N] float32 CPU in (F,H,W) order, tile map stats)."""
     dev = torch.device("cuda")
@@ -34,7 +34,7 @@ def run_gpu(bss, q, k, v, flags, params, want_lse=True, dense=False, BQ=None):
         bss.dense_attention(Q, K, V, O, lse=lse)
     else:
         ws = [torch.empty_like(Q) for _ in range(4)]
-        with bss.build_tile_map(params, BQ=BQ or bss.ATTN_BQ) as tm:
+        with bss.build_tile_map(params, BQ=BQ or bss.ATTN_BQ, BKV=BKV or bss.ATTN_BKV) as tm:
             bss.attention_step(Q, K, V, O, tm, fl, *ws, lse=lse)
             stats = (tm.stats(0), tm.stats(1))
             torch.cuda.synchronize()
@@ -55,14 +55,14 @@ def run_gpu(bss, q, k, v, flags, params, want_lse=True, dense=False, BQ=None):
     return out, lse_c, stats
 
 
-def oracle_rows(q, k, v, h, kind, g, rows, rounding, dense=False, BQ=None):
+def oracle_rows(q, k, v, h, kind, g, rows, rounding, dense=False, BQ=None, BKV=None):
     """Oracle rows; a rounded mask is rounded on the attention kernel's tile grid."""
     import block_sparse_spatio_gb300 as bss
     b = W.bf16_bits
     if dense:
         kind = oracle.DENSE
     return oracle.attention(b(q[h]), b(k[h]), b(v[h]), kind, g, rows=rows, rounding=bool(rounding),
-                            BQ=BQ or bss.ATTN_BQ, BKV=bss.ATTN_BKV)
+                            BQ=BQ or bss.ATTN_BQ, BKV=BKV or bss.ATTN_BKV)
 
 
 def compare(out_rows: np.ndarray, lse_rows, Oref: np.ndarray, lref: np.ndarray, what: str):
