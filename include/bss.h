@@ -113,8 +113,9 @@ typedef struct bss_tile_map_s* bss_tile_map;
  * and skipped tiles; section "Align the sparse mask with final execution":
  * tile-aligned rounding).  Counts retained pairs per tile on the GPU, compacts
  * non-skipped tiles to CSR.  Any BQ, BKV in [16, 65536] builds a map (for
- * statistics); bss_sparse_attention runs maps with BKV = 128 and BQ = 256
- * (two 128-row MMA halves per CTA, the default) or BQ = 128 (one half).
+ * statistics); bss_sparse_attention runs maps with BKV = 128 (the default) or
+ * 64 and BQ = 256 (two 128-row MMA halves per CTA, the default) or BQ = 128
+ * (one half); the fused permutation needs BKV = 128.
  * Synchronous: it allocates the map's device memory, synchronizes `stream`
  * and returns the map in *out.  Errors: INVALID_ARG (null, non-positive or
  * inconsistent sizes, windows < 0), UNSUPPORTED (sink_frames != 1,
@@ -164,8 +165,8 @@ bss_status bss_permute_flagged(const void* in, void* out, const uint8_t* head_is
  *               the map was built with temporal_permuted = 1.
  *   lse         optional device float[H][N], natural-log log-sum-exp per row
  *               (-inf for a row with no retained key, whose O row is 0).
- *   map         built with BKV = 128 and BQ = 256 (default) or 128 for this
- *               geometry.
+ *   map         built for this geometry with BKV = 128 (default) or 64 and
+ *               BQ = 256 (default) or 128.
  *   head_is_temporal  device uint8[H] (NULL = all spatial); changing flags
  *               needs no map rebuild.
  *   softmax_scale    <= 0 selects 1/sqrt(head_dim).
