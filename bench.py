@@ -387,7 +387,7 @@ def main():
                    "head_dim": w.d, "flags_temporal": flags, "spatial_frame_window": w.wf,
                    "temporal_raster_window": w.ws, "mask": ("dense control" if args.dense else
                             ["exact (full/boundary tiles, B2)", "tile-aligned (B3)",
-                             "every visited tile masked (B1)"][args.rounding]), "tile": [128, 128],
+                             "every visited tile masked (B1)"][args.rounding]), "tile": [tm.BQ, tm.BKV],
                    "step": ("dense attention" if args.dense else
                             "permute temporal heads' QKV -> sparse attention storing their O rows in (F,H,W) order"),
                    "l2": f"inputs larger than L2 (Q+K+V = {3 * Q.numel() * 2 / 1e6:.0f} MB)",
@@ -643,8 +643,30 @@ def e2e(bss, torch, params, tm, flags, Qd, Kd, Vd, flops, args):
         return t0.elapsed_time(t1) / n
 
     run(3)
+    # the copies alone, one step's worth each, on an idle GPU: how much time the
+    # pipeline has to hide behind the kernels
+    cs = ws["copy_stream"]
+    c0, c1, c2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+    torch.cuda.synchronize()
+    buf = ws["sets"][0]
+    with torch.cuda.stream(cs):
+        c0.record(cs)
+        for src, dst in ((hq, buf["Q"]), (hk, buf["K"]), (hv, buf["V"])):
+            dst.copy_(src, non_blocking=True)
+        c1.record(cs)
+        ho.copy_(buf["O"], non_blocking=True)
+        c2.record(cs)
+    torch.cuda.synchronize()
+    h2d_ms, d2h_ms = c0.elapsed_time(c1), c1.elapsed_time(c2)
+    sampler = ClockSampler(torch.cuda.current_device())
+    sampler.start()
+    time.sleep(0.3)
+    sampler.mark_begin()
     ms = run(steps)
-    return {"value": flops / (ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": ms, "steps": steps,
+    sampler.mark_end()
+    clocks = sampler.stop()
+    return {"value": flops / (ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": ms, "steps": steps, "clocks": clocks,
+            "copies_alone_ms": {"h2d_qkv": h2d_ms, "d2h_o": d2h_ms},
             "h2d_bytes_per_step": 3 * H * N * d * 2 + H, "d2h_bytes_per_step": H * N * d * 2,
             "pipelining": "two workspace sets: the H2D copy of step i+1 and the D2H copy of step i-1 "
                           "overlap the kernels of step i"}
