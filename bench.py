@@ -578,7 +578,38 @@ def variants(bss, torch, W, w, H, Q, K, V, dev, peaks, flags):
                           "flagged_only_half_heads": {"ms": half_ms, "gbs": hbytes / half_ms / 1e6,
                                                       "frac_of_hbm_peak": hbytes / half_ms / 1e6 / peaks["hbm_gbs"]},
                           "timing": "20 launches back to back between one pair of CUDA events"}
+    out["p1440_step"] = p1440_step(bss, torch, W, dev, peaks)
     return out
+
+
+def p1440_step(bss, torch, W, dev, peaks):
+    """The 1440p-scale workload (21 x 90 x 160 = 302,400 tokens, 10 heads, 5
+    spatial + 5 temporal, tile-aligned masks): the same step as the headline
+    (temporal heads' permutes + attention) and the dense control at that size."""
+    w2 = W.P1440_302K
+    Q, K, V = W.qkv_device(w2, dev)
+    O = torch.empty_like(Q)
+    Qp, Kp, Vp = (torch.empty_like(Q) for _ in range(3))
+    flags = w2.head_flags()
+    fl = torch.tensor(flags, dtype=torch.uint8, device=dev)
+    p = bss.MaskParams(w2.F, w2.Hs, w2.Ws, w2.d, w2.wf, w2.ws, temporal_permuted=1, rounding=1)
+    with bss.build_tile_map(p) as tm:
+        st = {kind: tm.stats(kind) for kind in (0, 1)}
+        pairs = sum(st[f]["retained_pairs"] for f in flags)
+        exact = sum(st[f]["exact_retained_pairs"] for f in flags)
+        ms = _time(torch, lambda: bss.attention_step(Q, K, V, O, tm, fl, Qp, Kp, Vp))
+    dense_ms = _time(torch, lambda: bss.dense_attention(Q, K, V, O), reps=3, warm=2)
+    status = bss.get_device_status()
+    if status != 0:
+        raise RuntimeError(f"device status {bss.status_string(status)} in the 1440p variant")
+    flops = 4.0 * w2.d * pairs
+    dense_flops = 4.0 * w2.d * w2.H * w2.N * w2.N
+    return {"workload": w2.name, "flags_temporal": flags, "step_ms": ms, "tflops": flops / ms / 1e9,
+            "frac_of_peak": flops / ms / 1e9 / peaks["bf16_tflops"],
+            "dense_ms": dense_ms, "dense_tflops": dense_flops / dense_ms / 1e9, "speedup_vs_dense": dense_ms / ms,
+            "retained_fraction": pairs / (w2.H * w2.N * w2.N),
+            "exact_retained_fraction": exact / (w2.H * w2.N * w2.N), "tiles": st,
+            "flops": "4 d x pairs kept by the tile-aligned masks"}
 
 
 def tile_shape_sweep(bss, torch, w):

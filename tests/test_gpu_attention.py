@@ -215,6 +215,27 @@ def test_full_size_1440p_302k_rounded_sampled(bss):
 
 
 @pytest.mark.gpu
+def test_full_size_1440p_dense_control_sampled(bss):
+    # the dense control at the size the benchmark times it: 10 heads x 302,400
+    # tokens, 2,363 kv tiles per row with a ragged last one
+    wl = W.P1440_302K
+    dev = torch.device("cuda")
+    Q, K, V = W.qkv_device(wl, dev)
+    O = torch.empty_like(Q)
+    lse = torch.empty(wl.H, wl.N, device=dev)
+    bss.dense_attention(Q, K, V, O, lse=lse)
+    torch.cuda.synchronize()
+    assert bss.get_device_status() == 0
+    g = oracle.Geometry(wl.F, wl.Hs, wl.Ws, wf=wl.wf, ws=wl.ws, bkv=128)
+    rows = W.sample_rows(wl.N, 12, seed=wl.index + 1)
+    for h in (0, wl.H - 1):
+        qh, kh, vh = (x[h].cpu() for x in (Q, K, V))
+        Oref, lref = oracle.attention(W.bf16_bits(qh), W.bf16_bits(kh), W.bf16_bits(vh), oracle.DENSE, g, rows=rows)
+        compare(O[h, rows].float().cpu().numpy(), lse[h, rows].cpu().numpy(), Oref, lref,
+                f"{wl.name} dense head {h}")
+
+
+@pytest.mark.gpu
 @pytest.mark.parametrize("geom", [(8, 16, 24, 128), (3, 10, 13, 64), (5, 7, 9, 128)], ids=["small", "ragged_d64", "ragged_d128"])
 def test_all_covering_windows_equal_dense_bit_for_bit(bss, geom):
     # spatial with wf >= F-1 and the (F,H,W) temporal mask with ws >= S-1 retain
