@@ -13,7 +13,10 @@
 // is two 128-row halves that share every K/V tile brought into shared memory
 // (half the L2 -> SM bytes and TMA operations per FLOP of 128-row tiles) and
 // whose softmaxes alternate with each other's MMAs.  A one-half instance
-// (128-row tiles, 256 threads, S double-buffered in TMEM) serves 128-row maps.
+// (128-row tiles, 256 threads, S double-buffered in TMEM) serves 128-row maps,
+// and 64-key instances (BKV = 64: S_h of 64 columns, P_h over its first 32, K
+// and V stages of 64 rows, a row's tile mask in two words) serve maps with
+// 64-key tiles.  The text below describes the default 128-key tiles.
 //   warp 0       TMA producer: Q (both halves) once, then K and V tiles of the
 //                list into separate kStages-deep rings (128-byte swizzled,
 //                64-column boxes).
@@ -56,7 +59,7 @@ namespace {
 
 constexpr int kBQ = 256;        // query rows per CTA of the default shape (two halves of 128)
 constexpr int kHalf = 128;      // rows per half = MMA M
-constexpr int kBKV = 128;       // key columns per tile = MMA N of S
+constexpr int kBKV = 128;       // key columns per tile of the default shape = MMA N of S
 // threads per CTA: producer, MMA and two spare warps, plus four softmax warps
 // per 128-row half
 template <int HALVES>
