@@ -872,8 +872,8 @@ bss_status launch_d(const AttnLaunch& a, cudaStream_t stream) {
     bss_status st;
     // query rows per head: N, or the sampled rows in routing mode
     const int64_t nq_rows = a.route ? a.Nq : a.N;
-    // keys per kv tile: the map's BKV (routing, the dense control and the fused
-    // permutation use 128)
+    // keys per kv tile: the map's BKV (routing and the dense control use 128;
+    // the fused permutation needs a 128-key map)
     const int bkv = (a.route || a.dense || a.bkv == 0) ? kBKV : a.bkv;
     if (bkv != 64 && bkv != kBKV) return set_error(BSS_ERR_UNSUPPORTED, "kv tile of %d keys", bkv);
     if (a.fused == 1 && bkv != kBKV)

@@ -208,7 +208,8 @@ bss_status bss_sparse_attention_split(const void* Q, const void* K, const void* 
  *   lse         optional device float[H][N] in (F,H,W) order.
  * Results are bit-identical to bss_permute -> bss_sparse_attention ->
  * inverse bss_permute of O (and of lse) with the same flags.  H*N must be
- * below 2^31.  Errors as bss_sparse_attention. */
+ * below 2^31; the map must have 128-key tiles (BKV = 128; a 64-key map gives
+ * UNSUPPORTED).  Errors as bss_sparse_attention. */
 bss_status bss_sparse_attention_fused(const void* Q, const void* K, const void* V, void* O, float* lse,
                                       bss_tile_map map, const uint8_t* head_is_temporal, int32_t H,
                                       float softmax_scale, cudaStream_t stream);

@@ -74,3 +74,23 @@ def test_bkv64_full_size_mixed_sampled(bss):
         else:
             lrow = lrow[rows]
         compare(O[h, rows].float().cpu().numpy(), lrow.numpy(), Oref, lref, f"bkv64 mixed head {h}")
+
+
+@pytest.mark.gpu
+def test_fused_permutation_refuses_a_64_key_map(bss):
+    # the 4-row gathers of the fused permutation fill 128-key tiles only: a map
+    # with 64-key tiles is refused on the host, before any launch, and the
+    # output is left untouched
+    wl = W.SMALL
+    dev = torch.device("cuda")
+    Q, K, V = (x.to(dev) for x in W.qkv(wl))
+    O = torch.full_like(Q, 7.0)
+    fl = torch.tensor(wl.head_flags(), dtype=torch.uint8, device=dev)
+    p = bss.MaskParams(wl.F, wl.Hs, wl.Ws, wl.d, wl.wf, wl.ws, temporal_permuted=1, rounding=0)
+    with bss.build_tile_map(p, BKV=64) as tm:
+        with pytest.raises(bss.BssError) as err:
+            bss.sparse_attention_fused(Q, K, V, O, tm, fl)
+    assert err.value.status == 2  # BSS_ERR_UNSUPPORTED
+    torch.cuda.synchronize()
+    assert bss.get_device_status() == 0
+    assert bool((O == 7.0).all())
