@@ -1,0 +1,79 @@
+"""Host-side logic of bench.py, without a GPU: the clock record parsed from
+nvidia-smi lines, the staleness rule of the committed DRAM-traffic figure, the
+code-only hash it rests on, and the whole-job throughput."""
+import datetime
+
+import pytest
+
+import bench
+
+
+def _line(ts, sm, smax, power, reasons=("Not Active",) * 4):
+    return ", ".join([ts.strftime("%Y/%m/%d %H:%M:%S.%f")[:-3], str(sm), str(smax), str(power), "0x0", *reasons])
+
+
+def test_clock_record_keeps_only_samples_inside_the_timed_region():
+    t0 = datetime.datetime(2026, 1, 2, 3, 4, 5)
+    s = bench.ClockSampler(0)
+    s.proc = None
+    s.t_begin = t0 + datetime.timedelta(seconds=1)
+    s.t_end = t0 + datetime.timedelta(seconds=2)
+    s.lines = [
+        _line(t0, 2070, 2070, 150.0),  # before the region: idle clock, ignored
+        _line(t0 + datetime.timedelta(seconds=1.1), 1800, 2070, 900.0,
+              ("Not Active", "Not Active", "Not Active", "Active")),
+        _line(t0 + datetime.timedelta(seconds=1.5), 1750, 2070, 950.0),
+        _line(t0 + datetime.timedelta(seconds=1.9), 1790, 2070, 940.0),
+        _line(t0 + datetime.timedelta(seconds=2.5), 300, 2070, 90.0,
+              ("Active", "Not Active", "Not Active", "Not Active")),  # after: ignored
+        "garbage line",
+    ]
+
+    class _Done:
+        def terminate(self):
+            pass
+
+        def wait(self, timeout=None):
+            return 0
+
+    s.proc = _Done()
+    rec = s.stop()
+    assert rec["samples"] == 3
+    assert rec["sm_mhz"] == 1790.0
+    assert rec["sm_mhz_min"] == 1750.0
+    assert rec["sm_max_mhz"] == 2070.0
+    assert rec["power_w_max"] == 950.0
+    # the hw_slowdown sample lies outside the region; sw_power_cap inside it counts
+    assert rec["reasons"] == ["sw_power_cap"]
+
+
+def test_clock_record_without_nvidia_smi_says_so():
+    s = bench.ClockSampler(0)
+    rec = s.stop()
+    assert rec["sm_mhz"] is None and rec["reasons"] == ["nvidia-smi unavailable"]
+
+
+def test_code_only_drops_comments_and_layout_but_not_code():
+    a = 'int x = 1;  // one\n/* block\n comment */ int y = "a//b";\n'
+    b = 'int x = 1;\nint y = "a//b"; // other words\n'
+    assert bench._code_only(a) == bench._code_only(b)
+    assert bench._code_only("int x = 1;") != bench._code_only("int x = 2;")
+    # a comment marker inside a string literal is code
+    assert '"a//b"' in bench._code_only(a)
+
+
+def test_traffic_figure_is_dropped_when_the_kernel_changes(monkeypatch, tmp_path):
+    f = tmp_path / "traffic.txt"
+    f.write_text("# comment: ignored\nsource_sha256_16: 0123456789abcdef\n"
+                 "dram_bytes_per_full_launch: 763224960\n")
+    monkeypatch.setattr(bench, "TRAFFIC_FILE", str(f))
+    monkeypatch.setattr(bench, "source_hash", lambda: "0123456789abcdef")
+    assert bench.traffic_from_profile() == 763224960.0
+    monkeypatch.setattr(bench, "source_hash", lambda: "fedcba9876543210")
+    assert bench.traffic_from_profile() is None
+
+
+@pytest.mark.parametrize("world", [1, 2, 8])
+def test_whole_job_throughput_counts_every_rank(world):
+    # every rank does the same work in the slowest rank's time
+    assert bench.whole_job_tflops(2.0e12, world, 1000.0) == pytest.approx(2.0 * world)
