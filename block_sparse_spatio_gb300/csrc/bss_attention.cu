@@ -611,11 +611,6 @@ __global__ void __launch_bounds__(threads_for<HALVES>(), 1) attn_fwd_kernel(cons
         float m = -INFINITY;
         float l = 0.0f;
         bool ok = true;
-        // warp-uniform: every row of the warp has a finite reference max (the fast
-        // path's condition).  The max moves only on the general path, which
-        // takes the vote again; caching it saves a vote per tile between the
-        // S-ready wait and the TMEM load (measured: 0.2-0.3% faster)
-        bool all_finite = false;
         for (int j = 0; j < n; ++j) {
             const uint32_t e = entry_at<ROUTE, BKV>(args, ents, j, code, j0);
             const int cls = static_cast<int>(e >> BSS_CLASS_SHIFT);
@@ -690,7 +685,7 @@ __global__ void __launch_bounds__(threads_for<HALVES>(), 1) attn_fwd_kernel(cons
                 for (int q4 = 0; q4 < kNW; ++q4) BSS_TMEM_ST16(t_s + 16 * q4, (pk + 16 * q4));
                 return true;
             };
-            if (all_finite) {
+            if (__all_sync(0xFFFFFFFFu, m != -INFINITY)) {
                 if (cls == BSS_CLASS_FULL) {
                     const uint32_t none[4] = {0u, 0u, 0u, 0u};
                     done = single_pass(std::integral_constant<bool, false>(), none);
@@ -771,7 +766,6 @@ __global__ void __launch_bounds__(threads_for<HALVES>(), 1) attn_fwd_kernel(cons
                 const float sum = ((sm[0] + sm[1]) + (sm[2] + sm[3])) + ((sm[4] + sm[5]) + (sm[6] + sm[7]));
                 l = l * alpha + sum;
                 m = m_new;
-                all_finite = __all_sync(0xFFFFFFFFu, m != -INFINITY);
             }
             tmem_wait_st();
             tc_fence_before();
