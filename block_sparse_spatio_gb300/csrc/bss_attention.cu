@@ -644,7 +644,10 @@ __global__ void __launch_bounds__(threads_for<HALVES>(), 1) attn_fwd_kernel(cons
                 uint32_t pk[BKV / 2];
                 uint64_t s2a = 0ull, s2b = 0ull;  // packed partial sums (two chains)
                 const uint64_t c2 = f2_pack(c, c);
-                const uint64_t nm2 = f2_pack(-m, -m);
+                // routing lets a row without a reference max (m = -inf) through when
+                // none of its columns is retained: exp2(-inf - 0) = 0 for all of them
+                const float mref = (ROUTE && m == -INFINITY) ? 0.0f : m;
+                const uint64_t nm2 = f2_pack(-mref, -mref);
                 // the row's 128 scores in one wait, so that the scheduler has 64
                 // independent pairs to interleave with the exponentials (measured:
                 // 1.9% faster than a wait per 32-column chunk)
@@ -693,6 +696,21 @@ __global__ void __launch_bounds__(threads_for<HALVES>(), 1) attn_fwd_kernel(cons
                     uint32_t bits[4];
                     tile_bits<kNW>(*reinterpret_cast<uint32_t(*)[kNW]>(bits), args, code, cls, c0, rp);
                     done = single_pass(std::integral_constant<bool, true>(), bits);
+                }
+            } else if constexpr (ROUTE) {
+                // routing: a kv split often holds no retained key of some sampled rows
+                // (a spatial window of other frames), whose reference max then stays
+                // -inf for the whole split.  A masked tile takes the single pass when
+                // every such row has no retained column in it (its P is 0), instead of
+                // sending the whole warp to the two-pass path on every tile.
+                if (cls != BSS_CLASS_FULL) {
+                    uint32_t bits[4];
+                    tile_bits<kNW>(*reinterpret_cast<uint32_t(*)[kNW]>(bits), args, code, cls, c0, rp);
+                    uint32_t any = 0u;
+#pragma unroll
+                    for (int w = 0; w < kNW; ++w) any |= bits[w];
+                    if (__all_sync(0xFFFFFFFFu, m != -INFINITY || any == 0u))
+                        done = single_pass(std::integral_constant<bool, true>(), bits);
                 }
             }
             if (!done) {

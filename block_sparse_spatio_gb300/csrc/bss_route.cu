@@ -18,9 +18,12 @@
 // launch computes, for every head, the dense, spatial and temporal outputs of
 // those rows over every kv tile (the masked kinds evaluate their predicate at
 // each row's own token), with the kv range split so that the launch fills the
-// GPU; each split writes its normalised fp32 output and log-sum-exp.  A final
-// kernel merges the splits through their log-sum-exps, sums the squared
-// deviations per head and sets the flags.
+// GPU; each split writes its normalised fp32 output and log-sum-exp.  Two
+// small kernels follow: one CTA per (sampled row, head) merges the splits
+// through their log-sum-exps and sums the row's squared deviations over the
+// channels; one CTA per head adds up its rows in a fixed order and sets the
+// flag.  (A single merge kernel with one CTA per head took 0.15 ms, 40% of the
+// routing time: ten CTAs walking dependent loads.)
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -49,44 +52,72 @@ __global__ void gather_rows_kernel(const uint4* __restrict__ Q, uint4* __restric
         Qs[(static_cast<size_t>(h) * R + r) * vec + v] = __ldg(Q + (static_cast<size_t>(h) * N + t) * vec + v);
 }
 
-// One CTA per head: merge the kv splits of the dense (m = 0), spatial (1) and
-// temporal (2) outputs, O = sum_p O_p exp(LSE_p - LSE), and sum the squared
-// deviations of the masked outputs from the dense one over rows and channels.
+// One CTA per (sampled row, head), one thread per channel: merge the kv splits
+// of the dense (m = 0), spatial (1) and temporal (2) outputs of the row,
+// O = sum_p O_p exp(LSE_p - LSE) / sum_p exp(LSE_p - LSE), and write the row's
+// squared deviations of the masked outputs from the dense one, summed over
+// channels, to partial[h][r][0..1] (zero for a row outside [0, N)).
 template <int D>
-__global__ void __launch_bounds__(kDevThreads) route_deviation_kernel(
-    const float* __restrict__ o_f32, const float* __restrict__ lse_f32, const int32_t* __restrict__ rows,
-    float* __restrict__ errors, uint8_t* __restrict__ flags, int H, int R, int N, int splits) {
-    const int h = blockIdx.x;
+__global__ void __launch_bounds__(D) route_merge_kernel(const float* __restrict__ o_f32,
+                                                        const float* __restrict__ lse_f32,
+                                                        const int32_t* __restrict__ rows, float* __restrict__ partial,
+                                                        int H, int R, int N, int splits) {
+    const int r = blockIdx.x, h = blockIdx.y, ch = threadIdx.x;
+    const int t = __ldg(rows + r);
     float dev[2] = {0.0f, 0.0f};
-    for (int i = threadIdx.x; i < R * D; i += kDevThreads) {
-        const int r = i / D, ch = i - r * D;
-        const int t = __ldg(rows + r);
-        if (t < 0 || t >= N) continue;
+    if (t >= 0 && t < N) {
         float o[3];
 #pragma unroll
         for (int m = 0; m < 3; ++m) {
-            const int vh = m * H + h;
+            const int64_t vh = static_cast<int64_t>(m) * H + h;
             float mx = -INFINITY;
-            for (int p = 0; p < splits; ++p)
-                mx = fmaxf(mx, __ldg(lse_f32 + (static_cast<int64_t>(p) * 3 * H + vh) * R + r));
+            for (int p = 0; p < splits; ++p) mx = fmaxf(mx, __ldg(lse_f32 + (p * 3 * H + vh) * R + r));
             float wsum = 0.0f, acc = 0.0f;
             for (int p = 0; p < splits; ++p) {
-                const float lp = __ldg(lse_f32 + (static_cast<int64_t>(p) * 3 * H + vh) * R + r);
+                const float lp = __ldg(lse_f32 + (p * 3 * H + vh) * R + r);
                 const float w = lp == -INFINITY ? 0.0f : expf(lp - mx);
                 wsum += w;
-                acc += w * __ldg(o_f32 + ((static_cast<int64_t>(p) * 3 * H + vh) * R + r) * D + ch);
+                acc += w * __ldg(o_f32 + ((p * 3 * H + vh) * R + r) * D + ch);
             }
             o[m] = wsum > 0.0f ? acc / wsum : 0.0f;
         }
-        dev[0] += (o[1] - o[0]) * (o[1] - o[0]);
-        dev[1] += (o[2] - o[0]) * (o[2] - o[0]);
+        dev[0] = (o[1] - o[0]) * (o[1] - o[0]);
+        dev[1] = (o[2] - o[0]) * (o[2] - o[0]);
+    }
+    __shared__ float red[2][D / 32];
+    const int lane = ch & 31, wid = ch >> 5;
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        float x = dev[k];
+        for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xFFFFFFFFu, x, off);
+        if (lane == 0) red[k][wid] = x;
+    }
+    __syncthreads();
+    if (ch < 2) {
+        float x = 0.0f;
+        for (int w = 0; w < D / 32; ++w) x += red[ch][w];
+        partial[(static_cast<int64_t>(h) * R + r) * 2 + ch] = x;
+    }
+}
+
+// One CTA per head: sum the rows' squared deviations in a fixed order (so the
+// result does not depend on scheduling) and route the head to the mask whose
+// output deviates less from the dense one.
+__global__ void __launch_bounds__(kDevThreads) route_flags_kernel(const float* __restrict__ partial,
+                                                                  float* __restrict__ errors,
+                                                                  uint8_t* __restrict__ flags, int R) {
+    const int h = blockIdx.x;
+    float dev[2] = {0.0f, 0.0f};
+    for (int r = threadIdx.x; r < R; r += kDevThreads) {
+        dev[0] += __ldg(partial + (static_cast<int64_t>(h) * R + r) * 2 + 0);
+        dev[1] += __ldg(partial + (static_cast<int64_t>(h) * R + r) * 2 + 1);
     }
     __shared__ float red[2][kDevThreads / 32];
     const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
 #pragma unroll
     for (int k = 0; k < 2; ++k) {
         float x = dev[k];
-        for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xFFFFFFFFu, x, o);
+        for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xFFFFFFFFu, x, off);
         if (lane == 0) red[k][wid] = x;
     }
     __syncthreads();
@@ -135,13 +166,15 @@ extern "C" bss_status bss_route_heads(const void* Q, const void* K, const void* 
     const size_t q_bytes = static_cast<size_t>(H) * R * d * 2;
     const size_t o_bytes = static_cast<size_t>(splits) * 3 * H * R * d * 4;
     const size_t l_bytes = static_cast<size_t>(splits) * 3 * H * R * 4;
+    const size_t p_bytes = static_cast<size_t>(H) * R * 2 * 4;
     uint8_t* scratch = nullptr;
-    if ((st = cuda_check(cudaMallocAsync(reinterpret_cast<void**>(&scratch), q_bytes + o_bytes + l_bytes + 512, stream),
+    if ((st = cuda_check(cudaMallocAsync(reinterpret_cast<void**>(&scratch), q_bytes + o_bytes + l_bytes + p_bytes + 512, stream),
                          "routing scratch")) != BSS_OK)
         return st;
     void* qs = scratch;
     float* o32 = reinterpret_cast<float*>(scratch + ((q_bytes + 255) & ~size_t(255)));
     float* l32 = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(o32) + o_bytes);
+    float* partial = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(l32) + l_bytes);
     int* status = device_status_ptr();
     if (status == nullptr) st = set_error(BSS_ERR_CUDA, "cannot resolve the device status word");
     if (st == BSS_OK) {
@@ -176,12 +209,14 @@ extern "C" bss_status bss_route_heads(const void* Q, const void* K, const void* 
     }
     if (st == BSS_OK) {
         if (d == 128)
-            route_deviation_kernel<128><<<H, kDevThreads, 0, stream>>>(o32, l32, rows, errors, head_is_temporal, H, R,
-                                                                      N, splits);
+            route_merge_kernel<128><<<dim3(R, H), 128, 0, stream>>>(o32, l32, rows, partial, H, R, N, splits);
         else
-            route_deviation_kernel<64><<<H, kDevThreads, 0, stream>>>(o32, l32, rows, errors, head_is_temporal, H, R,
-                                                                     N, splits);
-        st = cuda_check(cudaGetLastError(), "routing deviation launch");
+            route_merge_kernel<64><<<dim3(R, H), 64, 0, stream>>>(o32, l32, rows, partial, H, R, N, splits);
+        st = cuda_check(cudaGetLastError(), "routing merge launch");
+    }
+    if (st == BSS_OK) {
+        route_flags_kernel<<<H, kDevThreads, 0, stream>>>(partial, errors, head_is_temporal, R);
+        st = cuda_check(cudaGetLastError(), "routing flags launch");
     }
     const bss_status fst = cuda_check(cudaFreeAsync(scratch, stream), "routing scratch free");
     return st != BSS_OK ? st : fst;
