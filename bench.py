@@ -642,9 +642,9 @@ def tile_shape_sweep(bss, torch, w):
 def e2e(bss, torch, params, tm, flags, Qd, Kd, Vd, flops, args):
     """The same step through the public API from pinned host buffers.  Every
     step copies its Q, K, V and flags host -> device and its O device -> host;
-    ``attention_step_host`` pipelines the copies over consecutive steps (two
-    workspace sets: the copies of one step overlap the kernels of another).  K consecutive steps are timed with
-    one pair of events on the compute stream: the side streams start after the
+    ``attention_step_host`` pipelines the copies over consecutive steps (three
+    workspace sets: the copies of one step overlap the kernels of another).  K
+    consecutive steps are timed with one pair of events on the compute stream: the side streams start after the
     first event and the compute stream waits for the last step's D2H copy
     before the second, so every step's copies are inside the timed region."""
     H, N, d = Qd.shape
@@ -699,7 +699,7 @@ def e2e(bss, torch, params, tm, flags, Qd, Kd, Vd, flops, args):
     return {"value": flops / (ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": ms, "steps": steps, "clocks": clocks,
             "copies_alone_ms": {"h2d_qkv": h2d_ms, "d2h_o": d2h_ms},
             "h2d_bytes_per_step": 3 * H * N * d * 2 + H, "d2h_bytes_per_step": H * N * d * 2,
-            "pipelining": "two workspace sets: the H2D copy of step i+1 and the D2H copy of step i-1 "
+            "pipelining": "three workspace sets: the H2D copy of step i+1 and the D2H copy of step i-1 "
                           "overlap the kernels of step i"}
 
 

@@ -466,8 +466,12 @@ def attention_step_host(hQ, hK, hV, hO, tile_map: TileMap, head_is_temporal, wor
     return finished
 
 
-def step_workspace(H: int, N: int, d: int, device=None, depth: int = 2):
-    """Device buffer sets and side streams reused by ``attention_step_host``."""
+def step_workspace(H: int, N: int, d: int, device=None, depth: int = 3):
+    """Device buffer sets and side streams reused by ``attention_step_host``.
+    With three sets (the default) the host-to-device copy of a call can start
+    while the device-to-host copy of the call two back is still running; with
+    two it waits for it, and measured steps were 2.4% slower (6.00 vs 5.86 ms
+    on the mixed 75.6K workload, against 5.78 ms for the kernels alone)."""
     import torch
     device = device or torch.device("cuda")
     sets = [{k: torch.empty(H, N, d, dtype=torch.bfloat16, device=device)

@@ -1,5 +1,6 @@
 """The pipelined host-buffer step gives the same O as the device step, also when
-consecutive calls overlap (two workspace sets used in turn)."""
+consecutive calls overlap (the workspace's buffer sets used in turn, each
+reused once its previous call is done)."""
 import pytest
 import torch
 
@@ -9,13 +10,14 @@ import workloads as W
 @pytest.mark.gpu
 @pytest.mark.parametrize("hpc", [1, 2, 3])
 @pytest.mark.parametrize("host_flags", [False, True])
-def test_host_steps_match_device_step(bss, hpc, host_flags):
+@pytest.mark.parametrize("depth", [2, 3])
+def test_host_steps_match_device_step(bss, hpc, host_flags, depth):
     w = W.SMALL
     H = 5
     flags = torch.tensor([0, 1, 1, 0, 1], dtype=torch.uint8)
     p = bss.MaskParams(w.F, w.Hs, w.Ws, w.d, w.wf, w.ws)
     dev = torch.device("cuda")
-    calls = 3
+    calls = 5  # more calls than buffer sets: every set is reused
     inputs = [W.qkv(w, H=H, seed=21 + c) for c in range(calls)]
     with bss.build_tile_map(p) as tm:
         fl = flags.to(dev)
@@ -28,7 +30,7 @@ def test_host_steps_match_device_step(bss, hpc, host_flags):
             expect.append(O.cpu())
         hosts = [tuple(x.pin_memory() for x in qkv) for qkv in inputs]
         outs = [torch.empty_like(inputs[0][0]).pin_memory() for _ in range(calls)]
-        wsp = bss.step_workspace(H, w.N, w.d, dev)
+        wsp = bss.step_workspace(H, w.N, w.d, dev, depth=depth)
         hfl = flags.pin_memory() if host_flags else fl
         events = [bss.attention_step_host(*hosts[c], outs[c], tm, hfl, wsp, heads_per_chunk=hpc)
                   for c in range(calls)]
