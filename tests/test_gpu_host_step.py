@@ -59,3 +59,37 @@ def test_head_local_path_on_one_rank_is_the_attention_step(bss):
         torch.cuda.synchronize()
     assert bss.get_device_status() == 0
     assert torch.equal(O.view(torch.int16), O2.view(torch.int16))
+
+
+@pytest.mark.gpu
+def test_host_steps_at_full_size_match_device_step(bss):
+    # the configuration the benchmark's end-to-end leg times: mixed 75.6K tokens x
+    # 10 heads, the default workspace (three sets) and head groups (two heads),
+    # four consecutive calls with different inputs, so that copies and kernels
+    # of neighbouring calls overlap and a set is reused
+    w = W.MIXED_75K
+    dev = torch.device("cuda")
+    flags = torch.tensor(w.head_flags(), dtype=torch.uint8)
+    p = bss.MaskParams(w.F, w.Hs, w.Ws, w.d, w.wf, w.ws)
+    calls = 4
+    with bss.build_tile_map(p) as tm:
+        fl = flags.to(dev)
+        ws = [torch.empty(w.H, w.N, w.d, dtype=torch.bfloat16, device=dev) for _ in range(3)]
+        hosts, expect = [], []
+        for c in range(calls):
+            Q, K, V = W.qkv_device(w, dev, seed=500 + c)
+            O = torch.empty_like(Q)
+            bss.attention_step(Q, K, V, O, tm, fl, *ws)
+            expect.append(O.cpu())
+            hosts.append(tuple(x.cpu().pin_memory() for x in (Q, K, V)))
+            del Q, K, V, O
+        outs = [torch.empty(w.H, w.N, w.d, dtype=torch.bfloat16).pin_memory() for _ in range(calls)]
+        wsp = bss.step_workspace(w.H, w.N, w.d, dev)
+        hfl = flags.pin_memory()
+        events = [bss.attention_step_host(*hosts[c], outs[c], tm, hfl, wsp) for c in range(calls)]
+        for e in events:
+            e.synchronize()
+        torch.cuda.synchronize()
+        assert bss.get_device_status() == 0
+        for c in range(calls):
+            assert torch.equal(outs[c].view(torch.int16), expect[c].view(torch.int16)), f"call {c}"
