@@ -199,3 +199,34 @@ int main(void) {{
     r = subprocess.run([str(tmp_path / "prog")], capture_output=True, text=True)
     assert r.returncode == 0, r.stdout + r.stderr
     assert r.stdout.split() == [str(len(names)), str(lib.bss_version()), "BSS_ERR_TIMEOUT", "BSS_ERR_INVALID_ARG", "1"]
+
+
+def test_route_heads_rejects_bad_args_before_any_launch(lib):
+    p, bad = _params(), _params(head_dim=96)
+    a, r, f, e = (ctypes.c_void_p(x) for x in (0x10000, 0x20000, 0x30000, 0x40000))
+    pp = ctypes.byref(p)
+    assert lib.bss_route_heads(a, a, a, 2, None, r, 4, f, e, None) == 1                  # no params
+    assert lib.bss_route_heads(a, a, a, 2, ctypes.byref(bad), r, 4, f, e, None) == 2     # head_dim
+    assert lib.bss_route_heads(None, a, a, 2, pp, r, 4, f, e, None) == 1                 # NULL Q
+    assert lib.bss_route_heads(a, a, a, 2, pp, None, 4, f, e, None) == 1                 # NULL rows
+    assert lib.bss_route_heads(a, a, a, 2, pp, r, 4, None, e, None) == 1                 # NULL flags
+    assert lib.bss_route_heads(a, a, a, 2, pp, r, 4, f, None, None) == 1                 # NULL errors
+    assert lib.bss_route_heads(ctypes.c_void_p(0x10008), a, a, 2, pp, r, 4, f, e, None) == 1  # Q misaligned
+    assert lib.bss_route_heads(a, a, a, 2, pp, ctypes.c_void_p(0x20002), 4, f, e, None) == 1  # rows misaligned
+    assert lib.bss_route_heads(a, a, a, 0, pp, r, 4, f, e, None) == 1                    # H
+    assert lib.bss_route_heads(a, a, a, 2, pp, r, 0, f, e, None) == 1                    # R
+    assert lib.bss_last_error_message() != b""
+
+
+def test_split_and_fused_attention_reject_bad_args_before_any_launch(lib):
+    a, m = ctypes.c_void_p(0x10000), ctypes.c_void_p(0x1234)
+    # the temporal heads' buffers: NULL or misaligned
+    assert lib.bss_sparse_attention_split(a, a, a, a, None, a, a, None, None, m, None, 2, 0.0, None) == 1
+    assert lib.bss_sparse_attention_split(a, a, a, a, a, a, ctypes.c_void_p(0x10004), None, None, m, None, 2,
+                                          0.0, None) == 1
+    assert lib.bss_sparse_attention_split(a, a, a, a, a, a, a, ctypes.c_void_p(0x10004), None, m, None, 2,
+                                          0.0, None) == 1
+    # a map handle the library did not hand out
+    assert lib.bss_sparse_attention_split(a, a, a, a, a, a, a, None, None, m, None, 2, 0.0, None) == 1
+    assert lib.bss_sparse_attention_fused(a, a, a, a, None, m, None, 2, 0.0, None) == 1
+    assert lib.bss_sparse_attention_fused(a, a, a, a, None, None, None, 2, 0.0, None) == 1
