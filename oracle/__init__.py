@@ -30,7 +30,7 @@ import subprocess
 import numpy as np
 
 SPATIAL, TEMPORAL_PERMUTED, TEMPORAL_FHW, DENSE = 0, 1, 2, 3
-FULL, BOUNDARY, PAD, SKIP = 0, 1, 2, 3
+FULL, BOUNDARY, PAD, COLUMNS, SKIP = 0, 1, 2, 3, 4
 CLASS_SHIFT = 30
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -135,7 +135,9 @@ def num_cols(kind: int, g: Geometry) -> int:
 
 def classify(kind: int, g: Geometry, BQ: int, BKV: int, rounding, qt0: int = 0, qt1: int | None = None):
     """Per-tile retained real-pair counts and classes for q-tile rows [qt0, qt1).
-    rounding: 0 exact, 1 tile-aligned, 2 exact mask in every visited tile."""
+    rounding: 0 exact, 1 tile-aligned, 2 exact mask in every visited tile.
+    Rounded permuted-temporal rows mark a kept sink tile COLUMNS (or SKIP) when
+    some (or all) of its frame-0 keys also sit in a kept band tile of the row."""
     g = g.with_bkv(BKV)
     nq = -(-g.N // BQ)
     if qt1 is None:
@@ -153,8 +155,10 @@ def tile_map(kind: int, g: Geometry, BQ: int, BKV: int, rounding: bool, qt0: int
     """CSR tile map (ascending kv index per q-tile, class in bits 30..31) plus statistics.
 
     Returns (row_ptr int32 [rows+1], entries int32, stats dict).  ``retained_pairs``
-    is the exact retained count for the exact mask and the sum of kept tiles'
-    real areas for the rounded mask."""
+    is the exact retained count for the exact mask, and for the rounded mask the
+    number of distinct physical (query, key) pairs the kept tiles cover: every
+    real row of a q tile sees the same keys, those read by the real columns of
+    its kept tiles, each physical key once."""
     gg = g.with_bkv(BKV)
     counts, cls = classify(kind, gg, BQ, BKV, rounding, qt0, qt1)
     rows, nkv = cls.shape
@@ -165,20 +169,22 @@ def tile_map(kind: int, g: Geometry, BQ: int, BKV: int, rounding: bool, qt0: int
         ents.append((js.astype(np.int64) | (cls[i, js].astype(np.int64) << CLASS_SHIFT)))
         row_ptr[i + 1] = row_ptr[i] + js.size
     entries = np.concatenate(ents) if ents else np.zeros(0, np.int64)
-    # real-area of every tile, for the rounded retained-pair count
+    # real key columns, for the rounded retained-pair count
     ncols = num_cols(kind, gg)
     k = np.arange(nkv * BKV, dtype=np.int64)
     if kind == TEMPORAL_PERMUTED:
         col_real = ((k < gg.S_pad) & (k < gg.S)) | ((k >= gg.S_pad) & (k - gg.S_pad < gg.N))
     else:
         col_real = k < gg.N
-    col_real = col_real.astype(np.int64)
-    real_cols = col_real.reshape(nkv, BKV).sum(1)
     q0 = qt0 if qt0 else 0
     real_rows = np.array([min(BQ, max(0, gg.N - (q0 + i) * BQ)) for i in range(rows)], dtype=np.int64)
     kept = cls != SKIP
     if rounding == 1:
-        retained_pairs = int((kept * np.outer(real_rows, real_cols)).sum())
+        keys = key_rows(kind, gg)
+        retained_pairs = 0
+        for i in range(rows):
+            cols = np.repeat(kept[i], BKV)[: ncols] & col_real[: ncols]
+            retained_pairs += int(real_rows[i]) * int(np.unique(keys[cols]).size)
     else:
         retained_pairs = int(counts.sum())
     stats = {
@@ -188,9 +194,22 @@ def tile_map(kind: int, g: Geometry, BQ: int, BKV: int, rounding: bool, qt0: int
         "skip": int((cls == SKIP).sum()),
         "retained_pairs": retained_pairs,
         "exact_retained_pairs": int(counts.sum()),
+        "columns": int((cls == COLUMNS).sum()),
         "ncols": ncols,
     }
     return row_ptr.astype(np.int32), entries.astype(np.uint32).view(np.int32), stats
+
+
+def key_rows(kind: int, g: Geometry) -> np.ndarray:
+    """Physical row of the head's layout tensor that each key column reads: for
+    the permuted temporal kind, sink column v is the frame-0 key at raster v
+    (permuted row v*F) and band column S_pad + p is permuted row p; otherwise
+    column k is row k.  Padding columns map to row 0 (never read)."""
+    ncols = num_cols(kind, g)
+    k = np.arange(ncols, dtype=np.int64)
+    if kind != TEMPORAL_PERMUTED:
+        return k
+    return np.where(k < g.S_pad, np.where(k < g.S, k * g.F, 0), k - g.S_pad)
 
 
 def _layout_kind(kind: int, g: Geometry):
@@ -206,7 +225,9 @@ def attention(Q: np.ndarray, K: np.ndarray, V: np.ndarray, kind: int, g: Geometr
     rows: original token indices to evaluate (default: all).
     Returns (O [len(rows)][d] float64, lse [len(rows)] float64), rows in the order given.
     For the temporal-permuted kind the head is permuted (H,W,F) first, attention
-    runs over the virtual key space, and the rows are read back in (F,H,W) order."""
+    runs over the virtual key space, and the rows are read back in (F,H,W) order.
+    A rounded mask keeps, for every row of a q tile, the physical keys read by
+    the real columns of the tile's kept tiles, each key once."""
     lib = _load()
     Q = np.ascontiguousarray(Q, dtype=np.uint16)
     K = np.ascontiguousarray(K, dtype=np.uint16)

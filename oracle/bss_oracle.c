@@ -33,7 +33,8 @@
 #define ORC_FULL 0
 #define ORC_BOUNDARY 1
 #define ORC_PAD 2
-#define ORC_SKIP 3
+#define ORC_COLUMNS 3 /* kept tile of which some real columns are dropped (see orc_classify) */
+#define ORC_SKIP 4
 
 typedef struct {
     int64_t F, S, N;       /* frames, positions per frame, tokens */
@@ -156,7 +157,14 @@ int64_t orc_num_cols(int kind, const orc_geom *g) {
  *                  "balanced" rounding: at least half the tile is retained);
  *                  kept tiles with a padding column -> PAD, else FULL.
  *        naive     (mode 2, the blog's B1 naive traversal) c == 0 -> SKIP;
- *                  every visited tile -> BOUNDARY. */
+ *                  every visited tile -> BOUNDARY.
+ * Rounded temporal (H,W,F) maps, kind 1: the rounded result is attention over
+ * the SET of physical (query, key) pairs that the kept tiles cover.  In the
+ * virtual key space the frame-0 key at raster v has two columns, sink column v
+ * and band column S_pad + v*F (permuted row v*F), so a q tile can keep both.
+ * The copy in the sink segment is then dropped: a kept sink tile loses every
+ * real column whose band twin lies in a kept tile of the same q tile, and
+ * becomes COLUMNS (some real columns left) or SKIP (none left). */
 void orc_classify(int kind, const orc_geom *g, int64_t BQ, int64_t BKV, int rounding,
                   int64_t qt0, int64_t qt1, int64_t *counts, int8_t *cls) {
     int64_t ncols = orc_num_cols(kind, g);
@@ -185,6 +193,23 @@ void orc_classify(int kind, const orc_geom *g, int64_t BQ, int64_t BKV, int roun
         counts[idx] = c;
         cls[idx] = cl;
     }
+    if (kind == 1 && rounding == 1) {
+        int64_t nsink = g->S_pad / BKV;
+        for (int64_t I = qt0; I < qt1; ++I) {
+            int8_t *row = cls + (I - qt0) * nkv;
+            for (int64_t J = 0; J < nsink; ++J) {
+                if (row[J] == ORC_SKIP) continue;
+                int64_t real = 0, dropped = 0;
+                for (int64_t v = J * BKV; v < (J + 1) * BKV && v < g->S; ++v) {
+                    int64_t twin = g->S_pad + v * g->F; /* band column of the same key */
+                    ++real;
+                    if (row[twin / BKV] != ORC_SKIP) ++dropped;
+                }
+                if (dropped == real) row[J] = ORC_SKIP;
+                else if (dropped > 0) row[J] = ORC_COLUMNS;
+            }
+        }
+    }
 }
 
 /* Exact softmax attention for a list of query rows of ONE head, in fp64.
@@ -194,7 +219,9 @@ void orc_classify(int kind, const orc_geom *g, int64_t BQ, int64_t BKV, int roun
  *   Q, K, V : [N][d] bf16 in the head's layout (already permuted for kind 1)
  *   rows    : layout query indices
  *   kept    : NULL for the exact mask, else per-tile keep flags for rounded
- *             masks, indexed [q_tile][kv_tile] over the whole map
+ *             masks, indexed [q_tile][kv_tile] over the whole map; the row
+ *             then keeps every physical key that some real column of a kept
+ *             tile reads, each key once (a set of pairs, not a multiset)
  *   O       : [nrows][d] fp64, lse : [nrows] fp64 (natural log)
  * A row with no retained key gets O = 0 and lse = -inf. */
 void orc_attention(const uint16_t *Q, const uint16_t *K, const uint16_t *V, int64_t d,
@@ -208,6 +235,7 @@ void orc_attention(const uint16_t *Q, const uint16_t *K, const uint16_t *V, int6
         double *s = (double *)malloc(sizeof(double) * (size_t)ncols);
         int64_t *key = (int64_t *)malloc(sizeof(int64_t) * (size_t)ncols);
         double *q = (double *)malloc(sizeof(double) * (size_t)d);
+        char *taken = (char *)calloc((size_t)(g->N > 0 ? g->N : 1), 1); /* physical key rows seen */
 #pragma omp for schedule(dynamic, 1)
         for (int64_t r = 0; r < nrows; ++r) {
             int64_t qi = rows[r];
@@ -222,12 +250,15 @@ void orc_attention(const uint16_t *Q, const uint16_t *K, const uint16_t *V, int6
                 }
                 if (!keep) continue;
                 int64_t kr = orc_key_row(kind, g, k);
+                if (taken[kr]) continue; /* the same key through another column */
+                taken[kr] = 1;
                 double acc = 0.0;
                 for (int64_t c = 0; c < d; ++c) acc += q[c] * bf16_to_double(K[kr * d + c]);
                 s[n] = acc * scale;
                 key[n] = kr;
                 ++n;
             }
+            for (int64_t j = 0; j < n; ++j) taken[key[j]] = 0;
             double *o = O + r * d;
             for (int64_t c = 0; c < d; ++c) o[c] = 0.0;
             if (n == 0) {
@@ -249,5 +280,6 @@ void orc_attention(const uint16_t *Q, const uint16_t *K, const uint16_t *V, int6
         free(s);
         free(key);
         free(q);
+        free(taken);
     }
 }

@@ -84,7 +84,11 @@ def layout_mask(kind, F, Hs, Ws, wf, ws, BKV):
     return M, col_tok, col_real, pt
 
 
-def tile_classes(M, col_real, BQ, BKV, rounding):
+def tile_classes(M, col_real, BQ, BKV, rounding, col_tok=None):
+    """Tile counts and classes by numpy reshapes of the layout matrix.  With
+    ``col_tok`` (rounded masks), a kept sink-segment column whose physical token
+    is also read by another kept column of the same q tile is dropped: a kept
+    tile left with none of its real columns is SKIP, with some COLUMNS."""
     N, C = M.shape
     nq, nkv = -(-N // BQ), -(-C // BKV)
     Mp = np.zeros((nq * BQ, nkv * BKV), bool)
@@ -102,11 +106,53 @@ def tile_classes(M, col_real, BQ, BKV, rounding):
         kept = (area > 0) & (2 * counts >= area)
         cls[kept] = oracle.FULL
         cls[kept & (real_cols[None, :] < BKV)] = oracle.PAD
+        if col_tok is not None:
+            # how many kept real columns of q tile i read each token
+            kc = np.repeat(kept, BKV, axis=1)[:, :C] & col_real[None, :]
+            mult = token_counts(kc, col_tok, col_real, N)
+            S_pad = C - N
+            for i in range(nq):
+                for j in range(S_pad // BKV):
+                    if not kept[i, j]:
+                        continue
+                    cols = np.arange(j * BKV, (j + 1) * BKV)
+                    cols = cols[col_real[cols]]
+                    dropped = mult[i, col_tok[cols]] >= 2
+                    if dropped.all():
+                        cls[i, j] = oracle.SKIP
+                    elif dropped.any():
+                        cls[i, j] = oracle.COLUMNS
     else:
         cls[counts > 0] = oracle.BOUNDARY
         full = (counts == real_rows[:, None] * BKV) & (real_cols[None, :] == BKV) & (counts > 0)
         cls[full] = oracle.FULL
     return counts, cls
+
+
+def token_counts(keep, col_tok, col_real, N):
+    """R x N counts: how many real columns c with keep[:, c] read each token."""
+    out = np.zeros((keep.shape[0], N), np.int64)
+    for c in np.nonzero(col_real)[0]:
+        out[:, col_tok[c]] += keep[:, c]
+    return out
+
+
+def rounded_phys_mask(kind, F, Hs, Ws, wf, ws, BQ, BKV):
+    """Rounded mask as an explicit matrix over PHYSICAL tokens: rows are layout
+    queries, columns the N tokens in (F,H,W) order; a pair is retained iff some
+    real column of a kept tile of the query's q tile reads that token (a set:
+    a token read through two columns is one pair)."""
+    M, col_tok, col_real, pt = layout_mask(kind, F, Hs, Ws, wf, ws, BKV)
+    N = M.shape[0]
+    counts, _ = tile_classes(M, col_real, BQ, BKV, 0)
+    real_rows = np.minimum(BQ, N - np.arange(counts.shape[0]) * BQ)
+    cr = np.zeros(counts.shape[1] * BKV, bool)
+    cr[: col_real.size] = col_real
+    area = np.outer(real_rows, cr.reshape(-1, BKV).sum(1))
+    kept = (area > 0) & (2 * counts >= area)
+    keep = np.repeat(np.repeat(kept, BQ, 0), BKV, 1)[:N, : M.shape[1]] & col_real[None, :]
+    P = token_counts(keep, col_tok, col_real, N) > 0
+    return P, pt
 
 
 def torch_attention(Qf, Kf, Vf, mask, scale):
@@ -203,7 +249,7 @@ def test_temporal_virtual_space_counts_each_key_once(g):
 def test_classify_matches_numpy_tiling(g, kind, rounding):
     name, F, Hs, Ws, wf, ws, BQ, BKV = g
     M, col_tok, col_real, pt = layout_mask(kind, F, Hs, Ws, wf, ws, BKV)
-    counts_np, cls_np = tile_classes(M, col_real, BQ, BKV, rounding)
+    counts_np, cls_np = tile_classes(M, col_real, BQ, BKV, rounding, col_tok if rounding == 1 else None)
     counts, cls = oracle.classify(kind, geom(F, Hs, Ws, wf, ws, BKV), BQ, BKV, rounding)
     assert np.array_equal(counts, counts_np)
     assert np.array_equal(cls, cls_np)
@@ -310,13 +356,14 @@ def _oracle_vs_torch(name, F, Hs, Ws, wf, ws, BQ, BKV, kind, rounding, d=64, see
     gg = geom(F, Hs, Ws, wf, ws, BKV)
     O, lse = oracle.attention(bits(q), bits(k), bits(v), kind, gg, rounding=rounding, BQ=BQ, BKV=BKV)
     M, col_tok, col_real, pt = layout_mask(kind, F, Hs, Ws, wf, ws, BKV)
-    if rounding:
-        _, cls = tile_classes(M, col_real, BQ, BKV, 1)
-        keep = np.repeat(np.repeat(cls != oracle.SKIP, BQ, 0), BKV, 1)[: M.shape[0], : M.shape[1]]
-        M = keep & col_real[None, :]
     Qf, Kf, Vf = q.double(), k.double(), v.double()
-    # rows in layout order, keys through the column -> token map
-    Ol, lsel = torch_attention(Qf[pt], Kf[col_tok], Vf[col_tok], torch.from_numpy(M), 1.0 / np.sqrt(d))
+    if rounding:
+        # rows in layout order, keys the physical tokens of the explicit rounded matrix
+        P, pt = rounded_phys_mask(kind, F, Hs, Ws, wf, ws, BQ, BKV)
+        Ol, lsel = torch_attention(Qf[pt], Kf, Vf, torch.from_numpy(P), 1.0 / np.sqrt(d))
+    else:
+        # rows in layout order, keys through the column -> token map
+        Ol, lsel = torch_attention(Qf[pt], Kf[col_tok], Vf[col_tok], torch.from_numpy(M), 1.0 / np.sqrt(d))
     Oref = torch.empty_like(Ol)
     lref = torch.empty_like(lsel)
     Oref[pt] = Ol
@@ -361,6 +408,54 @@ def test_rounded_mask_rows_left_empty_give_zero_and_minus_infinity(BQ):
         Ol, ll = torch_attention(Qf[live], Kf, Vf, torch.from_numpy(M[live]), 1.0 / np.sqrt(d))
         np.testing.assert_allclose(O[live], Ol.numpy(), rtol=0, atol=1e-12)
         np.testing.assert_allclose(lse[live], ll.numpy(), rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("g", GEOMS, ids=[g[0] for g in GEOMS])
+@pytest.mark.parametrize("kind", KINDS)
+def test_rounded_mask_is_a_set_of_physical_pairs(g, kind):
+    # Rounded masks (section "Align the sparse mask with final execution") keep
+    # whole tiles; the result is attention over the SET of physical pairs they
+    # cover.  Q = 0 gives every retained key weight 1, so exp(LSE) is the number
+    # of distinct keys of the row, and the map's retained-pair count is the
+    # explicit physical matrix's sum.
+    name, F, Hs, Ws, wf, ws, BQ, BKV = g
+    N = F * Hs * Ws
+    _, k, v = rand_head(N, 64, 3)
+    q = torch.zeros_like(k)
+    gg = geom(F, Hs, Ws, wf, ws, BKV)
+    O, lse = oracle.attention(bits(q), bits(k), bits(v), kind, gg, rounding=True, BQ=BQ, BKV=BKV)
+    P, pt = rounded_phys_mask(kind, F, Hs, Ws, wf, ws, BQ, BKV)
+    Pt = np.zeros_like(P)
+    Pt[pt] = P                                   # rows back in (F,H,W) order
+    cnt = Pt.sum(1)
+    live = cnt > 0
+    np.testing.assert_array_equal(np.rint(np.exp(lse[live])).astype(np.int64), cnt[live])
+    assert np.all(np.isneginf(lse[~live]))
+    mean = (Pt[live].astype(np.float64) @ v.double().numpy()) / cnt[live][:, None]
+    np.testing.assert_allclose(O[live], mean, rtol=0, atol=1e-12)
+    _, _, st = oracle.tile_map(kind, gg, BQ, BKV, 1)
+    assert st["retained_pairs"] == int(P.sum())
+
+
+def test_rounded_temporal_small_drops_sink_twins():
+    # Small's rounded temporal map keeps frame-0 keys both as sink columns and
+    # inside kept band tiles; those sink tiles must lose the twin columns (else
+    # a key carries double weight), and the kept tiles still cover the same set.
+    w = W.SMALL
+    gg = geom(w.F, w.Hs, w.Ws, w.wf, w.ws, 128)
+    _, _, st = oracle.tile_map(TEMPORAL_PERMUTED, gg, 128, 128, 1)
+    assert st["columns"] > 0
+    M, col_tok, col_real, pt = layout_mask(TEMPORAL_PERMUTED, w.F, w.Hs, w.Ws, w.wf, w.ws, 128)
+    counts, _ = tile_classes(M, col_real, 128, 128, 0)
+    real_rows = np.minimum(128, w.N - np.arange(counts.shape[0]) * 128)
+    cr = np.zeros(counts.shape[1] * 128, bool)
+    cr[: col_real.size] = col_real
+    area = np.outer(real_rows, cr.reshape(-1, 128).sum(1))
+    kept = (area > 0) & (2 * counts >= area)
+    keep = np.repeat(np.repeat(kept, 128, 0), 128, 1)[: w.N, : M.shape[1]] & col_real[None, :]
+    multiset = int(keep.sum())
+    P, _ = rounded_phys_mask(TEMPORAL_PERMUTED, w.F, w.Hs, w.Ws, w.wf, w.ws, 128, 128)
+    assert st["retained_pairs"] == int(P.sum()) < multiset
 
 
 def test_attention_d128_small_rows_subset():
