@@ -22,13 +22,13 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(HERE, "libbss.so")
 
 KIND_SPATIAL, KIND_TEMPORAL = 0, 1
-CLASS_FULL, CLASS_BOUNDARY, CLASS_PAD = 0, 1, 2
+CLASS_FULL, CLASS_BOUNDARY, CLASS_PAD, CLASS_COLUMNS = 0, 1, 2, 3
 ATTN_BQ, ATTN_BKV = 256, 128   # default tile shape of bss_sparse_attention's map
 ATTN_BQ_SUPPORTED = (128, 256)  # query rows per tile it runs (one or two 128-row MMA halves)
 ATTN_BKV_SUPPORTED = (64, 128)  # keys per tile it runs (routing, dense control and fused permutation: 128)
 CLASS_SHIFT = 30
 TILE_INDEX_MASK = (1 << 30) - 1
-STAT_NAMES = ("full", "boundary", "pad", "skip", "retained_pairs", "exact_retained_pairs")
+STAT_NAMES = ("full", "boundary", "pad", "skip", "retained_pairs", "exact_retained_pairs", "columns")
 STATUS_NAMES = {0: "BSS_OK", 1: "BSS_ERR_INVALID_ARG", 2: "BSS_ERR_UNSUPPORTED", 3: "BSS_ERR_CUDA",
                 4: "BSS_ERR_TIMEOUT", 5: "BSS_ERR_OOM"}
 
@@ -231,7 +231,7 @@ def _raw_handle(m):
 
 
 def tile_map_stats(m, kind: int) -> dict:
-    out = (ctypes.c_int64 * 6)()
+    out = (ctypes.c_int64 * len(STAT_NAMES))()
     _check(load().bss_tile_map_stats(_raw_handle(m), kind, out))
     return dict(zip(STAT_NAMES, [int(x) for x in out]))
 
@@ -368,7 +368,7 @@ def noalloc_map_dims(params: MaskParams, kind: int, BQ: int = ATTN_BQ, BKV: int 
 def build_tile_map_csr_noalloc(params: MaskParams, kind: int, row_ptr, entries, stats, BQ: int = ATTN_BQ,
                                BKV: int = ATTN_BKV, stream=None):
     """Allocation-free CSR build of one kind into caller-owned device buffers
-    (int32 row_ptr[nq + 1], int32 entries[>= nq * nkv], int64 stats[6])."""
+    (int32 row_ptr[nq + 1], int32 entries[>= nq * nkv], int64 stats[len(STAT_NAMES)])."""
     import torch
     _dev_tensor(row_ptr, "row_ptr", torch.int32)
     _dev_tensor(entries, "entries", torch.int32)

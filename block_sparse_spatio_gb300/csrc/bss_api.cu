@@ -60,7 +60,9 @@ void free_kind(bss::KindMap& k) {
     if (k.d_row_ptr) cudaFree(k.d_row_ptr);
     if (k.d_entries) cudaFree(k.d_entries);
     if (k.d_order) cudaFree(k.d_order);
+    if (k.d_colmask) cudaFree(k.d_colmask);
     k.d_row_ptr = k.d_entries = k.d_order = nullptr;
+    k.d_colmask = nullptr;
 }
 
 }  // namespace
@@ -74,6 +76,8 @@ bss_status set_error(bss_status st, const char* fmt, ...) {
     va_end(ap);
     return st;
 }
+
+void clear_error() { t_last_error[0] = '\0'; }
 
 bss_status cuda_check(cudaError_t e, const char* what) {
     if (e == cudaSuccess) return BSS_OK;
@@ -342,6 +346,8 @@ bss_status sparse_attention_impl(const void* Q, const void* K, const void* V, vo
         a.row_ptr[k] = map->kind[k].d_row_ptr;
         a.entries[k] = map->kind[k].d_entries;
         a.order[k] = map->kind[k].d_order;
+        a.colmask[k] = map->kind[k].d_colmask;
+        if (map->kind[k].d_colmask != nullptr) a.nsink = map->kind[k].nsink;
     }
     a.softmax_scale = softmax_scale;
     a.fused = fused;

@@ -7,7 +7,10 @@
 // full tiles with no mask at all and evaluates the coordinate predicate only on
 // boundary tiles (section "Avoid intra-tile masking when there is nothing to
 // mask"), or only the padding predicate on padding tiles of a tile-aligned
-// mask (section "Align the sparse mask with final execution").
+// mask (section "Align the sparse mask with final execution"); a tile-aligned
+// map of permuted temporal heads also masks, in some sink-segment tiles, the
+// frame-0 keys that a kept band tile of the same q tile already holds (a
+// per-column bitmask from the map, the same for every row).
 //
 // GB300 design.  One CTA per (head, 256-row q tile), 384 threads.  The q tile
 // is two 128-row halves that share every K/V tile brought into shared memory
@@ -104,10 +107,12 @@ struct AttnArgs {
     const int32_t* row_ptr[2];
     const int32_t* entries[2];
     const int32_t* order[2];
+    const uint32_t* colmask[2];  // column bitmasks of BSS_CLASS_COLUMNS tiles, [nq][nsink][BKV/32]
     const uint8_t* flags;
     float* lse;
     int* status;
     int32_t code[2];
+    int32_t nsink;
     int32_t H, N, nq, F, S, S_pad, wf, ws, dense, nkv_dense;
     int32_t fused;  // 0: none, 1: permutation in loads and stores, 2: in the O stores only
     int32_t route, Nq, splits;  // routing mode: query rows per head, kv splits
@@ -194,10 +199,18 @@ __device__ __forceinline__ RowPred row_pred(const AttnArgs& a, int code, int q) 
 // Retained-column bitmask of one row over the tile starting at column c0.
 //   boundary tile: the coordinate predicate (all masks are unions of <= 3
 //   intervals except the striped (F,H,W) temporal mask, one interval per frame);
-//   padding tile: the real-column predicate only.
+//   padding tile: the real-column predicate only;
+//   column-set tile: the map's bitmask of the tile (cmask: this q tile's
+//   sink-segment tiles, NW words each).
 template <int NW>
 __device__ __forceinline__ void tile_bits(uint32_t (&bits)[NW], const AttnArgs& a, int code, int cls, int c0,
-                                          const RowPred& rp) {
+                                          const RowPred& rp, const uint32_t* cmask) {
+    if (cls == BSS_CLASS_COLUMNS) {
+        const uint32_t* m = cmask + (c0 / (NW * 32)) * NW;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) bits[w] = __ldg(m + w);
+        return;
+    }
 #pragma unroll
     for (int w = 0; w < NW; ++w) bits[w] = 0u;
     if (cls == BSS_CLASS_PAD) {
@@ -285,6 +298,7 @@ __global__ void __launch_bounds__(threads_for<HALVES>(), 1) attn_fwd_kernel(cons
     bool tbuf = false;  // head with flag 1: its tensors come from the temporal-head buffers
     int qt, n;
     const int32_t* ents = nullptr;
+    const uint32_t* cmask = nullptr;  // this q tile's column bitmasks (tile-aligned permuted temporal maps)
     if constexpr (ROUTE) {
         vh = item / (args.nq * args.splits);
         const int rem = item - vh * args.nq * args.splits;
@@ -311,6 +325,8 @@ __global__ void __launch_bounds__(threads_for<HALVES>(), 1) attn_fwd_kernel(cons
             const int rb = __ldg(args.row_ptr[kind] + qt);
             n = __ldg(args.row_ptr[kind] + qt + 1) - rb;
             ents = args.entries[kind] + rb;
+            if (args.colmask[kind] != nullptr)
+                cmask = args.colmask[kind] + static_cast<int64_t>(qt) * args.nsink * kNW;
         }
     }
 
@@ -694,7 +710,7 @@ __global__ void __launch_bounds__(threads_for<HALVES>(), 1) attn_fwd_kernel(cons
                     done = single_pass(std::integral_constant<bool, false>(), none);
                 } else {
                     uint32_t bits[4];
-                    tile_bits<kNW>(*reinterpret_cast<uint32_t(*)[kNW]>(bits), args, code, cls, c0, rp);
+                    tile_bits<kNW>(*reinterpret_cast<uint32_t(*)[kNW]>(bits), args, code, cls, c0, rp, cmask);
                     done = single_pass(std::integral_constant<bool, true>(), bits);
                 }
             } else if constexpr (ROUTE) {
@@ -705,7 +721,7 @@ __global__ void __launch_bounds__(threads_for<HALVES>(), 1) attn_fwd_kernel(cons
                 // sending the whole warp to the two-pass path on every tile.
                 if (cls != BSS_CLASS_FULL) {
                     uint32_t bits[4];
-                    tile_bits<kNW>(*reinterpret_cast<uint32_t(*)[kNW]>(bits), args, code, cls, c0, rp);
+                    tile_bits<kNW>(*reinterpret_cast<uint32_t(*)[kNW]>(bits), args, code, cls, c0, rp, cmask);
                     uint32_t any = 0u;
 #pragma unroll
                     for (int w = 0; w < kNW; ++w) any |= bits[w];
@@ -719,7 +735,7 @@ __global__ void __launch_bounds__(threads_for<HALVES>(), 1) attn_fwd_kernel(cons
                 // pass 2 exponentiates and writes P chunk by chunk.
                 uint32_t bits[4] = {0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu};
                 if (cls != BSS_CLASS_FULL)
-                    tile_bits<kNW>(*reinterpret_cast<uint32_t(*)[kNW]>(bits), args, code, cls, c0, rp);
+                    tile_bits<kNW>(*reinterpret_cast<uint32_t(*)[kNW]>(bits), args, code, cls, c0, rp, cmask);
                 float mx[8];
 #pragma unroll
                 for (int t = 0; t < 8; ++t) mx[t] = -INFINITY;
@@ -935,8 +951,10 @@ bss_status launch_d(const AttnLaunch& a, cudaStream_t stream) {
         args.row_ptr[k] = a.row_ptr[k];
         args.entries[k] = a.entries[k];
         args.order[k] = a.order[k];
+        args.colmask[k] = a.colmask[k];
         args.code[k] = a.code[k];
     }
+    args.nsink = a.nsink;
     args.flags = a.flags;
     args.lse = a.lse;
     args.status = device_status_ptr();

@@ -28,8 +28,16 @@ struct KindMap {
     int32_t* d_row_ptr = nullptr;  // [nq + 1]
     int32_t* d_entries = nullptr;  // [nnz]
     int32_t* d_order = nullptr;    // [nq] q tiles, most entries first
-    int64_t stats[BSS_STAT_COUNT] = {0, 0, 0, 0, 0, 0};
+    // rounded maps of permuted temporal heads: retained real columns of every
+    // (q tile, sink tile), tile_colmask_words(BKV) words each, [nq][nsink]
+    // (BSS_CLASS_COLUMNS entries read theirs); NULL otherwise
+    uint32_t* d_colmask = nullptr;
+    int32_t nsink = 0;  // sink-segment tiles (S_pad / BKV) of such a map
+    int64_t stats[BSS_STAT_COUNT] = {0, 0, 0, 0, 0, 0, 0};
 };
+
+// 32-column words of a kv tile's column bitmask
+constexpr int tile_colmask_words(int BKV) { return (BKV + 31) / 32; }
 
 struct Geom {
     int32_t F, S, N, wf, ws, S_pad;
@@ -46,6 +54,12 @@ bss_status launch_tile_classify(const Geom& geo, int32_t code, int32_t rounding,
                                 cudaStream_t stream);
 bss_status launch_tile_compact(int32_t nq, int32_t nkv, const uint8_t* cls, const int32_t* row_ptr, int32_t* entries,
                                cudaStream_t stream);
+// rounded maps of permuted temporal heads: drop sink columns whose band twin is
+// kept (no-op for other maps); colmask may be NULL
+bool tile_map_needs_dedup(int32_t code, int32_t rounding);
+bss_status launch_tile_dedup(const Geom& geo, int32_t code, int32_t rounding, int32_t BQ, int32_t BKV, int32_t nq,
+                             int32_t nkv, uint8_t* cls, int32_t* row_cnt, unsigned long long* stats, uint32_t* colmask,
+                             cudaStream_t stream);
 
 // permutation kernel launch (bss_permute.cu)
 // only_flagged: heads whose flag is 0 are not touched (else they are copied)
@@ -65,6 +79,8 @@ struct AttnLaunch {
     const int32_t* row_ptr[2];
     const int32_t* entries[2];
     const int32_t* order[2];
+    const uint32_t* colmask[2];  // per kind: column bitmasks of BSS_CLASS_COLUMNS tiles (or NULL)
+    int32_t nsink;               // sink-segment tiles per q tile in colmask
     float softmax_scale;
     // 1: Q, K, V, O and lse are in (F,H,W) token order for every head; the
     // temporal kind's (H,W,F) permutation is applied by the kernel's loads and
@@ -93,6 +109,7 @@ bool attention_supports_block_kv(int bkv);  // 64 or 128 for a map-driven call
 
 // helpers (bss_api.cu)
 bss_status set_error(bss_status st, const char* fmt, ...);
+void clear_error();  // empties the calling thread's last-error message
 bss_status cuda_check(cudaError_t e, const char* what);
 int* device_status_ptr();  // per-device status word (device address)
 bss_status encode_tmap_3d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint64_t heads,

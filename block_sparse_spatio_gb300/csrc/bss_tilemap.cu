@@ -13,6 +13,14 @@
 // retained set (at most three intervals, or one per frame for the striped
 // (F,H,W) temporal predicate) intersected with the tile's columns, so the cost
 // per tile is O(BQ), independent of BKV.
+//
+// Tile-aligned maps of permuted temporal heads are rounded in the virtual key
+// space, where the frame-0 key at raster v has two columns: sink column v and
+// band column S_pad + v*F.  The rounded result is attention over the set of
+// physical pairs that the kept tiles cover, so a kept sink tile then drops the
+// columns whose band twin lies in a kept tile of the same q tile (class
+// COLUMNS, with a per-column bitmask that is the same for every row; SKIP when
+// no real column is left).
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -26,7 +34,15 @@
 namespace bss {
 namespace {
 
-enum : uint8_t { CLS_FULL = 0, CLS_BOUNDARY = 1, CLS_PAD = 2, CLS_SKIP = 3 };
+enum : uint8_t { CLS_FULL = 0, CLS_BOUNDARY = 1, CLS_PAD = 2, CLS_COLUMNS = 3, CLS_SKIP = 4 };
+
+// statistics slot counting the tiles of a class
+__host__ __device__ constexpr int stat_of_class(uint8_t k) {
+    return k == CLS_SKIP ? BSS_STAT_SKIP : (k == CLS_COLUMNS ? BSS_STAT_COLUMNS : k);
+}
+static_assert(CLS_FULL == BSS_CLASS_FULL && CLS_BOUNDARY == BSS_CLASS_BOUNDARY && CLS_PAD == BSS_CLASS_PAD &&
+                  CLS_COLUMNS == BSS_CLASS_COLUMNS,
+              "tile classes are the entry class codes");
 
 struct TmArgs {
     int64_t F, S, N, wf, ws, S_pad;
@@ -83,7 +99,7 @@ __global__ void classify_kernel(TmArgs g, uint8_t* __restrict__ cls, int32_t* __
     if (threadIdx.x < BSS_STAT_COUNT) s_stats[threadIdx.x] = 0ull;
     __syncthreads();
     const int64_t ntiles = static_cast<int64_t>(g.nq) * g.nkv;
-    unsigned long long loc[BSS_STAT_COUNT] = {0, 0, 0, 0, 0, 0};
+    unsigned long long loc[BSS_STAT_COUNT] = {0, 0, 0, 0, 0, 0, 0};
     for (int64_t t = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; t < ntiles;
          t += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         const int64_t I = t / g.nkv, J = t - I * g.nkv;
@@ -109,7 +125,7 @@ __global__ void classify_kernel(TmArgs g, uint8_t* __restrict__ cls, int32_t* __
             retained = kept ? area : 0;
         }
         cls[t] = k;
-        loc[k] += 1;
+        loc[stat_of_class(k)] += 1;
         loc[BSS_STAT_RETAINED] += static_cast<unsigned long long>(retained);
         loc[BSS_STAT_EXACT_RETAINED] += static_cast<unsigned long long>(c);
         if (k != CLS_SKIP) atomicAdd(row_cnt + I, 1);
@@ -122,6 +138,55 @@ __global__ void classify_kernel(TmArgs g, uint8_t* __restrict__ cls, int32_t* __
     }
     __syncthreads();
     if (threadIdx.x < BSS_STAT_COUNT && s_stats[threadIdx.x]) atomicAdd(stats + threadIdx.x, s_stats[threadIdx.x]);
+}
+
+// Rounded maps of permuted temporal heads: one thread per (q tile I, sink tile
+// J).  A kept sink tile drops every real column v whose band twin (column
+// S_pad + v*F) lies in a kept tile of row I; statistics and row counts follow.
+// Only sink tiles are written and only band tiles are read, so the threads of a
+// row do not race.  colmask (may be NULL) receives the retained real columns of
+// every (I, J), nwords words of 32 columns each, row-major over [nq][nsink].
+__global__ void dedup_sink_kernel(TmArgs g, uint8_t* __restrict__ cls, int32_t* __restrict__ row_cnt,
+                                  unsigned long long* __restrict__ stats, uint32_t* __restrict__ colmask,
+                                  int nwords) {
+    const int64_t nsink = g.S_pad / g.BKV;
+    const int64_t t = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (t >= static_cast<int64_t>(g.nq) * nsink) return;
+    const int64_t I = t / nsink, J = t - I * nsink;
+    uint8_t* row = cls + I * g.nkv;
+    const uint8_t k = row[J];
+    uint32_t* mask = colmask != nullptr ? colmask + t * nwords : nullptr;
+    int64_t real = 0, dropped = 0;
+    for (int w = 0; w < nwords; ++w) {
+        uint32_t bits = 0u;
+        if (k != CLS_SKIP) {
+            for (int b = 0; b < 32; ++b) {
+                const int64_t col = static_cast<int64_t>(w) * 32 + b;
+                const int64_t v = J * g.BKV + col;
+                if (col >= g.BKV || v >= g.S) break;
+                ++real;
+                const int64_t twin = g.S_pad + v * g.F;
+                if (row[twin / g.BKV] != CLS_SKIP)
+                    ++dropped;
+                else
+                    bits |= 1u << b;
+            }
+        }
+        if (mask != nullptr) mask[w] = bits;
+    }
+    if (dropped == 0) return;
+    const int64_t rr = (I + 1) * g.BQ <= g.N ? g.BQ : g.N - I * g.BQ;
+    // unsigned wrap-around: adding 2^64 - x subtracts x
+    atomicAdd(stats + BSS_STAT_RETAINED, static_cast<unsigned long long>(-(rr * dropped)));
+    atomicAdd(stats + stat_of_class(k), ~0ull);
+    if (dropped == real) {
+        row[J] = CLS_SKIP;
+        atomicAdd(stats + BSS_STAT_SKIP, 1ull);
+        atomicAdd(row_cnt + I, -1);
+    } else {
+        row[J] = CLS_COLUMNS;
+        atomicAdd(stats + BSS_STAT_COLUMNS, 1ull);
+    }
 }
 
 // One warp per q-tile row: write its non-skipped tiles in ascending kv order.
@@ -176,6 +241,32 @@ bss_status launch_tile_classify(const Geom& geo, int32_t code, int32_t rounding,
     if (blocks < 1) blocks = 1;
     classify_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(g, cls, row_cnt, stats);
     return cuda_check(cudaGetLastError(), "classify launch");
+}
+
+bool tile_map_needs_dedup(int32_t code, int32_t rounding) { return code == MASK_TEMPORAL_VIRT && rounding == 1; }
+
+bss_status launch_tile_dedup(const Geom& geo, int32_t code, int32_t rounding, int32_t BQ, int32_t BKV, int32_t nq,
+                             int32_t nkv, uint8_t* cls, int32_t* row_cnt, unsigned long long* stats, uint32_t* colmask,
+                             cudaStream_t stream) {
+    if (!tile_map_needs_dedup(code, rounding)) return BSS_OK;
+    TmArgs g;
+    memset(&g, 0, sizeof(g));
+    g.F = geo.F;
+    g.S = geo.S;
+    g.N = geo.N;
+    g.S_pad = geo.S_pad;
+    g.code = code;
+    g.rounding = rounding;
+    g.BQ = BQ;
+    g.BKV = BKV;
+    g.nq = nq;
+    g.nkv = nkv;
+    const int64_t n = static_cast<int64_t>(nq) * (geo.S_pad / BKV);
+    if (n <= 0) return BSS_OK;
+    const int threads = 128;
+    dedup_sink_kernel<<<static_cast<unsigned>((n + threads - 1) / threads), threads, 0, stream>>>(
+        g, cls, row_cnt, stats, colmask, tile_colmask_words(BKV));
+    return cuda_check(cudaGetLastError(), "sink dedup launch");
 }
 
 bss_status launch_tile_compact(int32_t nq, int32_t nkv, const uint8_t* cls, const int32_t* row_ptr, int32_t* entries,
@@ -239,6 +330,21 @@ bss_status build_kind_map(const Geom& geo, int32_t code, int32_t rounding, int32
         if (blocks < 1) blocks = 1;
         classify_kernel<<<static_cast<unsigned>(blocks), threads, 0, stream>>>(g, d_cls, d_cnt, d_stats);
         if ((st = cuda_check(cudaGetLastError(), "classify launch")) != BSS_OK) goto done;
+    }
+    if (tile_map_needs_dedup(code, rounding)) {
+        // the kernel reads the column bitmasks of maps it can run (64- or 128-key tiles)
+        km->nsink = geo.S_pad / BKV;
+        if (BKV == 64 || BKV == 128) {
+            const size_t bytes = sizeof(uint32_t) * static_cast<size_t>(nq) * km->nsink * tile_colmask_words(BKV);
+            if (cudaMalloc(&km->d_colmask, bytes > 0 ? bytes : 4) != cudaSuccess) {
+                (void)cudaGetLastError();
+                st = set_error(BSS_ERR_OOM, "tile map column-mask allocation failed");
+                goto done;
+            }
+        }
+        if ((st = launch_tile_dedup(geo, code, rounding, BQ, BKV, nq, g.nkv, d_cls, d_cnt, d_stats, km->d_colmask,
+                                    stream)) != BSS_OK)
+            goto done;
     }
     if ((st = cuda_check(cudaMemcpyAsync(cnt.data(), d_cnt, sizeof(int32_t) * nq, cudaMemcpyDeviceToHost, stream),
                          "copy counts")) != BSS_OK)

@@ -51,8 +51,16 @@ typedef enum {
  * routing with fixed tensor shapes": one boolean per head). */
 enum { BSS_KIND_SPATIAL = 0, BSS_KIND_TEMPORAL = 1 };
 
-/* Tile classes stored in the top two bits of a tile-map entry. */
-enum { BSS_CLASS_FULL = 0, BSS_CLASS_BOUNDARY = 1, BSS_CLASS_PAD = 2 };
+/* Tile classes stored in the top two bits of a tile-map entry.
+ *   FULL      every pair retained: no mask
+ *   BOUNDARY  evaluates the coordinate predicate per row
+ *   PAD       kept tile of a tile-aligned mask with padding key columns: only
+ *             the padding is masked
+ *   COLUMNS   kept sink-segment tile of a tile-aligned map of permuted temporal
+ *             heads, some of whose frame-0 keys also sit in a kept band tile of
+ *             the same q tile: those columns (and padding) are masked, the same
+ *             for every row, so each physical key counts once */
+enum { BSS_CLASS_FULL = 0, BSS_CLASS_BOUNDARY = 1, BSS_CLASS_PAD = 2, BSS_CLASS_COLUMNS = 3 };
 #define BSS_CLASS_SHIFT 30
 #define BSS_TILE_INDEX_MASK 0x3FFFFFFF
 
@@ -62,9 +70,10 @@ enum {
     BSS_STAT_BOUNDARY = 1,      /* tiles that evaluate the coordinate predicate */
     BSS_STAT_PAD = 2,           /* kept tiles that mask padding columns only */
     BSS_STAT_SKIP = 3,          /* tiles never visited */
-    BSS_STAT_RETAINED = 4,      /* query-key pairs the result is defined over */
+    BSS_STAT_RETAINED = 4,      /* distinct query-key pairs the result is defined over */
     BSS_STAT_EXACT_RETAINED = 5,/* pairs retained by the exact (unrounded) mask */
-    BSS_STAT_COUNT = 6
+    BSS_STAT_COLUMNS = 6,       /* kept tiles masked by a column set (BSS_CLASS_COLUMNS) */
+    BSS_STAT_COUNT = 7
 };
 
 /* Video geometry and mask parameters.
@@ -88,7 +97,11 @@ enum {
  *                      blog's B2);
  *                      1: tile-aligned mask, a tile is kept iff at least half
  *                      of its real pairs are retained, then only padding
- *                      columns are masked (B3);
+ *                      columns are masked (B3); the result is attention over
+ *                      the set of physical pairs the kept tiles cover, so on
+ *                      permuted temporal heads a frame-0 key kept both in the
+ *                      sink segment and in a band tile is masked in the sink
+ *                      tile (BSS_CLASS_COLUMNS);
  *                      2: exact mask evaluated in every visited tile (the
  *                      blog's naive traversal B1, kept for comparison: every
  *                      non-skipped tile is classed BOUNDARY). */
@@ -103,9 +116,10 @@ typedef struct {
 } bss_mask_params;
 
 /* Opaque tile map: per mask kind, a CSR list of non-skipped kv tiles for every
- * q tile (ascending kv index, class in bits 30..31), its statistics and a
- * longest-first q-tile order.  Owns device memory; free with
- * bss_destroy_tile_map. */
+ * q tile (ascending kv index, class in bits 30..31), its statistics, a
+ * longest-first q-tile order and, for tile-aligned maps of permuted temporal
+ * heads, the retained-column bitmask of every (q tile, sink-segment tile).
+ * Owns device memory; free with bss_destroy_tile_map. */
 typedef struct bss_tile_map_s* bss_tile_map;
 
 /* Build the tile maps of both mask kinds for tiles of BQ query rows by BKV key
@@ -246,8 +260,11 @@ bss_status bss_route_heads(const void* Q, const void* K, const void* V, int32_t 
                            cudaStream_t stream);
 
 /* Scratch held by bss_build_tile_map_csr_noalloc (bytes): one byte per tile
- * plus one int32 per q tile (256-byte aligned) must fit in it. */
-#define BSS_NOALLOC_SCRATCH_BYTES (8u << 20)
+ * plus one int32 per q tile (256-byte aligned) must fit in it: about 8.3M
+ * tiles.  It holds the 302,400-token geometry (21 x 90 x 160) of either kind
+ * with 128 x 128 tiles (2,363 x 2,476 = 5.85M tiles), 256 x 128 or 256 x 64
+ * tiles, but not with 128 x 64 tiles (2,363 x 4,950 = 11.7M tiles). */
+#define BSS_NOALLOC_SCRATCH_BYTES ((int64_t)8 << 20)
 
 /* Tile-map build that allocates no device memory.  The blog has no counterpart
  * to this call: it exists for callers that cannot allocate device memory
@@ -270,9 +287,13 @@ bss_status bss_route_heads(const void* Q, const void* K, const void* V, int32_t 
  * Asynchronous on `stream`; calls no cudaMalloc, cudaFree or allocating
  * library routine.  The first call on a device looks up the array's device
  * address (cudaGetSymbolAddress), so make that first call before any stream
- * capture.  Every call uses the same array and it keeps the last call's
- * contents: calls whose work overlaps on the GPU (other streams or threads)
- * race and corrupt each other's maps, so serialize them.
+ * capture.  The address is kept for the process: it belongs to the context
+ * current at that first call (the primary context for runtime-API callers)
+ * and must not be used after that context is destroyed (cudaDeviceReset, or
+ * a driver-API context destroyed), so do not call this after either.  Every
+ * call uses the same array and it keeps the last call's contents: calls whose
+ * work overlaps on the GPU (other streams or threads) race and corrupt each
+ * other's maps, so serialize them.
  * Errors: INVALID_ARG (null / misaligned buffer, kind, tile sizes, capacity),
  * UNSUPPORTED (map larger than the scratch), CUDA. */
 bss_status bss_build_tile_map_csr_noalloc(const bss_mask_params* params, int32_t kind, int32_t BQ, int32_t BKV,

@@ -80,3 +80,39 @@ def compare(out_rows: np.ndarray, lse_rows, Oref: np.ndarray, lref: np.ndarray, 
             le = float(np.abs(lse_rows[fin] - lref[fin]).max())
             assert le <= LSE_ABS, f"{what}: max |dLSE| {le:.3e}"
     return maxe, meane, rel
+
+
+def rounded_row_counts(kind: int, g, BQ: int, BKV: int, qt0: int = 0, qt1=None):
+    """Distinct keys kept by each LAYOUT query row of q tiles [qt0, qt1) under the
+    tile-aligned mask, from the oracle's brute-force tile classes: every real row
+    of a q tile keeps the physical keys that the real columns of its kept tiles
+    read, each key once.  Returns an int64 array over the rows of those tiles
+    (padding rows past N dropped)."""
+    gg = g.with_bkv(BKV)
+    _, cls = oracle.classify(kind, gg, BQ, BKV, 1, qt0, qt1)
+    keys = oracle.key_rows(kind, gg)
+    ncols = keys.size
+    k = np.arange(ncols)
+    real = ((k < gg.S) | (k >= gg.S_pad)) if kind == oracle.TEMPORAL_PERMUTED else np.ones(ncols, bool)
+    per_tile = np.array([np.unique(keys[np.repeat(c != oracle.SKIP, BKV)[:ncols] & real]).size for c in cls],
+                        dtype=np.int64)
+    rows = np.repeat(per_tile, BQ)
+    return rows[: max(0, min(rows.size, gg.N - qt0 * BQ))]
+
+
+def exact_row_counts(kind: int, F: int, S: int, wf: int, ws: int):
+    """Closed-form retained keys of every query token t = f*S + s in (F,H,W)
+    order: spatial S*(frames in the band + the sink frame when outside it),
+    temporal F*b + (S - b) with b the raster positions in the band."""
+    t = np.arange(F * S, dtype=np.int64)
+    f, s = t // S, t % S
+    if kind == oracle.SPATIAL:
+        return S * (np.minimum(f + wf, F - 1) - np.maximum(f - wf, 0) + 1 + (f > wf))
+    b = np.minimum(s + ws, S - 1) - np.maximum(s - ws, 0) + 1
+    return F * b + (S - b)
+
+
+def fhw_of_layout(values: np.ndarray, F: int, S: int) -> np.ndarray:
+    """Reorder per-row values of a permuted (H,W,F) head to (F,H,W) token order."""
+    t = np.arange(F * S)
+    return values[(t % S) * F + t // S]

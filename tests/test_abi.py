@@ -73,7 +73,7 @@ def test_build_tile_map_rejects_bad_tiles_and_null(lib):
 
 def test_calls_with_stale_or_null_handles(lib):
     bogus = ctypes.c_void_p(0x1234)
-    out = (ctypes.c_int64 * 6)()
+    out = (ctypes.c_int64 * 7)()
     assert lib.bss_tile_map_stats(bogus, 0, out) == 1
     assert lib.bss_tile_map_stats(None, 0, out) == 1
     dims = (ctypes.c_int32 * 4)()

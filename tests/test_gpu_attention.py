@@ -163,7 +163,7 @@ def test_rounded_mask_with_empty_q_tiles_gives_zero_rows(bss, path):
         compare(O[h].float().cpu().numpy(), lrow.numpy(), ref[h][0], ref[h][1], f"{path} head {h}")
 
 
-def _full_size(bss, wl, tperm, rounding, heads, nrows):
+def _full_size(bss, wl, tperm, rounding, heads, nrows, tile_stride=1):
     dev = torch.device("cuda")
     Q, K, V = W.qkv_device(wl, dev)
     flags = wl.head_flags()
@@ -177,9 +177,20 @@ def _full_size(bss, wl, tperm, rounding, heads, nrows):
         torch.cuda.synchronize()
     assert bss.get_device_status() == 0
     g = oracle.Geometry(wl.F, wl.Hs, wl.Ws, wf=wl.wf, ws=wl.ws, bkv=128)
-    rows = W.sample_rows(wl.N, nrows, seed=wl.index)
+    sampled = W.sample_rows(wl.N, nrows, seed=wl.index)
+    # plus one row of every tile_stride-th q tile of the head's layout (the
+    # oracle classifies the q tile of every row of a rounded mask)
+    BQ = bss.ATTN_BQ
+    nq = -(-wl.N // BQ)
+    tiles = np.unique(np.append(np.arange(0, nq, tile_stride), nq - 1))
+    off = np.random.default_rng(wl.index).integers(0, BQ, tiles.size)
+    lay = np.minimum(tiles * BQ + off, wl.N - 1)
     for h in heads:
         kind = oracle_kind(flags[h], tperm)
+        per_tile = lay
+        if flags[h] and tperm:   # layout row p = s*F + f is token f*S + s
+            per_tile = (lay % wl.F) * wl.S + lay // wl.F
+        rows = sorted(set(sampled) | set(int(r) for r in per_tile))
         qh, kh, vh = (x[h].cpu() for x in (Q, K, V))
         Oref, lref = oracle.attention(W.bf16_bits(qh), W.bf16_bits(kh), W.bf16_bits(vh), kind, g, rows=rows,
                                       rounding=bool(rounding), BQ=bss.ATTN_BQ, BKV=bss.ATTN_BKV)
@@ -211,7 +222,7 @@ def test_full_size_mixed_75k_sampled(bss, tperm):
 def test_full_size_1440p_302k_rounded_sampled(bss):
     wl = W.P1440_302K
     fl = wl.head_flags()
-    _full_size(bss, wl, 1, 1, heads=[fl.index(0), fl.index(1)], nrows=12)
+    _full_size(bss, wl, 1, 1, heads=[fl.index(0), fl.index(1)], nrows=12, tile_stride=16)
 
 
 @pytest.mark.gpu

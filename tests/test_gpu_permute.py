@@ -96,3 +96,32 @@ def test_permute_flagged_touches_only_flagged_heads(bss):
             assert torch.equal(b[h].view(torch.int16), x[h].view(torch.int16))
         else:
             assert torch.all(b[h] == 7.0)
+
+
+@pytest.mark.gpu
+def test_permute_full_size_bit_exact_every_row(bss):
+    # all 10 heads x 75,600 rows of the mixed workload, forward and inverse, and
+    # the flagged-only form the step uses, against the oracle's scalar permutation
+    w = W.MIXED_75K
+    flags = w.head_flags()
+    dev = torch.device("cuda")
+    g = torch.Generator(device=dev).manual_seed(6)
+    X = torch.randint(-32768, 32767, (w.H, w.N, w.d), dtype=torch.int16, device=dev, generator=g)
+    Xb = X.view(torch.bfloat16)
+    fl = torch.tensor(flags, dtype=torch.uint8, device=dev)
+    p = bss.MaskParams(w.F, w.Hs, w.Ws, w.d, w.wf, w.ws)
+    xn = X.cpu().numpy().view(np.uint16)
+    for inverse in (False, True):
+        Y = torch.empty_like(Xb)
+        bss.permute(Xb, Y, fl, p, inverse=inverse)
+        Yf = torch.zeros_like(Xb)
+        bss.permute(Xb, Yf, fl, p, inverse=inverse, only_flagged=True)
+        torch.cuda.synchronize()
+        ref = oracle.permute(xn, w.F, w.S, flags, inverse=inverse)
+        assert np.array_equal(Y.cpu().view(torch.int16).numpy().view(np.uint16), ref)
+        yf = Yf.cpu().view(torch.int16).numpy().view(np.uint16)
+        for h in range(w.H):
+            if flags[h]:
+                assert np.array_equal(yf[h], ref[h]), f"head {h}"
+            else:
+                assert not yf[h].any(), f"head {h} was written"

@@ -26,7 +26,7 @@ def check_map(bss, tm, kind_code, g, BQ, BKV, rounding, qtiles=None):
         assert np.array_equal(row_ptr, orp)
         assert np.array_equal(entries, oent)
         st = tm.stats(kind)
-        for key in ("full", "boundary", "pad", "skip", "retained_pairs", "exact_retained_pairs"):
+        for key in ("full", "boundary", "pad", "skip", "retained_pairs", "exact_retained_pairs", "columns"):
             assert st[key] == ost[key], key
         return st
     for qt in qtiles:
@@ -102,8 +102,8 @@ def test_tile_map_full_size_sampled(bss, wl, tperm):
             assert st1["exact_retained_pairs"] == closed_form_temporal(wl.F, wl.S, wl.ws)
             for st, kd in ((st0, 0), (st1, 1)):
                 nq_, nkv, nnz, _ = tm.dims(kd)
-                assert st["full"] + st["boundary"] + st["pad"] + st["skip"] == nq_ * nkv
-                assert st["full"] + st["boundary"] + st["pad"] == nnz
+                assert st["full"] + st["boundary"] + st["pad"] + st["columns"] + st["skip"] == nq_ * nkv
+                assert st["full"] + st["boundary"] + st["pad"] + st["columns"] == nnz
                 if rounding == 0:
                     assert st["retained_pairs"] == st["exact_retained_pairs"]
                     assert st["pad"] == 0
@@ -120,3 +120,21 @@ def test_tile_map_pages_tile_shape_sampled(bss):
         assert nq == 23
         check_map(bss, tm, oracle.SPATIAL, g, 3328, 1536, 0, [0, nq - 1])
         assert tm.stats(0)["exact_retained_pairs"] == closed_form_spatial(wl.F, wl.S, wl.wf)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("rounding", [0, 1])
+@pytest.mark.parametrize("tperm", [1, 0])
+def test_tile_map_whole_75k_matches_oracle(bss, rounding, tperm):
+    # every q tile of the map the attention kernel runs at 75.6K tokens (256 x 128
+    # tiles) against the oracle's brute-force classifier, CSR and statistics
+    wl = W.MIXED_75K
+    BQ, BKV = 256, 128
+    g = oracle.Geometry(wl.F, wl.Hs, wl.Ws, wf=wl.wf, ws=wl.ws, bkv=BKV)
+    p = bss.MaskParams(wl.F, wl.Hs, wl.Ws, wl.d, wl.wf, wl.ws, temporal_permuted=tperm, rounding=rounding)
+    with bss.build_tile_map(p, BQ, BKV) as tm:
+        if tperm:
+            check_map(bss, tm, oracle.SPATIAL, g, BQ, BKV, rounding)
+        st = check_map(bss, tm, oracle.TEMPORAL_PERMUTED if tperm else oracle.TEMPORAL_FHW, g, BQ, BKV, rounding)
+    if rounding == 1 and tperm:
+        assert st["columns"] > 0
