@@ -3,9 +3,9 @@
 
 Step = one pass of the per-layer hot path of the blog "Accelerating
 Spatio-Temporal Attention for Video Diffusion on TPUs" (Figure 8) over one
-batch of synthetic input, all on the GPU:
-  flag-driven permutation of Q, K, V  ->  block-sparse attention (exact mask,
-  full / boundary tiles) whose stores put O back in (F,H,W) order
+batch of synthetic input, all on the GPU, two launches:
+  flag-driven permutation of Q, K, V (one launch)  ->  block-sparse attention
+  (exact mask, full / boundary tiles) whose stores put O back in (F,H,W) order
 on 75,600 tokens (21 x 45 x 80 latent patches) x 10 heads x d = 128, bf16,
 5 spatial heads (frame window 3 + first-frame sink) and 5 temporal heads
 (raster window 612 + sink) picked by seeded flags.  The tile map is built once
@@ -153,8 +153,114 @@ def traffic_from_profile():
         return None
 
 
+class NvmlClockSampler:
+    """In-process NVML sampling (read-only queries through ctypes) of the SM
+    clock, its maximum, the power draw and the clock-event reasons, every
+    `period_s` seconds on a background thread; only samples taken between
+    mark_begin() and mark_end() are kept."""
+    # clock-event reason bits of nvmlDeviceGetCurrentClocksEventReasons (nvml.h)
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+               0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, uuid: str | None, pci_bus_id: str | None, period_s: float = 0.005):
+        import ctypes
+        self.ok = False
+        self.period = period_s
+        self.samples = []
+        self.t_begin = self.t_end = None
+        self._stop = threading.Event()
+        self.thread = None
+        try:
+            lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if lib.nvmlInit_v2() != 0:
+                return
+            # NVML sees every GPU of the machine: find this process's GPU by its
+            # UUID or PCI bus id (an index could name another GPU)
+            h = ctypes.c_void_p()
+            rc = 1
+            if uuid:
+                rc = lib.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(h))
+            if rc != 0 and pci_bus_id:
+                rc = lib.nvmlDeviceGetHandleByPciBusId_v2(pci_bus_id.encode(), ctypes.byref(h))
+            if rc != 0:
+                return
+            self.lib, self.h, self.ct = lib, h, ctypes
+            mx = ctypes.c_uint()
+            self.max_mhz = float(mx.value) if lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0 else None
+            self.reason_fn = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                getattr(lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
+            self.ok = True
+        except Exception:
+            self.ok = False
+
+    def _one(self):
+        ct, lib, h = self.ct, self.lib, self.h
+        mhz, mw, rs = ct.c_uint(), ct.c_uint(), ct.c_ulonglong()
+        if lib.nvmlDeviceGetClockInfo(h, 1, ct.byref(mhz)) != 0:
+            return None
+        power = float(mw.value) / 1e3 if lib.nvmlDeviceGetPowerUsage(h, ct.byref(mw)) == 0 else None
+        reasons = int(rs.value) if self.reason_fn(h, ct.byref(rs)) == 0 else 0
+        return (time.monotonic(), float(mhz.value), power, reasons)
+
+    def _loop(self):
+        while not self._stop.is_set():
+            smp = self._one()
+            if smp is not None:
+                self.samples.append(smp)
+            time.sleep(self.period)
+
+    def start(self):
+        if self.ok:
+            self.thread = threading.Thread(target=self._loop, daemon=True)
+            self.thread.start()
+
+    def mark_begin(self):
+        self.t_begin = time.monotonic()
+
+    def mark_end(self):
+        self.t_end = time.monotonic()
+
+    def stop(self):
+        self._stop.set()
+        if self.thread:
+            self.thread.join(timeout=2)
+        kept = [x for x in self.samples if self.t_begin is not None and self.t_begin <= x[0] <= self.t_end]
+        return summarize_clocks([x[1] for x in kept], [self.max_mhz] if self.max_mhz else [],
+                                [x[2] for x in kept if x[2] is not None],
+                                {nm for x in kept for bit, nm in self.REASONS.items() if x[3] & bit},
+                                f"in-process NVML every {self.period * 1e3:.0f} ms")
+
+
+def summarize_clocks(sm, smax, power, reasons, how):
+    return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+            "sm_mhz_min": min(sm) if sm else None, "power_w_max": max(power) if power else None,
+            "reasons": sorted(reasons), "samples": len(sm),
+            "window": f"samples taken between the start and the end of the timed region ({how})"}
+
+
+def clock_sampler(torch, device_index: int):
+    """The NVML sampler when the driver's library answers, else nvidia-smi."""
+    uuid = bus = None
+    try:
+        prop = torch.cuda.get_device_properties(device_index)
+    except Exception:
+        prop = None
+    try:
+        u = str(prop.uuid)
+        uuid = u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        uuid = None
+    try:
+        bus = f"{prop.pci_domain_id:08X}:{prop.pci_bus_id:02X}:{prop.pci_device_id:02X}.0"
+    except Exception:
+        bus = None
+    s = NvmlClockSampler(uuid, bus)
+    return s if s.ok else ClockSampler(device_index)
+
+
 class ClockSampler:
-    """nvidia-smi sampling of SM clocks and throttle reasons during the timed region."""
+    """nvidia-smi sampling of SM clocks and throttle reasons during the timed
+    region (the fallback when NVML cannot be loaded in-process)."""
     QUERY = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -214,10 +320,7 @@ class ClockSampler:
             for nm, val in zip(names, parts[5:9]):
                 if val.lower() == "active":
                     reasons.add(nm)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
-                "sm_mhz_min": min(sm) if sm else None, "power_w_max": max(power) if power else None,
-                "reasons": sorted(reasons), "samples": len(sm),
-                "window": "samples taken between the start and the end of the timed region"}
+        return summarize_clocks(sm, smax, power, reasons, "nvidia-smi every 50 ms")
 
 
 # --------------------------------------------------------------------------- oracle (host)
@@ -331,10 +434,9 @@ def main():
                 e1.record(stream)
                 attn_events.append((e0, e1))
             return
-        # temporal heads permuted into the workspaces, spatial heads used in place
-        bss.permute(Q, Qp, fl, params, False, only_flagged=True)
-        bss.permute(K, Kp, fl, params, False, only_flagged=True)
-        bss.permute(V, Vp, fl, params, False, only_flagged=True)
+        # temporal heads' Q, K, V permuted into the workspaces (one launch),
+        # spatial heads used in place
+        bss.permute_flagged_multi((Q, K, V), (Qp, Kp, Vp), fl, params)
         if record:
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
@@ -344,7 +446,7 @@ def main():
             e1.record(stream)
             attn_events.append((e0, e1))
 
-    launches_per_step = 1 if args.dense else 4
+    launches_per_step = 1 if args.dense else 2
     for _ in range(max(3, args.warmup)):
         step()
     torch.cuda.synchronize()
@@ -352,7 +454,7 @@ def main():
     if status != 0:
         raise RuntimeError(f"device status {bss.status_string(status)} during warm-up")
 
-    sampler = ClockSampler(local_rank)
+    sampler = clock_sampler(torch, local_rank)
     sampler.start()
     time.sleep(0.3)
     sampler.mark_begin()
@@ -378,6 +480,9 @@ def main():
     attn_ms = statistics.mean(a.elapsed_time(b) for a, b in attn_events)
     value = whole_job_tflops(flops, world, ms_per_step)
     attn_tflops = flops / (attn_ms * 1e-3) / 1e12
+    dense_ctl = None
+    if not args.dense and not args.no_extras:
+        dense_ctl = dense_control(bss, torch, Q, K, V, O, Qp, Kp, Vp, tm, fl, retained, peaks)
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -389,7 +494,7 @@ def main():
                             ["exact (full/boundary tiles, B2)", "tile-aligned (B3)",
                              "every visited tile masked (B1)"][args.rounding]), "tile": [tm.BQ, tm.BKV],
                    "step": ("dense attention" if args.dense else
-                            "permute temporal heads' QKV -> sparse attention storing their O rows in (F,H,W) order"),
+                            "permute temporal heads' QKV (one launch) -> sparse attention storing their O rows in (F,H,W) order"),
                    "l2": f"inputs larger than L2 (Q+K+V = {3 * Q.numel() * 2 / 1e6:.0f} MB)",
                    "parallelism": "replicas" if world > 1 else "single GPU",
                    "retained_pairs": retained,
@@ -401,6 +506,8 @@ def main():
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clocks,
     }
+    if dense_ctl is not None:
+        line["dense_control"] = dense_ctl
     traffic = traffic_from_profile()
     if H != w.H and traffic is not None:
         traffic = traffic * H / w.H
@@ -477,29 +584,51 @@ def _time_interleaved(torch, fns, rounds=9, warm=2):
     return {n: statistics.median(a.elapsed_time(b) for a, b in ev[n]) for n in names}
 
 
+def dense_control(bss, torch, Q, K, V, O, Qp, Kp, Vp, tm, fl, retained, peaks, rounds=7):
+    """The library's dense kernel on the step's shape against the step's sparse
+    attention launch, timed interleaved (each round times both, in alternating
+    order, so clock drift under the power cap falls on both): the speed-up and
+    the retained-fraction target 1 / (retained pairs / all pairs)."""
+    H, N, d = Q.shape
+    Od = torch.empty_like(Q)
+    ms = _time_interleaved(torch, {
+        "sparse": lambda: bss.sparse_attention_split(Q, K, V, O, Qp, Kp, Vp, None, tm, fl),
+        "dense": lambda: bss.dense_attention(Q, K, V, Od)}, rounds=rounds)
+    frac = retained / (H * N * N)
+    speedup = ms["dense"] / ms["sparse"]
+    dense_flops = 4.0 * d * H * N * N
+    return {"ms": ms["dense"], "tflops": dense_flops / ms["dense"] / 1e9,
+            "frac_of_peak": dense_flops / ms["dense"] / 1e9 / peaks["bf16_tflops"],
+            "sparse_attention_ms": ms["sparse"], "speedup": speedup, "retained_fraction": frac,
+            "target_speedup": 1.0 / frac, "speedup_over_target": speedup * frac,
+            "timing": f"median of {rounds} interleaved rounds, same inputs"}
+
+
 def variants(bss, torch, W, w, H, Q, K, V, dev, peaks, flags):
     """Attention-kernel timings of the pages' other measurements, same inputs."""
     out = {}
     O = torch.empty_like(Q)
-    dense_ms = _time(torch, lambda: bss.dense_attention(Q, K, V, O))
     dense_flops = 4.0 * w.d * H * w.N * w.N
-    out["dense_control"] = {"ms": dense_ms, "tflops": dense_flops / dense_ms / 1e9,
-                            "frac_of_peak": dense_flops / dense_ms / 1e9 / peaks["bf16_tflops"]}
     zeros = torch.zeros(H, dtype=torch.uint8, device=dev)
-    # the pages' B1 -> B2 -> B3 progression, timed interleaved
+    # the pages' B0 (dense) -> B1 -> B2 -> B3 progression, timed interleaved
     bvars = (("spatial_naive_B1", 2), ("spatial_exact_B2", 0), ("spatial_tile_aligned_B3", 1))
     maps = {name: bss.build_tile_map(bss.MaskParams(w.F, w.Hs, w.Ws, w.d, w.wf, w.ws, temporal_permuted=1,
                                                     rounding=rnd)) for name, rnd in bvars}
     try:
-        bms = _time_interleaved(torch, {name: (lambda tm=tm: bss.sparse_attention(Q, K, V, O, tm, zeros))
-                                        for name, tm in maps.items()})
+        fns = {name: (lambda tm=tm: bss.sparse_attention(Q, K, V, O, tm, zeros)) for name, tm in maps.items()}
+        fns["dense"] = lambda: bss.dense_attention(Q, K, V, O)
+        bms = _time_interleaved(torch, fns)
+        dense_ms = bms["dense"]
+        out["dense_control"] = {"ms": dense_ms, "tflops": dense_flops / dense_ms / 1e9,
+                                "frac_of_peak": dense_flops / dense_ms / 1e9 / peaks["bf16_tflops"]}
         for name, _ in bvars:
             s0 = maps[name].stats(0)
             ms = bms[name]
             fl_ = 4.0 * w.d * H * s0["retained_pairs"]
+            frac = s0["retained_pairs"] / w.N ** 2
             out[name] = {"ms": ms, "tflops": fl_ / ms / 1e9, "frac_of_peak": fl_ / ms / 1e9 / peaks["bf16_tflops"],
-                         "speedup_vs_dense": dense_ms / ms, "retained_fraction": s0["retained_pairs"] / w.N ** 2,
-                         "tiles": s0}
+                         "speedup_vs_dense": dense_ms / ms, "retained_fraction": frac,
+                         "speedup_over_target": dense_ms / ms * frac, "tiles": s0}
     finally:
         for tm in maps.values():
             tm.destroy()
@@ -516,9 +645,9 @@ def variants(bss, torch, W, w, H, Q, K, V, dev, peaks, flags):
         for (bq, bkv), tmq in qmaps.items():
             st0 = tmq.stats(0)
             ms = qms[(bq, bkv)]
-            ex = st0["full"] + st0["boundary"] + st0["pad"]
+            ex = st0["full"] + st0["boundary"] + st0["pad"] + st0["columns"]
             lat[f"BQ{bq}_BKV{bkv}"] = {"ms": ms, "tflops": 4.0 * w.d * H * st0["retained_pairs"] / ms / 1e9,
-                                       "masked_share": (st0["boundary"] + st0["pad"]) / ex}
+                                       "masked_share": (st0["boundary"] + st0["pad"] + st0["columns"]) / ex}
     finally:
         for tmq in qmaps.values():
             tmq.destroy()
@@ -573,10 +702,15 @@ def variants(bss, torch, W, w, H, Q, K, V, dev, peaks, flags):
         nflag = int(half.sum().item())
         half_ms = _time_batched(torch, lambda: bss.permute(Q, Qp, half, p1, False, only_flagged=True))
         hbytes = 2.0 * nflag * w.N * w.d * 2
+        # the step's launch: the flagged heads of Q, K and V in one launch
+        qkv_ms = _time_batched(torch, lambda: bss.permute_flagged_multi((Q, K, V), (Qp, Kp, Vp), half, p1))
         out["permute"] = {"ms": perm_ms, "gbs": nbytes / perm_ms / 1e6, "frac_of_hbm_peak":
                           nbytes / perm_ms / 1e6 / peaks["hbm_gbs"],
                           "flagged_only_half_heads": {"ms": half_ms, "gbs": hbytes / half_ms / 1e6,
                                                       "frac_of_hbm_peak": hbytes / half_ms / 1e6 / peaks["hbm_gbs"]},
+                          "flagged_half_heads_qkv_one_launch": {
+                              "ms": qkv_ms, "gbs": 3 * hbytes / qkv_ms / 1e6,
+                              "frac_of_hbm_peak": 3 * hbytes / qkv_ms / 1e6 / peaks["hbm_gbs"]},
                           "timing": "20 launches back to back between one pair of CUDA events"}
     out["p1440_step"] = p1440_step(bss, torch, W, dev, peaks)
     return out
@@ -631,8 +765,9 @@ def tile_shape_sweep(bss, torch, w):
         row = {"BQ": bq, "BKV": bkv, "build_ms": s0.elapsed_time(s1)}
         for kind, name in ((0, "spatial"), (1, "temporal")):
             st = tm.stats(kind)
-            ex = st["full"] + st["boundary"] + st["pad"]
-            row[name] = {"executed_tiles": ex, "masked_share": (st["boundary"] + st["pad"]) / max(ex, 1),
+            ex = st["full"] + st["boundary"] + st["pad"] + st["columns"]
+            row[name] = {"executed_tiles": ex,
+                         "masked_share": (st["boundary"] + st["pad"] + st["columns"]) / max(ex, 1),
                          "executed_pairs_per_retained": ex * bq * bkv / st["retained_pairs"]}
         tm.destroy()
         rows.append(row)
@@ -640,20 +775,21 @@ def tile_shape_sweep(bss, torch, w):
 
 
 def e2e(bss, torch, params, tm, flags, Qd, Kd, Vd, flops, args):
-    """The same step through the public API from pinned host buffers.  Every
-    step copies its Q, K, V and flags host -> device and its O device -> host;
-    ``attention_step_host`` pipelines the copies over consecutive steps (three
-    workspace sets: the copies of one step overlap the kernels of another).  K
-    consecutive steps are timed with one pair of events on the compute stream: the side streams start after the
-    first event and the compute stream waits for the last step's D2H copy
-    before the second, so every step's copies are inside the timed region."""
+    """The same step through the library's host-buffer call
+    (bss_attention_step_host): every step copies its Q, K, V and flags host ->
+    device and its O device -> host, pipelined by the library over consecutive
+    steps (three workspace sets: the copies of one step overlap the kernels of
+    another; heads in groups of two).  K consecutive steps are timed with one
+    pair of events on the compute stream: the workspace's copy streams are
+    ordered after the first event and the compute stream waits for the last
+    step's D2H copy before the second, so every step's copies are inside the
+    timed region."""
     H, N, d = Qd.shape
     hq, hk, hv = (torch.empty(H, N, d, dtype=torch.bfloat16, pin_memory=True) for _ in range(3))
     ho = torch.empty(H, N, d, dtype=torch.bfloat16, pin_memory=True)
     for x, src in ((hq, Qd), (hk, Kd), (hv, Vd)):
         x.copy_(src.cpu())
-    dev = Qd.device
-    ws = bss.step_workspace(H, N, d, dev)
+    ws = bss.step_workspace(params, H)
     fl_host = torch.tensor(flags, dtype=torch.uint8).pin_memory()
     main = torch.cuda.current_stream()
     # as many steps as the device timing: the pipeline's fill (the first H2D
@@ -663,8 +799,7 @@ def e2e(bss, torch, params, tm, flags, Qd, Kd, Vd, flops, args):
     def run(n):
         t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         t0.record(main)
-        ws["copy_stream"].wait_event(t0)
-        ws["out_stream"].wait_event(t0)
+        ws.wait_stream(main)
         last = None
         for _ in range(n):
             last = bss.attention_step_host(hq, hk, hv, ho, tm, fl_host, ws)
@@ -676,29 +811,32 @@ def e2e(bss, torch, params, tm, flags, Qd, Kd, Vd, flops, args):
     run(3)
     # the copies alone, one step's worth each, on an idle GPU: how much time the
     # pipeline has to hide behind the kernels
-    cs = ws["copy_stream"]
+    cs = torch.cuda.Stream()
+    scratch = [torch.empty_like(Qd) for _ in range(3)]
     c0, c1, c2 = (torch.cuda.Event(enable_timing=True) for _ in range(3))
     torch.cuda.synchronize()
-    buf = ws["sets"][0]
     with torch.cuda.stream(cs):
         c0.record(cs)
-        for src, dst in ((hq, buf["Q"]), (hk, buf["K"]), (hv, buf["V"])):
+        for src, dst in zip((hq, hk, hv), scratch):
             dst.copy_(src, non_blocking=True)
         c1.record(cs)
-        ho.copy_(buf["O"], non_blocking=True)
+        ho.copy_(scratch[0], non_blocking=True)
         c2.record(cs)
     torch.cuda.synchronize()
     h2d_ms, d2h_ms = c0.elapsed_time(c1), c1.elapsed_time(c2)
-    sampler = ClockSampler(torch.cuda.current_device())
+    del scratch
+    sampler = clock_sampler(torch, torch.cuda.current_device())
     sampler.start()
     time.sleep(0.3)
     sampler.mark_begin()
     ms = run(steps)
     sampler.mark_end()
     clocks = sampler.stop()
+    ws.destroy()
     return {"value": flops / (ms * 1e-3) / 1e12, "unit": UNIT, "ms_per_step": ms, "steps": steps, "clocks": clocks,
             "copies_alone_ms": {"h2d_qkv": h2d_ms, "d2h_o": d2h_ms},
             "h2d_bytes_per_step": 3 * H * N * d * 2 + H, "d2h_bytes_per_step": H * N * d * 2,
+            "api": "bss_attention_step_host (C ABI) from pinned host buffers",
             "pipelining": "three workspace sets: the H2D copy of step i+1 and the D2H copy of step i-1 "
                           "overlap the kernels of step i; heads copied in and computed in groups of two"}
 

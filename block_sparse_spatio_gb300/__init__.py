@@ -78,7 +78,9 @@ EXPORTED = ("bss_build_tile_map", "bss_tile_map_stats", "bss_tile_map_dims", "bs
             "bss_get_device_status", "bss_status_string", "bss_last_error_message", "bss_version",
             "bss_diag_mma_tile", "bss_build_tile_map_csr_noalloc", "bss_route_heads",
             "bss_sparse_attention_fused", "bss_permute_flagged", "bss_sparse_attention_split",
-            "bss_diag_wait_timeout")
+            "bss_diag_wait_timeout", "bss_attention_step", "bss_step_workspace_create",
+            "bss_step_workspace_destroy", "bss_step_workspace_wait_stream", "bss_attention_step_host",
+            "bss_permute_flagged_multi")
 
 
 def load(path: str | None = None):
@@ -130,6 +132,18 @@ def load(path: str | None = None):
     lib.bss_build_tile_map_csr_noalloc.restype = st
     lib.bss_route_heads.argtypes = [p, p, p, i32, MP, p, i32, p, p, p]
     lib.bss_route_heads.restype = st
+    lib.bss_permute_flagged_multi.argtypes = [ctypes.POINTER(p), ctypes.POINTER(p), i32, p, i32, MP, i32, p]
+    lib.bss_permute_flagged_multi.restype = st
+    lib.bss_attention_step.argtypes = [p, p, p, p, p, p, p, i32, p, p, p, p]
+    lib.bss_attention_step.restype = st
+    lib.bss_step_workspace_create.argtypes = [MP, i32, i32, i32, ctypes.POINTER(p)]
+    lib.bss_step_workspace_create.restype = st
+    lib.bss_step_workspace_destroy.argtypes = [p]
+    lib.bss_step_workspace_destroy.restype = None
+    lib.bss_step_workspace_wait_stream.argtypes = [p, p]
+    lib.bss_step_workspace_wait_stream.restype = st
+    lib.bss_attention_step_host.argtypes = [p, p, p, p, p, p, p, p, p]
+    lib.bss_attention_step_host.restype = st
     _lib = lib
     return lib
 
@@ -271,6 +285,26 @@ def permute(x, out, head_is_temporal, params: MaskParams, inverse: bool = False,
     return out
 
 
+def permute_flagged_multi(xs, outs, head_is_temporal, params: MaskParams, inverse: bool = False, stream=None):
+    """outs[i] <- the flagged heads of xs[i] permuted, 1 to 3 tensors in one launch
+    (heads with flag 0 are left untouched in outs)."""
+    import torch
+    if len(xs) != len(outs) or not 1 <= len(xs) <= 3:
+        raise ValueError("1 to 3 (input, output) pairs")
+    for i, (x, o) in enumerate(zip(xs, outs)):
+        _dev_tensor(x, f"xs[{i}]", torch.bfloat16)
+        _dev_tensor(o, f"outs[{i}]", torch.bfloat16)
+        if x.shape != xs[0].shape or o.shape != xs[0].shape:
+            raise ValueError("every tensor must have the same shape")
+    _dev_tensor(head_is_temporal, "head_is_temporal", torch.uint8)
+    n = len(xs)
+    ins = (ctypes.c_void_p * n)(*[x.data_ptr() for x in xs])
+    ous = (ctypes.c_void_p * n)(*[o.data_ptr() for o in outs])
+    _check(load().bss_permute_flagged_multi(ins, ous, n, _ptr(head_is_temporal), xs[0].shape[0],
+                                            ctypes.byref(params.c()), int(bool(inverse)), _stream(stream)))
+    return outs
+
+
 def sparse_attention(Q, K, V, O, tile_map: TileMap, head_is_temporal=None, lse=None, softmax_scale: float = 0.0,
                      stream=None):
     """O <- block-sparse attention of [H][N][d] bf16 Q, K, V (temporal heads pre-permuted)."""
@@ -394,97 +428,112 @@ def route_heads(Q, K, V, params: MaskParams, rows, head_is_temporal, errors, str
 
 
 def attention_step(Q, K, V, O, tile_map: TileMap, head_is_temporal, Qp, Kp, Vp, Op=None, lse=None, stream=None):
-    """The per-layer path of the blog's Figure 8 on one GPU: permute the temporal
-    heads' Q, K, V to (H,W,F), run block-sparse attention, restore O's order.
-    Q, K, V, O are in (F,H,W) order; Qp, Kp, Vp are caller-owned workspaces (Op
-    is not needed: the attention writes the temporal heads' O rows straight to
-    their (F,H,W) positions; it is accepted for callers that pass four
-    workspaces).  lse, if given, is in each head's own layout."""
-    p = tile_map.params
-    if p.temporal_permuted:
-        # only the temporal heads are permuted; spatial heads are read from Q, K, V
-        # and written to O in place, temporal heads' rows are stored back in order
-        permute(Q, Qp, head_is_temporal, p, False, stream, only_flagged=True)
-        permute(K, Kp, head_is_temporal, p, False, stream, only_flagged=True)
-        permute(V, Vp, head_is_temporal, p, False, stream, only_flagged=True)
-        sparse_attention_split(Q, K, V, O, Qp, Kp, Vp, None, tile_map, head_is_temporal, lse, stream=stream)
-    else:
-        sparse_attention(Q, K, V, O, tile_map, head_is_temporal, lse, stream=stream)
+    """The per-layer path of the blog's Figure 8 on one GPU (``bss_attention_step``):
+    permute the temporal heads' Q, K, V to (H,W,F) into the workspaces Qp, Kp,
+    Vp, run block-sparse attention, and store their O rows back in (F,H,W)
+    order.  Q, K, V, O are in (F,H,W) order; Op is not needed (accepted for
+    callers that pass four workspaces).  lse, if given, is in each head's own
+    layout."""
+    import torch
+    named = [(Q, "Q"), (K, "K"), (V, "V"), (O, "O")] + [(t, n) for t, n in ((Qp, "Qp"), (Kp, "Kp"), (Vp, "Vp"))
+                                                          if t is not None]
+    for t, n in named:
+        _dev_tensor(t, n, torch.bfloat16)
+    _dev_tensor(head_is_temporal, "head_is_temporal", torch.uint8)
+    _dev_tensor(lse, "lse", torch.float32)
+    _check_shapes(tile_map, lse, *named)
+    _check(load().bss_attention_step(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(lse), tile_map.handle,
+                                     _ptr(head_is_temporal), Q.shape[0], _ptr(Qp), _ptr(Kp), _ptr(Vp),
+                                     _stream(stream)))
     return O
 
 
-def attention_step_host(hQ, hK, hV, hO, tile_map: TileMap, head_is_temporal, workspace, heads_per_chunk: int = 2,
-                        stream=None):
-    """The per-layer path from pinned HOST buffers: H2D copies of Q, K, V, the
-    permute -> block-sparse attention path of ``attention_step``, and the D2H copy of O,
-    pipelined over groups of heads (heads are independent) on three streams.
+class StepWorkspace:
+    """Owning wrapper of a ``bss_step_workspace`` (device buffer sets, copy
+    streams and events of ``attention_step_host``)."""
 
-    hQ, hK, hV, hO: pinned CPU bf16 [H][N][d]; head_is_temporal: device uint8[H],
-    or a pinned CPU uint8[H] that is copied to the device as part of the step;
-    workspace: from ``step_workspace``.  The
-    workspace holds ``depth`` buffer sets used in turn, so the copies of one
-    call overlap the kernels of the previous call; a set is reused only after
-    the kernels and the D2H copy of its previous call are done.  Kernels run on
-    ``stream`` (default: current), copies on the workspace's two side streams.
-    Groups of ``heads_per_chunk`` heads are copied in and computed in turn, so
-    the attention of one group starts while the next group is still being
-    copied.  Two heads a group (the default) cost nothing when the host link
-    keeps up and shorten the step when it does not: measured on the mixed
-    75.6K workload, 6.07 ms per step (median of 12) against 7.22 ms for one
-    group of all ten heads and 5.80 ms for the kernels alone, on a box whose
-    host-to-device copies slowed down now and then; single-head groups were
-    slower (7.2-7.4 ms: ten small attention launches, each with its own tail).
-    Returns a CUDA event that completes when the D2H copy of O is done."""
+    def __init__(self, handle, params: MaskParams, H: int, depth: int, heads_per_group: int):
+        self._h = handle
+        self.params, self.H, self.depth, self.heads_per_group = params, H, depth, heads_per_group
+
+    @property
+    def handle(self):
+        if self._h is None:
+            raise ValueError("step workspace destroyed")
+        return self._h
+
+    def wait_stream(self, stream=None):
+        """Order the workspace's copy streams after the work enqueued on ``stream``."""
+        _check(load().bss_step_workspace_wait_stream(self.handle, _stream(stream)))
+
+    def destroy(self):
+        if self._h is not None and _lib is not None:
+            _lib.bss_step_workspace_destroy(self._h)
+        self._h = None
+
+    def __del__(self):
+        try:
+            self.destroy()
+        except Exception:
+            pass
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.destroy()
+
+
+def step_workspace(params: MaskParams, H: int, depth: int = 3, heads_per_group: int = 2) -> StepWorkspace:
+    """Workspace of ``attention_step_host`` (``bss_step_workspace_create``).
+
+    depth buffer sets used in turn: with three (the default) the host-to-device
+    copy of a call can start while the device-to-host copy of the call two back
+    is still running; measured with two, steps were 2.4% slower (6.00 vs 5.86
+    ms on the mixed 75.6K workload, against 5.78 ms for the kernels alone).
+    heads_per_group heads are copied in and computed together: two (the
+    default) cost nothing when the host link keeps up and shorten the step when
+    it does not (6.07 ms per step against 7.22 ms for one group of all ten
+    heads on a box whose host-to-device copies slowed down now and then);
+    single-head groups were slower (7.2-7.4 ms: ten small attention launches,
+    each with its own tail)."""
+    h = ctypes.c_void_p()
+    mp = params.c()
+    _check(load().bss_step_workspace_create(ctypes.byref(mp), H, depth, heads_per_group, ctypes.byref(h)))
+    return StepWorkspace(h, params, H, depth, heads_per_group)
+
+
+def _host_tensor(t, name, dtype):
     import torch
-    H = hQ.shape[0]
-    main = torch.cuda.current_stream() if stream is None else stream
-    cs, os_ = workspace["copy_stream"], workspace["out_stream"]
-    k = workspace["next"]
-    workspace["next"] = (k + 1) % len(workspace["sets"])
-    buf = workspace["sets"][k]
-    Q, K, V, O = buf["Q"], buf["K"], buf["V"], buf["O"]
-    Qp, Kp, Vp = buf["Qp"], buf["Kp"], buf["Vp"]
-    free = workspace["free"][k]
-    if free is not None:
-        cs.wait_event(free)
-    flags = head_is_temporal
-    if not head_is_temporal.is_cuda:
-        flags = buf["flags"][:H]
-        with torch.cuda.stream(cs):
-            flags.copy_(head_is_temporal, non_blocking=True)
-    for h0 in range(0, H, heads_per_chunk):
-        h1 = min(H, h0 + heads_per_chunk)
-        with torch.cuda.stream(cs):
-            for src, dst in ((hQ, Q), (hK, K), (hV, V)):
-                dst[h0:h1].copy_(src[h0:h1], non_blocking=True)
-        ready = torch.cuda.Event()
-        ready.record(cs)
-        main.wait_event(ready)
-        with torch.cuda.stream(main):
-            attention_step(Q[h0:h1], K[h0:h1], V[h0:h1], O[h0:h1], tile_map, flags[h0:h1],
-                           Qp[h0:h1], Kp[h0:h1], Vp[h0:h1], stream=main)
-        done = torch.cuda.Event()
-        done.record(main)
-        os_.wait_event(done)
-        with torch.cuda.stream(os_):
-            hO[h0:h1].copy_(O[h0:h1], non_blocking=True)
-    finished = torch.cuda.Event()
-    finished.record(os_)
-    workspace["free"][k] = finished
-    return finished
+    if not isinstance(t, torch.Tensor) or t.is_cuda:
+        raise ValueError(f"{name} must be a CPU tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
 
 
-def step_workspace(H: int, N: int, d: int, device=None, depth: int = 3):
-    """Device buffer sets and side streams reused by ``attention_step_host``.
-    With three sets (the default) the host-to-device copy of a call can start
-    while the device-to-host copy of the call two back is still running; with
-    two it waits for it, and measured steps were 2.4% slower (6.00 vs 5.86 ms
-    on the mixed 75.6K workload, against 5.78 ms for the kernels alone)."""
+def attention_step_host(hQ, hK, hV, hO, tile_map: TileMap, head_is_temporal, workspace: StepWorkspace, stream=None):
+    """The per-layer path from HOST buffers (``bss_attention_step_host``): H2D
+    copies of Q, K, V, the ``attention_step`` kernels and the D2H copy of O,
+    pipelined over groups of heads on the workspace's copy streams and
+    ``stream`` (default: current).  hQ, hK, hV, hO: CPU bf16 [H][N][d], pinned
+    for overlap; head_is_temporal: CPU uint8[H].  Returns a CUDA event that
+    completes when hO is written; the inputs must not change before it."""
     import torch
-    device = device or torch.device("cuda")
-    sets = [{k: torch.empty(H, N, d, dtype=torch.bfloat16, device=device)
-             for k in ("Q", "K", "V", "O", "Qp", "Kp", "Vp")} for _ in range(depth)]
-    for st in sets:
-        st["flags"] = torch.empty(H, dtype=torch.uint8, device=device)
-    return {"sets": sets, "free": [None] * depth, "next": 0,
-            "copy_stream": torch.cuda.Stream(device=device), "out_stream": torch.cuda.Stream(device=device)}
+    for t, n in ((hQ, "hQ"), (hK, "hK"), (hV, "hV"), (hO, "hO")):
+        _host_tensor(t, n, torch.bfloat16)
+    _host_tensor(head_is_temporal, "head_is_temporal", torch.uint8)
+    p = tile_map.params
+    shape = (workspace.H, p.N, p.head_dim)
+    for t, n in ((hQ, "hQ"), (hK, "hK"), (hV, "hV"), (hO, "hO")):
+        if tuple(t.shape) != shape:
+            raise ValueError(f"{n} has shape {tuple(t.shape)}, the workspace and map want {shape}")
+    if tuple(head_is_temporal.shape) != (workspace.H,):
+        raise ValueError(f"head_is_temporal must have {workspace.H} entries")
+    done = torch.cuda.Event()
+    done.record()  # creates the event; the library records it again after the D2H copy
+    _check(load().bss_attention_step_host(_ptr(hQ), _ptr(hK), _ptr(hV), _ptr(hO), _ptr(head_is_temporal),
+                                          tile_map.handle, workspace.handle, ctypes.c_void_p(done.cuda_event),
+                                          _stream(stream)))
+    return done

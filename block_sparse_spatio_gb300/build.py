@@ -19,7 +19,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libbss.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["bss_api.cu", "bss_attention.cu", "bss_tilemap.cu", "bss_permute.cu", "bss_diag.cu", "bss_noalloc.cu", "bss_route.cu"]
+SOURCES = ["bss_api.cu", "bss_attention.cu", "bss_tilemap.cu", "bss_permute.cu", "bss_diag.cu", "bss_noalloc.cu",
+           "bss_route.cu", "bss_step.cu"]
 
 
 def nvcc() -> str:

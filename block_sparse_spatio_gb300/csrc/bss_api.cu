@@ -79,6 +79,8 @@ bss_status set_error(bss_status st, const char* fmt, ...) {
 
 void clear_error() { t_last_error[0] = '\0'; }
 
+bool tile_map_is_live(const bss_tile_map_s* m) { return map_is_live(const_cast<bss_tile_map>(m)); }
+
 bss_status cuda_check(cudaError_t e, const char* what) {
     if (e == cudaSuccess) return BSS_OK;
     return set_error(e == cudaErrorMemoryAllocation ? BSS_ERR_OOM : BSS_ERR_CUDA, "%s: %s", what,
@@ -300,6 +302,39 @@ bss_status bss_permute(const void* in, void* out, const uint8_t* head_is_tempora
 bss_status bss_permute_flagged(const void* in, void* out, const uint8_t* head_is_temporal, int32_t H,
                                const bss_mask_params* params, int32_t inverse, cudaStream_t stream) {
     return permute_impl(in, out, head_is_temporal, H, params, inverse, 1, stream);
+}
+
+bss_status bss_permute_flagged_multi(const void* const* in, void* const* out, int32_t count,
+                                     const uint8_t* head_is_temporal, int32_t H, const bss_mask_params* params,
+                                     int32_t inverse, cudaStream_t stream) {
+    using namespace bss;
+    t_last_error[0] = '\0';
+    bss_status st = validate_params(params);
+    if (st != BSS_OK) return st;
+    if (in == nullptr || out == nullptr) return set_error(BSS_ERR_INVALID_ARG, "NULL tensor array");
+    if (count < 1 || count > kMaxPermuteTensors)
+        return set_error(BSS_ERR_INVALID_ARG, "count must lie in [1, %d]", kMaxPermuteTensors);
+    if (H <= 0) return set_error(BSS_ERR_INVALID_ARG, "H must be positive");
+    if (inverse != 0 && inverse != 1) return set_error(BSS_ERR_INVALID_ARG, "inverse must be 0 or 1");
+    if (head_is_temporal == nullptr) return set_error(BSS_ERR_INVALID_ARG, "head_is_temporal is NULL (no head to permute)");
+    const int64_t S = static_cast<int64_t>(params->Hs) * params->Ws;
+    const uintptr_t bytes = static_cast<uintptr_t>(static_cast<int64_t>(H) * S * params->F * params->head_dim * 2);
+    for (int i = 0; i < count; ++i) {
+        if (in[i] == nullptr || out[i] == nullptr) return set_error(BSS_ERR_INVALID_ARG, "NULL tensor");
+        if (!aligned16(in[i]) || !aligned16(out[i])) return set_error(BSS_ERR_INVALID_ARG, "tensors must be 16-byte aligned");
+    }
+    // no output may overlap an input or another output
+    for (int i = 0; i < count; ++i) {
+        const uintptr_t b = reinterpret_cast<uintptr_t>(out[i]);
+        for (int j = 0; j < count; ++j) {
+            const uintptr_t a = reinterpret_cast<uintptr_t>(in[j]);
+            if (a < b + bytes && b < a + bytes) return set_error(BSS_ERR_INVALID_ARG, "an output overlaps an input");
+            const uintptr_t c = reinterpret_cast<uintptr_t>(out[j]);
+            if (j != i && c < b + bytes && b < c + bytes) return set_error(BSS_ERR_INVALID_ARG, "outputs overlap");
+        }
+    }
+    return launch_permute_multi(in, out, count, head_is_temporal, H, params->F, static_cast<int32_t>(S),
+                                params->head_dim, inverse, 1, stream);
 }
 
 namespace {

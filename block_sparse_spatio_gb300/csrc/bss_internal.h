@@ -8,6 +8,8 @@
 
 #include "bss.h"
 
+struct bss_tile_map_s;
+
 namespace bss {
 
 constexpr uint64_t kMapMagic = 0x6273735f6d617031ull;  // "bss_map1"
@@ -65,6 +67,11 @@ bss_status launch_tile_dedup(const Geom& geo, int32_t code, int32_t rounding, in
 // only_flagged: heads whose flag is 0 are not touched (else they are copied)
 bss_status launch_permute(const void* in, void* out, const uint8_t* flags, int32_t H, int32_t F, int32_t S,
                           int32_t d, int32_t inverse, int32_t only_flagged, cudaStream_t stream);
+// the same for `count` (in, out) pairs in one launch
+constexpr int kMaxPermuteTensors = 3;
+bss_status launch_permute_multi(const void* const* in, void* const* out, int32_t count, const uint8_t* flags,
+                                int32_t H, int32_t F, int32_t S, int32_t d, int32_t inverse, int32_t only_flagged,
+                                cudaStream_t stream);
 
 // attention launch (bss_attention.cu)
 struct AttnLaunch {
@@ -110,6 +117,7 @@ bool attention_supports_block_kv(int bkv);  // 64 or 128 for a map-driven call
 // helpers (bss_api.cu)
 bss_status set_error(bss_status st, const char* fmt, ...);
 void clear_error();  // empties the calling thread's last-error message
+bool tile_map_is_live(const bss_tile_map_s* m);  // a handle bss_build_tile_map returned and not destroyed
 bss_status cuda_check(cudaError_t e, const char* what);
 int* device_status_ptr();  // per-device status word (device address)
 bss_status encode_tmap_3d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint64_t heads,

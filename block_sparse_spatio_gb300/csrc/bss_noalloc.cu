@@ -19,7 +19,7 @@
 namespace bss {
 namespace {
 
-constexpr size_t kNoallocScratchBytes = BSS_NOALLOC_SCRATCH_BYTES;
+constexpr size_t kNoallocScratchBytes = static_cast<size_t>(BSS_NOALLOC_SCRATCH_BYTES);
 
 // Scratch shared by every call: [class byte per tile | pad to 256 | int32 per q tile].
 static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoallocScratchBytes];
@@ -30,7 +30,9 @@ uint8_t* g_scratch_dev[kMaxDevices] = {nullptr};
 
 // Device address of the scratch array on the current device.  Host code only
 // holds a stand-in for the array's name, so the address is looked up once per
-// device, with that device current.
+// device, with that device current, in the context then current (the device's
+// primary context for runtime-API callers); it stays valid for that context's
+// lifetime.
 bss_status scratch_address(uint8_t** out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -90,6 +92,7 @@ extern "C" bss_status bss_build_tile_map_csr_noalloc(const bss_mask_params* para
                                                      int32_t BKV, int32_t* row_ptr, int32_t* entries,
                                                      int64_t entries_capacity, int64_t* stats, cudaStream_t stream) {
     using namespace bss;
+    clear_error();
     bss_status st = check_mask_params(params);
     if (st != BSS_OK) return st;
     if (kind != 0 && kind != 1) return set_error(BSS_ERR_INVALID_ARG, "kind must be 0 or 1");
@@ -134,6 +137,11 @@ extern "C" bss_status bss_build_tile_map_csr_noalloc(const bss_mask_params* para
         return st;
     st = launch_tile_classify(g, code, params->rounding, BQ, BKV, static_cast<int32_t>(nq), static_cast<int32_t>(nkv),
                               cls, cnt, reinterpret_cast<unsigned long long*>(stats), stream);
+    if (st != BSS_OK) return st;
+    // rounded maps of permuted temporal heads: the sink copies of kept band keys
+    // (the column bitmasks are not needed for the CSR)
+    st = launch_tile_dedup(g, code, params->rounding, BQ, BKV, static_cast<int32_t>(nq), static_cast<int32_t>(nkv), cls,
+                           cnt, reinterpret_cast<unsigned long long*>(stats), nullptr, stream);
     if (st != BSS_OK) return st;
     row_ptr_scan_kernel<<<1, 1024, 0, stream>>>(cnt, row_ptr, static_cast<int32_t>(nq));
     if ((st = cuda_check(cudaGetLastError(), "row_ptr scan launch")) != BSS_OK) return st;

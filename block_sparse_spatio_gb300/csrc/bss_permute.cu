@@ -14,6 +14,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <cstring>
 
 #include "bss_internal.h"
 
@@ -38,16 +39,23 @@ __device__ __forceinline__ void st_stream(uint4* p, const uint4& v) {
 // grid ran 12% faster than a one-wave grid whose blocks loop).  A thread moves one
 // 16-byte piece of UNROLL rows, 256 / VEC_PER_ROW rows apart; the source row
 // index (one 32-bit division per row) is the only arithmetic.
+// blockIdx.z picks one of up to kMaxTensors (in, out) pairs permuted by the
+// same flags in one launch (the step's Q, K and V).
+struct Tensors {
+    const uint4* in[kMaxPermuteTensors];
+    uint4* out[kMaxPermuteTensors];
+};
+
 template <int VEC_PER_ROW, int UNROLL>
-__global__ void __launch_bounds__(256) permute_kernel(const uint4* __restrict__ in, uint4* __restrict__ out,
+__global__ void __launch_bounds__(256) permute_kernel(const __grid_constant__ Tensors t,
                                                       const uint8_t* __restrict__ flags, uint32_t N, uint32_t F,
                                                       uint32_t S, int inverse, int only_flagged) {
     constexpr uint32_t kRowsPerBlock = 256 / VEC_PER_ROW;
     const uint32_t h = blockIdx.y;
     const bool perm = flags != nullptr && flags[h] != 0;
     if (only_flagged && !perm) return;  // the head's rows stay as they are in `out`
-    const uint4* src_h = in + static_cast<size_t>(h) * N * VEC_PER_ROW;
-    uint4* dst_h = out + static_cast<size_t>(h) * N * VEC_PER_ROW;
+    const uint4* src_h = t.in[blockIdx.z] + static_cast<size_t>(h) * N * VEC_PER_ROW;
+    uint4* dst_h = t.out[blockIdx.z] + static_cast<size_t>(h) * N * VEC_PER_ROW;
     const uint32_t piece = threadIdx.x % VEC_PER_ROW;
     const uint32_t row0 = blockIdx.x * (kRowsPerBlock * UNROLL) + threadIdx.x / VEC_PER_ROW;
     uint4 v[UNROLL];
@@ -79,8 +87,18 @@ __global__ void __launch_bounds__(256) permute_kernel(const uint4* __restrict__ 
 
 bss_status launch_permute(const void* in, void* out, const uint8_t* flags, int32_t H, int32_t F, int32_t S,
                           int32_t d, int32_t inverse, int32_t only_flagged, cudaStream_t stream) {
+    const void* ins[1] = {in};
+    void* outs[1] = {out};
+    return launch_permute_multi(ins, outs, 1, flags, H, F, S, d, inverse, only_flagged, stream);
+}
+
+bss_status launch_permute_multi(const void* const* in, void* const* out, int32_t count, const uint8_t* flags,
+                                int32_t H, int32_t F, int32_t S, int32_t d, int32_t inverse, int32_t only_flagged,
+                                cudaStream_t stream) {
     const int64_t N = static_cast<int64_t>(F) * S;
-    if (N == 0 || H == 0) return BSS_OK;
+    if (N == 0 || H == 0 || count == 0) return BSS_OK;
+    if (count < 0 || count > kMaxPermuteTensors)
+        return set_error(BSS_ERR_INVALID_ARG, "between 1 and %d tensors per launch", kMaxPermuteTensors);
     if (N > 0xFFFFFFFFll / 16) return set_error(BSS_ERR_UNSUPPORTED, "too many tokens per head");
     if (H > 65535) return set_error(BSS_ERR_UNSUPPORTED, "too many heads (at most 65535)");
     const int threads = 256;
@@ -88,15 +106,19 @@ bss_status launch_permute(const void* in, void* out, const uint8_t* flags, int32
     constexpr int kUnroll = 4;
     const int64_t rows_per_block = threads / vec;
     const int64_t bx = (N + rows_per_block * kUnroll - 1) / (rows_per_block * kUnroll);
-    const dim3 grid(static_cast<unsigned>(bx), static_cast<unsigned>(H), 1);
-    const uint4* src = static_cast<const uint4*>(in);
-    uint4* dst = static_cast<uint4*>(out);
+    const dim3 grid(static_cast<unsigned>(bx), static_cast<unsigned>(H), static_cast<unsigned>(count));
+    Tensors t;
+    memset(&t, 0, sizeof(t));
+    for (int i = 0; i < count; ++i) {
+        t.in[i] = static_cast<const uint4*>(in[i]);
+        t.out[i] = static_cast<uint4*>(out[i]);
+    }
     if (d == 128) {
-        permute_kernel<16, kUnroll><<<grid, threads, 0, stream>>>(src, dst, flags, static_cast<uint32_t>(N), F, S,
-                                                                 inverse, only_flagged);
+        permute_kernel<16, kUnroll><<<grid, threads, 0, stream>>>(t, flags, static_cast<uint32_t>(N), F, S, inverse,
+                                                                 only_flagged);
     } else if (d == 64) {
-        permute_kernel<8, kUnroll><<<grid, threads, 0, stream>>>(src, dst, flags, static_cast<uint32_t>(N), F, S,
-                                                                inverse, only_flagged);
+        permute_kernel<8, kUnroll><<<grid, threads, 0, stream>>>(t, flags, static_cast<uint32_t>(N), F, S, inverse,
+                                                                only_flagged);
     } else {
         return set_error(BSS_ERR_UNSUPPORTED, "head_dim %d not supported (64 or 128)", d);
     }

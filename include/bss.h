@@ -25,7 +25,8 @@
  *  - Device-side problems (a pipeline wait that exceeded its time limit) are
  *    recorded in a per-device status word read by bss_get_device_status();
  *    the kernel then returns normally instead of hanging.
- *  - No call allocates device memory except bss_build_tile_map.
+ *  - No call allocates device memory except bss_build_tile_map,
+ *    bss_step_workspace_create and bss_route_heads (stream-ordered pool).
  *  - Handles are not thread-safe; one GPU, one stream per call.
  */
 #ifndef BSS_H_
@@ -171,6 +172,14 @@ bss_status bss_permute(const void* in, void* out, const uint8_t* head_is_tempora
 bss_status bss_permute_flagged(const void* in, void* out, const uint8_t* head_is_temporal, int32_t H,
                                const bss_mask_params* params, int32_t inverse, cudaStream_t stream);
 
+/* bss_permute_flagged of `count` (1..3) tensors with the same flags in one
+ * launch (the step's Q, K and V): in[i] -> out[i], host arrays of device
+ * pointers.  No output may overlap an input or another output.
+ * Errors: INVALID_ARG, UNSUPPORTED. */
+bss_status bss_permute_flagged_multi(const void* const* in, void* const* out, int32_t count,
+                                     const uint8_t* head_is_temporal, int32_t H, const bss_mask_params* params,
+                                     int32_t inverse, cudaStream_t stream);
+
 /* Block-sparse attention O = softmax(Q K^T * scale) V over the retained pairs
  * of each head's mask (blog: tiles of Q[i1:i2] K[j1:j2]^T with running softmax
  * statistics; full tiles mask-free, boundary tiles masked, skipped tiles never
@@ -258,6 +267,63 @@ bss_status bss_dense_attention(const void* Q, const void* K, const void* V, void
 bss_status bss_route_heads(const void* Q, const void* K, const void* V, int32_t H, const bss_mask_params* params,
                            const int32_t* rows, int32_t R, uint8_t* head_is_temporal, float* errors,
                            cudaStream_t stream);
+
+/* The per-layer path on device buffers (the blog's Figure 8; section "Support
+ * dynamic routing with fixed tensor shapes"): with a map built with
+ * temporal_permuted = 1, the temporal heads' Q, K, V are permuted into the
+ * workspaces Qp, Kp, Vp (bss_permute_flagged_multi, one launch), then
+ * bss_sparse_attention_split reads the spatial heads in place and stores every
+ * temporal head's output row straight to its (F,H,W) row of O; with
+ * temporal_permuted = 0, or
+ * head_is_temporal = NULL (every head spatial), it is bss_sparse_attention on
+ * Q, K, V.  Q, K, V, O: device [H][N][d] bf16 in (F,H,W) order; Qp, Kp, Vp:
+ * device [H][N][d] workspaces (only the temporal heads' rows are written; may
+ * be NULL when nothing is permuted); lse: optional device float[H][N], each
+ * head in its own layout (permuted temporal heads in (H,W,F) order).  Two
+ * launches on `stream`, no allocation.  Errors: those of the calls it makes. */
+bss_status bss_attention_step(const void* Q, const void* K, const void* V, void* O, float* lse, bss_tile_map map,
+                              const uint8_t* head_is_temporal, int32_t H, void* Qp, void* Kp, void* Vp,
+                              cudaStream_t stream);
+
+/* Opaque workspace of bss_attention_step_host: `depth` device buffer sets (Q,
+ * K, V, O and the three permutation workspaces, [H][N][d] bf16 each, plus the
+ * flags), two copy streams and events.  Owns device memory. */
+typedef struct bss_step_workspace_s* bss_step_workspace;
+
+/* Create a workspace for H heads of the geometry in params (F, Hs, Ws,
+ * head_dim; the windows are not used).  depth in [1, 8] buffer sets: a call
+ * uses the next set in turn, so with depth >= 2 the copies of one call overlap
+ * the kernels of the previous one (3 sets let the H2D copy of call i+1 start
+ * while the D2H copy of call i-1 still runs).  heads_per_group in [1, H]:
+ * heads copied in, computed and copied out together.  Allocates
+ * depth * (7 * H * N * d * 2 + H) bytes of device memory.  Synchronous.
+ * Errors: INVALID_ARG, UNSUPPORTED, OOM, CUDA. */
+bss_status bss_step_workspace_create(const bss_mask_params* params, int32_t H, int32_t depth,
+                                     int32_t heads_per_group, bss_step_workspace* out);
+
+/* Wait for the workspace's work to finish, then free it (no-op for NULL). */
+void bss_step_workspace_destroy(bss_step_workspace ws);
+
+/* Order the workspace's copy streams after all work enqueued on `stream` so
+ * far (e.g. after an event that opens a timed region). */
+bss_status bss_step_workspace_wait_stream(bss_step_workspace ws, cudaStream_t stream);
+
+/* bss_attention_step from HOST buffers, pipelined.  hQ, hK, hV: host [H][N][d]
+ * bf16 inputs in (F,H,W) order; hO: host output of the same shape;
+ * h_head_is_temporal: host uint8[H] flags, copied each call.  Host buffers
+ * should be page-locked (cudaHostAlloc / cudaHostRegister): pageable memory
+ * works, but its copies do not overlap anything.  Per group of heads: H2D
+ * copies of Q, K, V on the workspace's copy-in stream, the step's kernels on
+ * `stream` once they have landed, the D2H copy of O on the copy-out stream
+ * once they are done.  Returns once everything is enqueued; `done` (optional,
+ * a caller-created event) is recorded after the last D2H copy: do not read hO,
+ * or change the inputs, before it completes.  The map must be of the
+ * workspace's geometry (H, N, d).  Not thread-safe per workspace.
+ * Errors: INVALID_ARG (NULL buffer, stale handle, geometry), those of the
+ * calls it makes, CUDA. */
+bss_status bss_attention_step_host(const void* hQ, const void* hK, const void* hV, void* hO,
+                                   const uint8_t* h_head_is_temporal, bss_tile_map map, bss_step_workspace ws,
+                                   cudaEvent_t done, cudaStream_t stream);
 
 /* Scratch held by bss_build_tile_map_csr_noalloc (bytes): one byte per tile
  * plus one int32 per q tile (256-byte aligned) must fit in it: about 8.3M

@@ -230,3 +230,42 @@ def test_split_and_fused_attention_reject_bad_args_before_any_launch(lib):
     assert lib.bss_sparse_attention_split(a, a, a, a, a, a, a, None, None, m, None, 2, 0.0, None) == 1
     assert lib.bss_sparse_attention_fused(a, a, a, a, None, m, None, 2, 0.0, None) == 1
     assert lib.bss_sparse_attention_fused(a, a, a, a, None, None, None, 2, 0.0, None) == 1
+
+
+def test_step_calls_reject_bad_args_before_any_device_work(lib):
+    bogus = ctypes.c_void_p(0x1234)
+    x = ctypes.c_void_p(0x10000)
+    p = _params()
+    assert lib.bss_attention_step(x, x, x, x, None, bogus, None, 2, None, None, None, None) == 1
+    assert lib.bss_attention_step(x, x, x, x, None, None, None, 2, None, None, None, None) == 1
+    out = ctypes.c_void_p()
+    assert lib.bss_step_workspace_create(ctypes.byref(p), 0, 3, 1, ctypes.byref(out)) == 1        # H
+    assert lib.bss_step_workspace_create(ctypes.byref(p), 4, 0, 1, ctypes.byref(out)) == 1        # depth
+    assert lib.bss_step_workspace_create(ctypes.byref(p), 4, 9, 1, ctypes.byref(out)) == 1
+    assert lib.bss_step_workspace_create(ctypes.byref(p), 4, 3, 5, ctypes.byref(out)) == 1        # group
+    assert lib.bss_step_workspace_create(ctypes.byref(p), 4, 3, 0, ctypes.byref(out)) == 1
+    assert lib.bss_step_workspace_create(ctypes.byref(p), 4, 3, 1, None) == 1
+    bad = _params(head_dim=96)
+    assert lib.bss_step_workspace_create(ctypes.byref(bad), 4, 3, 1, ctypes.byref(out)) == 2
+    assert out.value is None
+    assert lib.bss_attention_step_host(x, x, x, x, x, bogus, bogus, None, None) == 1
+    assert lib.bss_step_workspace_wait_stream(bogus, None) == 1
+    lib.bss_step_workspace_destroy(None)
+    lib.bss_step_workspace_destroy(bogus)  # unknown handles are ignored
+
+
+def test_permute_flagged_multi_rejects_bad_args(lib):
+    p = _params()
+    a = [ctypes.c_void_p(0x10000 + i * 0x10000000) for i in range(6)]
+    arr = lambda *xs: (ctypes.c_void_p * len(xs))(*xs)  # noqa: E731
+    fl = ctypes.c_void_p(0x9000)
+    ins, outs = arr(a[0], a[1], a[2]), arr(a[3], a[4], a[5])
+    assert lib.bss_permute_flagged_multi(ins, outs, 0, fl, 2, ctypes.byref(p), 0, None) == 1   # count
+    assert lib.bss_permute_flagged_multi(ins, outs, 4, fl, 2, ctypes.byref(p), 0, None) == 1
+    assert lib.bss_permute_flagged_multi(ins, outs, 3, None, 2, ctypes.byref(p), 0, None) == 1  # flags
+    assert lib.bss_permute_flagged_multi(None, outs, 3, fl, 2, ctypes.byref(p), 0, None) == 1
+    assert lib.bss_permute_flagged_multi(ins, arr(a[3], a[1], a[5]), 3, fl, 2, ctypes.byref(p), 0, None) == 1
+    assert lib.bss_permute_flagged_multi(ins, arr(a[3], a[3], a[5]), 3, fl, 2, ctypes.byref(p), 0, None) == 1
+    assert lib.bss_permute_flagged_multi(ins, arr(a[3], ctypes.c_void_p(0x30000008), a[5]), 3, fl, 2,
+                                         ctypes.byref(p), 0, None) == 1                        # misaligned
+    assert lib.bss_permute_flagged_multi(ins, outs, 3, fl, 0, ctypes.byref(p), 0, None) == 1   # H

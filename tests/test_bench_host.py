@@ -77,3 +77,38 @@ def test_traffic_figure_is_dropped_when_the_kernel_changes(monkeypatch, tmp_path
 def test_whole_job_throughput_counts_every_rank(world):
     # every rank does the same work in the slowest rank's time
     assert bench.whole_job_tflops(2.0e12, world, 1000.0) == pytest.approx(2.0 * world)
+
+
+def test_nvml_clock_record_window_and_reason_bits():
+    # the in-process sampler keeps samples inside the timed region only and
+    # decodes the clock-event reason bits of each kept sample
+    s = bench.NvmlClockSampler.__new__(bench.NvmlClockSampler)
+    s.period, s.max_mhz, s.thread = 0.005, 2070.0, None
+    s._stop = bench.threading.Event()
+    s.t_begin, s.t_end = 10.0, 11.0
+    s.samples = [
+        (9.9, 2070.0, 120.0, 0x0),          # before the region
+        (10.1, 1800.0, 1380.0, 0x4),        # sw_power_cap
+        (10.5, 1755.0, 1395.0, 0x4 | 0x0),
+        (10.9, 1790.0, 1390.0, 0x0),
+        (11.2, 600.0, 90.0, 0x8 | 0x40),    # after: hw_slowdown / hw_thermal_slowdown not counted
+    ]
+    rec = s.stop()
+    assert rec["samples"] == 3
+    assert rec["sm_mhz"] == 1790.0 and rec["sm_mhz_min"] == 1755.0 and rec["sm_max_mhz"] == 2070.0
+    assert rec["power_w_max"] == 1395.0
+    assert rec["reasons"] == ["sw_power_cap"]
+    assert "NVML" in rec["window"]
+
+
+def test_nvml_sampler_without_the_driver_falls_back():
+    # no NVML here: the sampler reports itself unusable and clock_sampler
+    # falls back to the nvidia-smi reader
+    s = bench.NvmlClockSampler(None, None)
+    if not s.ok:
+        class _T:
+            class cuda:
+                @staticmethod
+                def get_device_properties(i):
+                    raise RuntimeError("no GPU")
+        assert isinstance(bench.clock_sampler(_T, 0), bench.ClockSampler)

@@ -1,6 +1,7 @@
-"""The pipelined host-buffer step gives the same O as the device step, also when
-consecutive calls overlap (the workspace's buffer sets used in turn, each
-reused once its previous call is done)."""
+"""The pipelined host-buffer step (bss_attention_step_host, through the C ABI)
+gives the same O as the device step, also when consecutive calls overlap (the
+workspace's buffer sets used in turn, each reused once its previous call is
+done)."""
 import pytest
 import torch
 
@@ -8,10 +9,10 @@ import workloads as W
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("hpc", [1, 2, 3])
-@pytest.mark.parametrize("host_flags", [False, True])
-@pytest.mark.parametrize("depth", [2, 3])
-def test_host_steps_match_device_step(bss, hpc, host_flags, depth):
+@pytest.mark.parametrize("hpc", [1, 2, 3, 5])
+@pytest.mark.parametrize("pinned", [False, True])
+@pytest.mark.parametrize("depth", [1, 2, 3])
+def test_host_steps_match_device_step(bss, hpc, pinned, depth):
     w = W.SMALL
     H = 5
     flags = torch.tensor([0, 1, 1, 0, 1], dtype=torch.uint8)
@@ -28,18 +29,44 @@ def test_host_steps_match_device_step(bss, hpc, host_flags, depth):
             ws = [torch.empty_like(Q) for _ in range(4)]
             bss.attention_step(Q, K, V, O, tm, fl, *ws)
             expect.append(O.cpu())
-        hosts = [tuple(x.pin_memory() for x in qkv) for qkv in inputs]
-        outs = [torch.empty_like(inputs[0][0]).pin_memory() for _ in range(calls)]
-        wsp = bss.step_workspace(H, w.N, w.d, dev, depth=depth)
-        hfl = flags.pin_memory() if host_flags else fl
-        events = [bss.attention_step_host(*hosts[c], outs[c], tm, hfl, wsp, heads_per_chunk=hpc)
-                  for c in range(calls)]
+        pin = (lambda x: x.pin_memory()) if pinned else (lambda x: x.clone())  # pageable copies work too
+        hosts = [tuple(pin(x) for x in qkv) for qkv in inputs]
+        outs = [pin(torch.empty_like(inputs[0][0])) for _ in range(calls)]
+        wsp = bss.step_workspace(p, H, depth=depth, heads_per_group=hpc)
+        hfl = pin(flags)
+        events = [bss.attention_step_host(*hosts[c], outs[c], tm, hfl, wsp) for c in range(calls)]
         for e in events:
             e.synchronize()
         torch.cuda.synchronize()
         assert bss.get_device_status() == 0
         for c in range(calls):
             assert torch.equal(outs[c].view(torch.int16), expect[c].view(torch.int16)), f"call {c}"
+        wsp.destroy()
+
+
+@pytest.mark.gpu
+def test_host_step_rejects_mismatched_buffers_before_any_work(bss):
+    w = W.SMALL
+    p = bss.MaskParams(w.F, w.Hs, w.Ws, w.d, w.wf, w.ws)
+    hq = torch.zeros(2, w.N, w.d, dtype=torch.bfloat16).pin_memory()
+    ho = torch.full_like(hq, 5.0)
+    flags = torch.tensor([0, 1], dtype=torch.uint8)
+    with bss.build_tile_map(p) as tm, bss.step_workspace(p, 2) as wsp:
+        with pytest.raises(ValueError):  # shape of another H
+            bss.attention_step_host(hq[:1], hq[:1], hq[:1], ho[:1], tm, flags[:1], wsp)
+        other = bss.MaskParams(w.F, w.Hs, w.Ws + 8, w.d, w.wf, w.ws)
+        with bss.build_tile_map(other) as tm2, pytest.raises(ValueError):  # geometry
+            bss.attention_step_host(hq, hq, hq, ho, tm2, flags, wsp)
+        lib = bss.load()
+        import ctypes
+        rc = lib.bss_attention_step_host(ctypes.c_void_p(hq.data_ptr()), ctypes.c_void_p(hq.data_ptr()),
+                                         ctypes.c_void_p(hq.data_ptr()), ctypes.c_void_p(ho.data_ptr()),
+                                         None, tm.handle, wsp.handle, None, None)
+        assert rc == 1 and b"NULL" in lib.bss_last_error_message()
+        torch.cuda.synchronize()
+        assert bool((ho == 5.0).all())
+    with pytest.raises(bss.BssError):
+        bss.step_workspace(p, 2, depth=9)
 
 
 @pytest.mark.gpu
@@ -84,7 +111,7 @@ def test_host_steps_at_full_size_match_device_step(bss):
             hosts.append(tuple(x.cpu().pin_memory() for x in (Q, K, V)))
             del Q, K, V, O
         outs = [torch.empty(w.H, w.N, w.d, dtype=torch.bfloat16).pin_memory() for _ in range(calls)]
-        wsp = bss.step_workspace(w.H, w.N, w.d, dev)
+        wsp = bss.step_workspace(p, w.H)
         hfl = flags.pin_memory()
         events = [bss.attention_step_host(*hosts[c], outs[c], tm, hfl, wsp) for c in range(calls)]
         for e in events:
@@ -93,3 +120,4 @@ def test_host_steps_at_full_size_match_device_step(bss):
         assert bss.get_device_status() == 0
         for c in range(calls):
             assert torch.equal(outs[c].view(torch.int16), expect[c].view(torch.int16)), f"call {c}"
+        wsp.destroy()

@@ -125,3 +125,32 @@ def test_permute_full_size_bit_exact_every_row(bss):
                 assert np.array_equal(yf[h], ref[h]), f"head {h}"
             else:
                 assert not yf[h].any(), f"head {h} was written"
+
+
+@pytest.mark.gpu
+def test_permute_flagged_multi_equals_three_single_launches(bss):
+    # one launch for Q, K and V (the step's) is bit for bit three flagged launches;
+    # unflagged heads of every output keep their bytes
+    w = W.SMALL
+    H = 4
+    flags = [1, 0, 1, 1]
+    p = bss.MaskParams(w.F, w.Hs, w.Ws, w.d, w.wf, w.ws)
+    dev = torch.device("cuda")
+    xs = [t.to(dev) for t in W.qkv(w, H=H, seed=8)]
+    fl = torch.tensor(flags, dtype=torch.uint8, device=dev)
+    for inverse in (False, True):
+        one = [torch.full_like(xs[0], 7.0) for _ in range(3)]
+        bss.permute_flagged_multi(xs, one, fl, p, inverse)
+        ref = [torch.full_like(xs[0], 7.0) for _ in range(3)]
+        for x, r in zip(xs, ref):
+            bss.permute(x, r, fl, p, inverse, only_flagged=True)
+        torch.cuda.synchronize()
+        for a, b in zip(one, ref):
+            assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+        assert torch.all(one[1][1] == 7.0)
+    for n in (1, 2):
+        outs = [torch.empty_like(xs[0]) for _ in range(n)]
+        bss.permute_flagged_multi(xs[:n], outs, fl, p)
+    torch.cuda.synchronize()
+    with pytest.raises(bss.BssError):   # an output overlapping an input
+        bss.permute_flagged_multi(xs, [xs[1], one[1], one[2]], fl, p)
