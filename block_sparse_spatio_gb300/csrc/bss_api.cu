@@ -144,22 +144,6 @@ bss_status encode_tmap_3d(CUtensorMap* map, const void* base, uint64_t inner, ui
     return BSS_OK;
 }
 
-bss_status encode_tmap_rows_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows,
-                               uint64_t row_stride_bytes, uint32_t box_inner) {
-    PFN_cuTensorMapEncodeTiled_v12000 enc = nullptr;
-    bss_status st = encode_fn(&enc);
-    if (st != BSS_OK) return st;
-    cuuint64_t dims[2] = {inner, rows};
-    cuuint64_t strides[1] = {row_stride_bytes};
-    cuuint32_t box[2] = {box_inner, 1};
-    cuuint32_t estr[2] = {1, 1};
-    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) return set_error(BSS_ERR_CUDA, "cuTensorMapEncodeTiled (rows) failed (CUresult %d)", (int)r);
-    return BSS_OK;
-}
-
 bss_status check_mask_params(const bss_mask_params* p) { return validate_params(p); }
 
 }  // namespace bss

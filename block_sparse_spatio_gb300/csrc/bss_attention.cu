@@ -99,7 +99,7 @@ static_assert(kRegsControl + 2 * kRegsSoftmax <= 512, "register split exceeds an
 struct AttnArgs {
     CUtensorMap tm_q, tm_k, tm_v, tm_o, tm_ks, tm_vs;
     CUtensorMap tm_qt, tm_kt, tm_vt, tm_ot;  // heads with flag 1 (= the maps above unless split buffers)
-    CUtensorMap tm_qg, tm_kg, tm_vg;  // [H*N] rows views, one-row boxes (fused permutation)
+    const uint16_t *q_rows, *k_rows, *v_rows;  // Q, K, V as bf16 bits (fused permutation: row gathers)
     uint16_t* o_rows;                 // O as bf16 bits (fused permutation: row-wise stores)
     const int32_t* qmap;              // routing: token index of each query row (mask predicate)
     float* o_f32;                     // routing: [splits][3H][Nq][D] normalised fp32 outputs
@@ -119,20 +119,36 @@ struct AttnArgs {
     float scale_log2;
 };
 
-static_assert(kHalf == 128 && kBKV == 128, "the gather producer maps 4 rows to each of 32 lanes");
+// Fused permutation: the threads of warps 2 and 3 gather the permuted rows of
+// a temporal head's Q and band K / V tiles with 16-byte cp.async copies.
+constexpr int kGatherThreads = 64;
+constexpr int kGatherThread0 = 64;  // first thread of warp 2
 
-// Fused permutation: row of the (F,H,W)-ordered tensor (in the [H*N] rows view)
-// holding (H,W,F)-permuted rows p0 .. p0+3 of head h, p = s*F + f -> f*S + s.
-// Rows past the end of the sequence repeat the last row: they are padding
-// (query rows never stored, key columns masked with P = 0).
-__device__ __forceinline__ void fused_rows4(const AttnArgs& a, int h, int p0, int (&r)[4]) {
-    int s = p0 / a.F, f = p0 - s * a.F;
-    const int base = h * a.N;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        r[i] = p0 + i < a.N ? base + f * a.S + s : base + a.N - 1;
-        if (++f == a.F) {
-            f = 0;
+// One 128-row tile of permuted rows p0 .. p0+127 of a head whose (F,H,W) rows
+// start at g (already offset by this thread's 16-byte unit): permuted row
+// p = s*F + f is row f*S + s of g; rows past the end of the sequence repeat the
+// last row (they are padding: query rows are never stored, key columns are
+// masked with P = 0).  Thread (unit, rsub) copies unit `unit` of rows rsub,
+// rsub + RPR, ... into the 128-byte swizzled layout of a tiled TMA load with
+// 64-column boxes: 64-column chunk unit / 8 (chunks chunk_bytes apart), row r
+// at r * 128, 16-byte unit (unit % 8) ^ (r % 8).  Consecutive lanes copy
+// consecutive units of a row, so a warp instruction reads whole rows.
+template <int D, int RPR>
+__device__ __forceinline__ void gather_tile(uint32_t sbase, const uint16_t* g, int p0, int rsub, int unit,
+                                            const AttnArgs& a) {
+    const uint32_t base = sbase + static_cast<uint32_t>(unit >> 3) * kChunkBytesSw128;
+    const uint32_t u = static_cast<uint32_t>(unit & 7);
+    int p = p0 + rsub;
+    int s = p / a.F, f = p - s * a.F;
+#pragma unroll 4
+    for (int r = rsub; r < kHalf; r += RPR) {
+        const int row = p < a.N ? f * a.S + s : a.N - 1;
+        cp_async_16(base + static_cast<uint32_t>(r) * 128u + ((u ^ static_cast<uint32_t>(r & 7)) << 4),
+                    g + static_cast<size_t>(row) * D);
+        p += RPR;
+        f += RPR;
+        while (f >= a.F) {
+            f -= a.F;
             ++s;
         }
     }
@@ -330,11 +346,19 @@ __global__ void __launch_bounds__(threads_for<HALVES>(), 1) attn_fwd_kernel(cons
         }
     }
 
+    // temporal head whose (H,W,F) permutation is applied by the loads and stores
+    // (fused mode 1), or by the output stores only (mode 2: Q, K, V come permuted,
+    // O rows go straight to their (F,H,W) positions)
+    const bool gather = BKV == 128 && !ROUTE && args.fused == 1 && code == MASK_TEMPORAL_VIRT;
+    const bool scatter = gather || (!ROUTE && args.fused == 2 && code == MASK_TEMPORAL_VIRT);
+    // a stage filled by the gathering threads completes with one arrival of each
+    const uint32_t fill_arrivals = gather ? kGatherThreads : 1;
+
     if (threadIdx.x == 0) {
-        mbar_init(bar_q, 1);
+        mbar_init(bar_q, fill_arrivals);
         for (int s = 0; s < kStages; ++s) {
-            mbar_init(bar_k_full + s, 1);
-            mbar_init(bar_v_full + s, 1);
+            mbar_init(bar_k_full + s, fill_arrivals);
+            mbar_init(bar_v_full + s, fill_arrivals);
             mbar_init(bar_k_empty + s, 1);
             mbar_init(bar_v_empty + s, 1);
         }
@@ -352,35 +376,38 @@ __global__ void __launch_bounds__(threads_for<HALVES>(), 1) attn_fwd_kernel(cons
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    // temporal head whose (H,W,F) permutation is applied by the loads and stores
-    // (fused mode 1), or by the output stores only (mode 2: Q, K, V come permuted,
-    // O rows go straight to their (F,H,W) positions)
-    const bool gather = BKV == 128 && !ROUTE && args.fused == 1 && code == MASK_TEMPORAL_VIRT;
-    const bool scatter = gather || (!ROUTE && args.fused == 2 && code == MASK_TEMPORAL_VIRT);
-
     if (warp < 4) {
         // warpgroup 0: TMA producer, MMA issuer, two spare warps
         if constexpr (HALVES == 2) setmaxnreg_dec<kRegsControl>();
-        if (warp == 0 && gather) {
-            // =========================== TMA producer, fused permutation: each lane
-            // gathers 4 permuted rows of every 128-row tile (tile::gather4 per 64-column
-            // chunk); frame-0 keys of the sink segment are contiguous, one box load.
-            if (lane == 0) {
-                tma_prefetch_desc(&args.tm_qg);
-                tma_prefetch_desc(&args.tm_kg);
-                tma_prefetch_desc(&args.tm_vg);
-                mbar_arrive_expect_tx(bar_q, HALVES * L::kTile);
+        if (gather && (warp == 2 || warp == 3)) {
+            // =========================== gather producer, fused permutation: the 64
+            // threads of warps 2-3 copy Q and every band K / V tile row by row
+            // (gather_tile) with cp.async; each thread's arrival on the fill's
+            // barrier fires when its copies have landed (64 arrivals a fill), so
+            // the threads only ever wait for a free stage, as a TMA producer does.
+            // The copies are generic-proxy writes: the MMA issuer orders them
+            // before the tensor cores' reads with a proxy fence after its wait.
+            // Sink tiles (frame-0 keys, contiguous in (F,H,W) order) are one box
+            // load each (thread 0 arms the barrier, the others arrive).
+            constexpr int kUnits = D / 8;  // 16-byte units per row
+            constexpr int kRPR = kGatherThreads / kUnits;
+            const int t = static_cast<int>(threadIdx.x) - kGatherThread0;
+            const int unit = t % kUnits, rsub = t / kUnits;
+            const size_t head_off = static_cast<size_t>(h) * args.N * D + static_cast<size_t>(unit) * 8;
+            const uint16_t* gq = args.q_rows + head_off;
+            const uint16_t* gk = args.k_rows + head_off;
+            const uint16_t* gv = args.v_rows + head_off;
+            // the barrier gets this thread's arrival when its copies so far have
+            // landed: the thread goes on to the next fill without waiting
+            auto close_fill = [&](uint64_t* bar) { cp_async_mbar_arrive_noinc(bar); };
+            if (t == 0) {
+                tma_prefetch_desc(&args.tm_ks);
+                tma_prefetch_desc(&args.tm_vs);
             }
-            __syncwarp();
 #pragma unroll
-            for (int hh = 0; hh < HALVES; ++hh) {
-                int r4[4];
-                fused_rows4(args, h, qt * kBQt + hh * kHalf + 4 * lane, r4);
-#pragma unroll
-                for (int c = 0; c < kChunks; ++c)
-                    tma_gather4_2d(sQ + hh * L::kTile + c * kChunkBytesSw128 + lane * 512, &args.tm_qg, c * 64, r4[0],
-                                   r4[1], r4[2], r4[3], bar_q);
-            }
+            for (int hh = 0; hh < HALVES; ++hh)
+                gather_tile<D, kRPR>(smem_u32(sQ + hh * L::kTile), gq, qt * kBQt + hh * kHalf, rsub, unit, args);
+            close_fill(bar_q);
             bool ok = true;
             int jk = 0, jv = 0;
             for (; jv < n; ++jv) {
@@ -388,54 +415,58 @@ __global__ void __launch_bounds__(threads_for<HALVES>(), 1) attn_fwd_kernel(cons
                 const uint32_t e = entry_at<ROUTE, BKV>(args, ents, jv, code, j0);
                 const int col0 = static_cast<int>(e & BSS_TILE_INDEX_MASK) * BKV;
                 const bool sink = col0 < args.S_pad;
-                int r4[4] = {0, 0, 0, 0};
-                if (!sink) fused_rows4(args, h, col0 - args.S_pad + 4 * lane, r4);
-                if (jv >= kStages)
+                if (jv >= kStages) {
                     ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_k_empty + st, ((jv / kStages) - 1) & 1, status));
+                    // the tensor cores' reads of the stage come before these writes
+                    fence_proxy_async_smem();
+                }
                 if (!ok) break;
-                if (lane == 0) mbar_arrive_expect_tx(bar_k_full + st, L::kTileKV);
-                __syncwarp();
                 if (sink) {
-                    if (lane == 0) {
+                    if (t == 0) {
+                        mbar_arrive_expect_tx(bar_k_full + st, L::kTileKV);
 #pragma unroll
                         for (int c = 0; c < kChunks; ++c)
                             tma_load_3d(sK + st * L::kTileKV + c * L::kChunkKV, &args.tm_ks, c * 64, col0, h,
                                         bar_k_full + st);
+                    } else {
+                        mbar_arrive(bar_k_full + st);
                     }
                 } else {
-#pragma unroll
-                    for (int c = 0; c < kChunks; ++c)
-                        tma_gather4_2d(sK + st * L::kTileKV + c * L::kChunkKV + lane * 512, &args.tm_kg, c * 64, r4[0],
-                                       r4[1], r4[2], r4[3], bar_k_full + st);
+                    gather_tile<D, kRPR>(smem_u32(sK + st * L::kTileKV), gk, col0 - args.S_pad, rsub, unit, args);
+                    close_fill(bar_k_full + st);
                 }
                 jk = jv + 1;
-                if (jv >= kStages)
+                if (jv >= kStages) {
                     ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_v_empty + st, ((jv / kStages) - 1) & 1, status));
+                    fence_proxy_async_smem();
+                }
                 if (!ok) break;
-                if (lane == 0) mbar_arrive_expect_tx(bar_v_full + st, L::kTileKV);
-                __syncwarp();
                 if (sink) {
-                    if (lane == 0) {
+                    if (t == 0) {
+                        mbar_arrive_expect_tx(bar_v_full + st, L::kTileKV);
 #pragma unroll
                         for (int c = 0; c < kChunks; ++c)
                             tma_load_3d(sV + st * L::kTileKV + c * L::kChunkKV, &args.tm_vs, c * 64, col0, h,
                                         bar_v_full + st);
+                    } else {
+                        mbar_arrive(bar_v_full + st);
                     }
                 } else {
-#pragma unroll
-                    for (int c = 0; c < kChunks; ++c)
-                        tma_gather4_2d(sV + st * L::kTileKV + c * L::kChunkKV + lane * 512, &args.tm_vg, c * 64, r4[0],
-                                       r4[1], r4[2], r4[3], bar_v_full + st);
+                    gather_tile<D, kRPR>(smem_u32(sV + st * L::kTileKV), gv, col0 - args.S_pad, rsub, unit, args);
+                    close_fill(bar_v_full + st);
                 }
             }
-            if (lane == 0) {
+            // no copy may still be landing in shared memory at exit
+            cp_async_commit();
+            cp_async_wait_group<0>();
+            if (t == 0) {
                 mbar_wait(bar_q, 0, status);
                 for (int jj = (jk - kStages > 0 ? jk - kStages : 0); jj < jk; ++jj)
                     mbar_wait(bar_k_full + jj % kStages, (jj / kStages) & 1, status);
                 for (int jj = (jv - kStages > 0 ? jv - kStages : 0); jj < jv; ++jj)
                     mbar_wait(bar_v_full + jj % kStages, (jj / kStages) & 1, status);
             }
-        } else if (warp == 0) {
+        } else if (warp == 0 && !gather) {
             // =========================== TMA producer
             if (lane == 0) {
                 const CUtensorMap* mq = tbuf ? &args.tm_qt : &args.tm_q;
@@ -527,6 +558,12 @@ __global__ void __launch_bounds__(threads_for<HALVES>(), 1) attn_fwd_kernel(cons
                 auto commit = [&](uint64_t* bar) {
                     if (leader) tc_commit(bar);
                 };
+                // after a wait: tcgen05 ordering, and with gathered tiles (generic-proxy
+                // cp.async writes) a proxy fence before the tensor cores read them
+                auto after_wait = [&]() {
+                    tc_fence_after();
+                    if (gather) fence_proxy_async_smem();
+                };
                 bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_q, 0, status));
                 if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_k_full, 0, status));
                 if constexpr (HALVES == 1) {
@@ -534,7 +571,7 @@ __global__ void __launch_bounds__(threads_for<HALVES>(), 1) attn_fwd_kernel(cons
                     // S(j+1) is issued before PV(j) and overlaps the softmax of tile j;
                     // the P-ready barrier is double-buffered the same way
                     if (ok) {
-                        tc_fence_after();
+                        after_wait();
                         issue_s(kColS, dq0, dk0);
                         commit(bar_s_full + 0);
                         commit(bar_k_empty + 0);
@@ -546,7 +583,7 @@ __global__ void __launch_bounds__(threads_for<HALVES>(), 1) attn_fwd_kernel(cons
                             ok = __all_sync(0xFFFFFFFFu,
                                             mbar_wait(bar_k_full + st1, ((j + 1) / kStages) & 1, status));
                             if (!ok) break;
-                            tc_fence_after();
+                            after_wait();
                             issue_s(kColS + 128 * ((j + 1) & 1), dq0, dk0 + st1 * kStageStep);
                             commit(bar_s_full + ((j + 1) & 1));
                             commit(bar_k_empty + st1);
@@ -554,14 +591,14 @@ __global__ void __launch_bounds__(threads_for<HALVES>(), 1) attn_fwd_kernel(cons
                         ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_v_full + st, (j / kStages) & 1, status));
                         if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_p_full + (j & 1), (j >> 1) & 1, status));
                         if (!ok) break;
-                        tc_fence_after();
+                        after_wait();
                         issue_pv(kColO, kColS + 128 * (j & 1), dv0 + st * kStageStep, j > 0);
                         commit(bar_o_done + 0);
                         commit(bar_v_empty + st);
                     }
                 } else {
                     if (ok) {
-                        tc_fence_after();
+                        after_wait();
                         issue_s(kColS, dq0, dk0);
                         commit(bar_s_full + 0);
                     }
@@ -577,7 +614,7 @@ __global__ void __launch_bounds__(threads_for<HALVES>(), 1) attn_fwd_kernel(cons
                         ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_v_full + st, (j / kStages) & 1, status));
                         if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_p_full + 0, j & 1, status));
                         if (!ok) break;
-                        tc_fence_after();
+                        after_wait();
                         issue_pv(kColO, kColS, dv, j > 0);
                         commit(bar_o_done + 0);
                         // S_0(j+1)
@@ -585,14 +622,14 @@ __global__ void __launch_bounds__(threads_for<HALVES>(), 1) attn_fwd_kernel(cons
                             const int st1 = (j + 1) % kStages;
                             ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_k_full + st1, ((j + 1) / kStages) & 1, status));
                             if (!ok) break;
-                            tc_fence_after();
+                            after_wait();
                             issue_s(kColS, dq0, dk0 + st1 * kStageStep);
                             commit(bar_s_full + 0);
                         }
                         // PV_1(j)
                         ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_p_full + 1, j & 1, status));
                         if (!ok) break;
-                        tc_fence_after();
+                        after_wait();
                         issue_pv(kColO + 128, kColS + 128, dv, j > 0);
                         commit(bar_o_done + 1);
                         commit(bar_v_empty + st);
@@ -932,13 +969,11 @@ bss_status launch_d(const AttnLaunch& a, cudaStream_t stream) {
     if ((st = encode_tmap_3d(&args.tm_ot, Ot, a.d, nq_rows, a.H, rs, rs * nq_rows, 64, kHalf)) != BSS_OK) return st;
     if ((st = encode_tmap_3d(&args.tm_ks, Kt, a.d, a.S, a.H, sink_rs, hs, 64, bkv)) != BSS_OK) return st;
     if ((st = encode_tmap_3d(&args.tm_vs, Vt, a.d, a.S, a.H, sink_rs, hs, 64, bkv)) != BSS_OK) return st;
-    if (a.fused == 1) {
-        const uint64_t rows = static_cast<uint64_t>(a.H) * static_cast<uint64_t>(a.N);
-        if (rows > 0x7FFFFFFFull) return set_error(BSS_ERR_UNSUPPORTED, "H*N too large for the fused permutation");
-        if ((st = encode_tmap_rows_2d(&args.tm_qg, a.Q, a.d, rows, rs, 64)) != BSS_OK) return st;
-        if ((st = encode_tmap_rows_2d(&args.tm_kg, a.K, a.d, rows, rs, 64)) != BSS_OK) return st;
-        if ((st = encode_tmap_rows_2d(&args.tm_vg, a.V, a.d, rows, rs, 64)) != BSS_OK) return st;
-    }
+    if (a.fused == 1 && static_cast<uint64_t>(a.H) * static_cast<uint64_t>(a.N) > 0x7FFFFFFFull)
+        return set_error(BSS_ERR_UNSUPPORTED, "H*N too large for the fused permutation");
+    args.q_rows = static_cast<const uint16_t*>(a.Q);
+    args.k_rows = static_cast<const uint16_t*>(a.K);
+    args.v_rows = static_cast<const uint16_t*>(a.V);
     args.o_rows = static_cast<uint16_t*>(a.O);
     args.fused = a.fused;
     args.route = a.route;

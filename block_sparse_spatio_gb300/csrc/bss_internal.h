@@ -123,9 +123,6 @@ int* device_status_ptr();  // per-device status word (device address)
 bss_status encode_tmap_3d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint64_t heads,
                           uint64_t row_stride_bytes, uint64_t head_stride_bytes, uint32_t box_inner,
                           uint32_t box_rows);
-// 2-D rows view (inner x rows) with a one-row box, for tile::gather4 loads
-bss_status encode_tmap_rows_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows,
-                               uint64_t row_stride_bytes, uint32_t box_inner);
 int num_sms();
 bss_status check_mask_params(const bss_mask_params* p);  // validation shared by the entry points
 

@@ -100,16 +100,24 @@ __device__ __forceinline__ void tma_load_3d(void* smem_dst, const CUtensorMap* m
         : "memory");
 }
 
-// Four rows (r0..r3, any order) of a 2-D tensor map whose box is one row high:
-// the rows land one after another at smem_dst (4 x box bytes), swizzled by
-// their shared-memory address like a tiled load of the same rows.
-__device__ __forceinline__ void tma_gather4_2d(void* smem_dst, const CUtensorMap* map, int32_t c0, int32_t r0,
-                                               int32_t r1, int32_t r2, int32_t r3, uint64_t* bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cta.global.tile::gather4.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_u32(smem_dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(smem_u32(bar))
-        : "memory");
+// 16-byte asynchronous copy global -> shared, cached in L2 only; completion is
+// tracked per thread by commit / wait groups.
+__device__ __forceinline__ void cp_async_16(uint32_t smem_dst, const void* gsrc) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_dst), "l"(gsrc) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+
+// Arrive on `bar` once every cp.async issued so far by this thread has
+// completed; the arrival counts toward the barrier's expected count (noinc).
+__device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint64_t* bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// Wait until at most N of this thread's committed groups are still in flight.
+template <int N>
+__device__ __forceinline__ void cp_async_wait_group() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 // 3-D tiled bulk tensor store shared -> global (rows outside the tensor are clipped).

@@ -226,8 +226,9 @@ bss_status bss_sparse_attention_split(const void* Q, const void* K, const void* 
  *               head_is_temporal[h] != 0 and a map built with
  *               temporal_permuted = 1 the kernel walks the permuted tile map
  *               and gathers its query / key rows (row s*F + f of the permuted
- *               order is row f*S + s of the input) with 4-row TMA gathers,
- *               and writes each output row to its (F,H,W) position.
+ *               order is row f*S + s of the input) with 16-byte cp.async
+ *               copies, and writes each output row to its (F,H,W) position.
+ *               Measured slower than bss_attention_step (permute first).
  *   lse         optional device float[H][N] in (F,H,W) order.
  * Results are bit-identical to bss_permute -> bss_sparse_attention ->
  * inverse bss_permute of O (and of lse) with the same flags.  H*N must be
