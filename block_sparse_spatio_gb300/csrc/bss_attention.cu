@@ -216,20 +216,19 @@ __device__ __forceinline__ RowPred row_pred(const AttnArgs& a, int code, int q) 
 //   boundary tile: the coordinate predicate (all masks are unions of <= 3
 //   intervals except the striped (F,H,W) temporal mask, one interval per frame);
 //   padding tile: the real-column predicate only;
-//   column-set tile: the map's bitmask of the tile (cmask: this q tile's
-//   sink-segment tiles, NW words each).
+//   column-set tile: the map's bitmask of the tile.
 template <int NW>
 __device__ __forceinline__ void tile_bits(uint32_t (&bits)[NW], const AttnArgs& a, int code, int cls, int c0,
-                                          const RowPred& rp, const uint32_t* cmask) {
-    if (cls == BSS_CLASS_COLUMNS) {
-        const uint32_t* m = cmask + (c0 / (NW * 32)) * NW;
-#pragma unroll
-        for (int w = 0; w < NW; ++w) bits[w] = __ldg(m + w);
-        return;
-    }
+                                          const RowPred& rp, int kind, int qt) {
 #pragma unroll
     for (int w = 0; w < NW; ++w) bits[w] = 0u;
-    if (cls == BSS_CLASS_PAD) {
+    if (cls >= BSS_CLASS_PAD) {
+        if (cls == BSS_CLASS_COLUMNS) {
+            const uint32_t* m = a.colmask[kind] + (static_cast<int64_t>(qt) * a.nsink + c0 / (NW * 32)) * NW;
+#pragma unroll
+            for (int w = 0; w < NW; ++w) bits[w] = __ldg(m + w);
+            return;
+        }
         if (code == MASK_TEMPORAL_VIRT) {
             add_interval(bits, 0, a.S, c0);
             add_interval(bits, a.S_pad, a.S_pad + a.N, c0);
@@ -314,7 +313,6 @@ __global__ void __launch_bounds__(threads_for<HALVES>(), 1) attn_fwd_kernel(cons
     bool tbuf = false;  // head with flag 1: its tensors come from the temporal-head buffers
     int qt, n;
     const int32_t* ents = nullptr;
-    const uint32_t* cmask = nullptr;  // this q tile's column bitmasks (tile-aligned permuted temporal maps)
     if constexpr (ROUTE) {
         vh = item / (args.nq * args.splits);
         const int rem = item - vh * args.nq * args.splits;
@@ -341,8 +339,6 @@ __global__ void __launch_bounds__(threads_for<HALVES>(), 1) attn_fwd_kernel(cons
             const int rb = __ldg(args.row_ptr[kind] + qt);
             n = __ldg(args.row_ptr[kind] + qt + 1) - rb;
             ents = args.entries[kind] + rb;
-            if (args.colmask[kind] != nullptr)
-                cmask = args.colmask[kind] + static_cast<int64_t>(qt) * args.nsink * kNW;
         }
     }
 
@@ -382,13 +378,18 @@ __global__ void __launch_bounds__(threads_for<HALVES>(), 1) attn_fwd_kernel(cons
         if (gather && (warp == 2 || warp == 3)) {
             // =========================== gather producer, fused permutation: the 64
             // threads of warps 2-3 copy Q and every band K / V tile row by row
-            // (gather_tile) with cp.async; each thread's arrival on the fill's
-            // barrier fires when its copies have landed (64 arrivals a fill), so
-            // the threads only ever wait for a free stage, as a TMA producer does.
-            // The copies are generic-proxy writes: the MMA issuer orders them
-            // before the tensor cores' reads with a proxy fence after its wait.
-            // Sink tiles (frame-0 keys, contiguous in (F,H,W) order) are one box
-            // load each (thread 0 arms the barrier, the others arrive).
+            // (gather_tile) with cp.async; each thread waits for its own copies,
+            // makes them visible to the tensor cores' (async) proxy and arrives on
+            // the fill's barrier (64 arrivals a fill), one fill behind the copies
+            // it issues, so that one fill's copies are in flight while the next is
+            // issued.  Measured for 10 temporal heads at 75.6K: 11.6 ms, the same
+            // as asynchronous arrivals (cp.async.mbarrier.arrive) with the proxy
+            // fence in the MMA issuer, which slowed the kernel's other paths, and
+            // faster than two fills in flight (13.8 ms).  Sink tiles (frame-0
+            // keys, contiguous in (F,H,W) order) are one box load each (thread 0
+            // arms the barrier, the others arrive); the fill still pending is
+            // completed before one, because the producer may then wait for a stage
+            // that only that fill's consumption frees.
             constexpr int kUnits = D / 8;  // 16-byte units per row
             constexpr int kRPR = kGatherThreads / kUnits;
             const int t = static_cast<int>(threadIdx.x) - kGatherThread0;
@@ -397,9 +398,22 @@ __global__ void __launch_bounds__(threads_for<HALVES>(), 1) attn_fwd_kernel(cons
             const uint16_t* gq = args.q_rows + head_off;
             const uint16_t* gk = args.k_rows + head_off;
             const uint16_t* gv = args.v_rows + head_off;
-            // the barrier gets this thread's arrival when its copies so far have
-            // landed: the thread goes on to the next fill without waiting
-            auto close_fill = [&](uint64_t* bar) { cp_async_mbar_arrive_noinc(bar); };
+            uint64_t* pending = nullptr;
+            auto complete_pending = [&](bool keep_newest) {
+                if (pending == nullptr) return;
+                if (keep_newest)
+                    cp_async_wait_group<1>();
+                else
+                    cp_async_wait_group<0>();
+                fence_proxy_async_smem();
+                mbar_arrive(pending);
+                pending = nullptr;
+            };
+            auto close_fill = [&](uint64_t* bar) {  // after issuing a gathered fill
+                cp_async_commit();
+                complete_pending(true);
+                pending = bar;
+            };
             if (t == 0) {
                 tma_prefetch_desc(&args.tm_ks);
                 tma_prefetch_desc(&args.tm_vs);
@@ -415,6 +429,7 @@ __global__ void __launch_bounds__(threads_for<HALVES>(), 1) attn_fwd_kernel(cons
                 const uint32_t e = entry_at<ROUTE, BKV>(args, ents, jv, code, j0);
                 const int col0 = static_cast<int>(e & BSS_TILE_INDEX_MASK) * BKV;
                 const bool sink = col0 < args.S_pad;
+                if (sink) complete_pending(false);
                 if (jv >= kStages) {
                     ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_k_empty + st, ((jv / kStages) - 1) & 1, status));
                     // the tensor cores' reads of the stage come before these writes
@@ -457,7 +472,7 @@ __global__ void __launch_bounds__(threads_for<HALVES>(), 1) attn_fwd_kernel(cons
                 }
             }
             // no copy may still be landing in shared memory at exit
-            cp_async_commit();
+            complete_pending(false);
             cp_async_wait_group<0>();
             if (t == 0) {
                 mbar_wait(bar_q, 0, status);
@@ -558,12 +573,7 @@ __global__ void __launch_bounds__(threads_for<HALVES>(), 1) attn_fwd_kernel(cons
                 auto commit = [&](uint64_t* bar) {
                     if (leader) tc_commit(bar);
                 };
-                // after a wait: tcgen05 ordering, and with gathered tiles (generic-proxy
-                // cp.async writes) a proxy fence before the tensor cores read them
-                auto after_wait = [&]() {
-                    tc_fence_after();
-                    if (gather) fence_proxy_async_smem();
-                };
+
                 bool ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_q, 0, status));
                 if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_k_full, 0, status));
                 if constexpr (HALVES == 1) {
@@ -571,7 +581,7 @@ __global__ void __launch_bounds__(threads_for<HALVES>(), 1) attn_fwd_kernel(cons
                     // S(j+1) is issued before PV(j) and overlaps the softmax of tile j;
                     // the P-ready barrier is double-buffered the same way
                     if (ok) {
-                        after_wait();
+                        tc_fence_after();
                         issue_s(kColS, dq0, dk0);
                         commit(bar_s_full + 0);
                         commit(bar_k_empty + 0);
@@ -583,7 +593,7 @@ __global__ void __launch_bounds__(threads_for<HALVES>(), 1) attn_fwd_kernel(cons
                             ok = __all_sync(0xFFFFFFFFu,
                                             mbar_wait(bar_k_full + st1, ((j + 1) / kStages) & 1, status));
                             if (!ok) break;
-                            after_wait();
+                            tc_fence_after();
                             issue_s(kColS + 128 * ((j + 1) & 1), dq0, dk0 + st1 * kStageStep);
                             commit(bar_s_full + ((j + 1) & 1));
                             commit(bar_k_empty + st1);
@@ -591,14 +601,14 @@ __global__ void __launch_bounds__(threads_for<HALVES>(), 1) attn_fwd_kernel(cons
                         ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_v_full + st, (j / kStages) & 1, status));
                         if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_p_full + (j & 1), (j >> 1) & 1, status));
                         if (!ok) break;
-                        after_wait();
+                        tc_fence_after();
                         issue_pv(kColO, kColS + 128 * (j & 1), dv0 + st * kStageStep, j > 0);
                         commit(bar_o_done + 0);
                         commit(bar_v_empty + st);
                     }
                 } else {
                     if (ok) {
-                        after_wait();
+                        tc_fence_after();
                         issue_s(kColS, dq0, dk0);
                         commit(bar_s_full + 0);
                     }
@@ -614,7 +624,7 @@ __global__ void __launch_bounds__(threads_for<HALVES>(), 1) attn_fwd_kernel(cons
                         ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_v_full + st, (j / kStages) & 1, status));
                         if (ok) ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_p_full + 0, j & 1, status));
                         if (!ok) break;
-                        after_wait();
+                        tc_fence_after();
                         issue_pv(kColO, kColS, dv, j > 0);
                         commit(bar_o_done + 0);
                         // S_0(j+1)
@@ -622,14 +632,14 @@ __global__ void __launch_bounds__(threads_for<HALVES>(), 1) attn_fwd_kernel(cons
                             const int st1 = (j + 1) % kStages;
                             ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_k_full + st1, ((j + 1) / kStages) & 1, status));
                             if (!ok) break;
-                            after_wait();
+                            tc_fence_after();
                             issue_s(kColS, dq0, dk0 + st1 * kStageStep);
                             commit(bar_s_full + 0);
                         }
                         // PV_1(j)
                         ok = __all_sync(0xFFFFFFFFu, mbar_wait(bar_p_full + 1, j & 1, status));
                         if (!ok) break;
-                        after_wait();
+                        tc_fence_after();
                         issue_pv(kColO + 128, kColS + 128, dv, j > 0);
                         commit(bar_o_done + 1);
                         commit(bar_v_empty + st);
@@ -747,7 +757,7 @@ __global__ void __launch_bounds__(threads_for<HALVES>(), 1) attn_fwd_kernel(cons
                     done = single_pass(std::integral_constant<bool, false>(), none);
                 } else {
                     uint32_t bits[4];
-                    tile_bits<kNW>(*reinterpret_cast<uint32_t(*)[kNW]>(bits), args, code, cls, c0, rp, cmask);
+                    tile_bits<kNW>(*reinterpret_cast<uint32_t(*)[kNW]>(bits), args, code, cls, c0, rp, tbuf ? 1 : 0, qt);
                     done = single_pass(std::integral_constant<bool, true>(), bits);
                 }
             } else if constexpr (ROUTE) {
@@ -758,7 +768,7 @@ __global__ void __launch_bounds__(threads_for<HALVES>(), 1) attn_fwd_kernel(cons
                 // sending the whole warp to the two-pass path on every tile.
                 if (cls != BSS_CLASS_FULL) {
                     uint32_t bits[4];
-                    tile_bits<kNW>(*reinterpret_cast<uint32_t(*)[kNW]>(bits), args, code, cls, c0, rp, cmask);
+                    tile_bits<kNW>(*reinterpret_cast<uint32_t(*)[kNW]>(bits), args, code, cls, c0, rp, tbuf ? 1 : 0, qt);
                     uint32_t any = 0u;
 #pragma unroll
                     for (int w = 0; w < kNW; ++w) any |= bits[w];
@@ -772,7 +782,7 @@ __global__ void __launch_bounds__(threads_for<HALVES>(), 1) attn_fwd_kernel(cons
                 // pass 2 exponentiates and writes P chunk by chunk.
                 uint32_t bits[4] = {0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu};
                 if (cls != BSS_CLASS_FULL)
-                    tile_bits<kNW>(*reinterpret_cast<uint32_t(*)[kNW]>(bits), args, code, cls, c0, rp, cmask);
+                    tile_bits<kNW>(*reinterpret_cast<uint32_t(*)[kNW]>(bits), args, code, cls, c0, rp, tbuf ? 1 : 0, qt);
                 float mx[8];
 #pragma unroll
                 for (int t = 0; t < 8; ++t) mx[t] = -INFINITY;

@@ -108,12 +108,6 @@ __device__ __forceinline__ void cp_async_16(uint32_t smem_dst, const void* gsrc)
 
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 
-// Arrive on `bar` once every cp.async issued so far by this thread has
-// completed; the arrival counts toward the barrier's expected count (noinc).
-__device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint64_t* bar) {
-    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
 // Wait until at most N of this thread's committed groups are still in flight.
 template <int N>
 __device__ __forceinline__ void cp_async_wait_group() {
