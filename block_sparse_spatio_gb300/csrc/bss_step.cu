@@ -15,8 +15,10 @@
 // two copy streams, and every call copies its inputs in, computes and copies O
 // out in groups of heads (heads are independent), so that a group's kernels
 // start while the next group is still being copied and the copies of one call
-// overlap the kernels of the previous one.  Every copy is one cudaMemcpyAsync;
-// events order the three streams.
+// overlap the kernels of the previous one.  Odd groups compute on a second
+// stream, so a group's launches can start on the SMs that the previous group's
+// attention leaves idle at its end.  Every copy is one cudaMemcpyAsync; events
+// order the four streams.
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -50,6 +52,10 @@ struct bss_step_workspace_s {
     uint64_t magic;
     int32_t H, N, d, F, S, device, depth, group, ngroups, next;
     cudaStream_t copy_in = nullptr, copy_out = nullptr;
+    // odd head groups run on this stream, even ones on the caller's, so that a
+    // group's kernels can start while the previous group's attention drains
+    cudaStream_t compute2 = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
     std::vector<StepSet> sets;
 };
 
@@ -63,6 +69,7 @@ bool ws_is_live(const bss_step_workspace w) {
 void free_workspace(bss_step_workspace w) {
     if (w->copy_in) cudaStreamSynchronize(w->copy_in);
     if (w->copy_out) cudaStreamSynchronize(w->copy_out);
+    if (w->compute2) cudaStreamSynchronize(w->compute2);
     for (StepSet& s : w->sets) {
         if (s.free_ev) cudaEventSynchronize(s.free_ev);
         for (void* p : {s.Q, s.K, s.V, s.O, s.Qp, s.Kp, s.Vp})
@@ -76,6 +83,9 @@ void free_workspace(bss_step_workspace w) {
     }
     if (w->copy_in) cudaStreamDestroy(w->copy_in);
     if (w->copy_out) cudaStreamDestroy(w->copy_out);
+    if (w->compute2) cudaStreamDestroy(w->compute2);
+    if (w->fork) cudaEventDestroy(w->fork);
+    if (w->join) cudaEventDestroy(w->join);
     w->magic = 0;
     delete w;
 }
@@ -141,9 +151,12 @@ bss_status bss_step_workspace_create(const bss_mask_params* params, int32_t H, i
         return s;
     };
     if (cudaStreamCreateWithFlags(&w->copy_in, cudaStreamNonBlocking) != cudaSuccess ||
-        cudaStreamCreateWithFlags(&w->copy_out, cudaStreamNonBlocking) != cudaSuccess) {
+        cudaStreamCreateWithFlags(&w->copy_out, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaStreamCreateWithFlags(&w->compute2, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&w->fork, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&w->join, cudaEventDisableTiming) != cudaSuccess) {
         (void)cudaGetLastError();
-        return fail(set_error(BSS_ERR_CUDA, "copy stream creation failed"));
+        return fail(set_error(BSS_ERR_CUDA, "stream or event creation failed"));
     }
     w->sets.resize(depth);
     for (StepSet& s : w->sets) {
@@ -226,6 +239,11 @@ bss_status bss_attention_step_host(const void* hQ, const void* hK, const void* h
     // the set's previous call must be done with it: its kernels read Q, K, V and
     // its D2H copy reads O
     if (s.used) BSS_TRY(cudaStreamWaitEvent(ws->copy_in, s.free_ev, 0), "wait for the buffer set");
+    // the second compute stream starts after the caller's work so far
+    if (ws->ngroups > 1) {
+        BSS_TRY(cudaEventRecord(ws->fork, stream), "record fork");
+        BSS_TRY(cudaStreamWaitEvent(ws->compute2, ws->fork, 0), "fork the second compute stream");
+    }
     BSS_TRY(cudaMemcpyAsync(s.flags, h_head_is_temporal, static_cast<size_t>(ws->H), cudaMemcpyHostToDevice,
                             ws->copy_in),
             "copy flags");
@@ -240,13 +258,19 @@ bss_status bss_attention_step_host(const void* hQ, const void* hK, const void* h
         BSS_TRY(cudaMemcpyAsync(at_mut(s.K), at(hK), n, cudaMemcpyHostToDevice, ws->copy_in), "copy K in");
         BSS_TRY(cudaMemcpyAsync(at_mut(s.V), at(hV), n, cudaMemcpyHostToDevice, ws->copy_in), "copy V in");
         BSS_TRY(cudaEventRecord(s.ready[g], ws->copy_in), "record inputs ready");
-        BSS_TRY(cudaStreamWaitEvent(stream, s.ready[g], 0), "wait for inputs");
+        cudaStream_t cs = (g & 1) ? ws->compute2 : stream;
+        BSS_TRY(cudaStreamWaitEvent(cs, s.ready[g], 0), "wait for inputs");
         if ((st = step_device(at(s.Q), at(s.K), at(s.V), at_mut(s.O), nullptr, map, s.flags + h0, h1 - h0,
-                              at_mut(s.Qp), at_mut(s.Kp), at_mut(s.Vp), stream)) != BSS_OK)
+                              at_mut(s.Qp), at_mut(s.Kp), at_mut(s.Vp), cs)) != BSS_OK)
             return st;
-        BSS_TRY(cudaEventRecord(s.done[g], stream), "record outputs done");
+        BSS_TRY(cudaEventRecord(s.done[g], cs), "record outputs done");
         BSS_TRY(cudaStreamWaitEvent(ws->copy_out, s.done[g], 0), "wait for outputs");
         BSS_TRY(cudaMemcpyAsync(at_mut(hO), at(s.O), n, cudaMemcpyDeviceToHost, ws->copy_out), "copy O out");
+    }
+    // the caller's stream is ordered after every group's kernels
+    if (ws->ngroups > 1) {
+        BSS_TRY(cudaEventRecord(ws->join, ws->compute2), "record join");
+        BSS_TRY(cudaStreamWaitEvent(stream, ws->join, 0), "join the second compute stream");
     }
     BSS_TRY(cudaEventRecord(s.free_ev, ws->copy_out), "record set free");
     if (done != nullptr) BSS_TRY(cudaEventRecord(done, ws->copy_out), "record done");

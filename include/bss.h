@@ -314,9 +314,12 @@ bss_status bss_step_workspace_wait_stream(bss_step_workspace ws, cudaStream_t st
  * h_head_is_temporal: host uint8[H] flags, copied each call.  Host buffers
  * should be page-locked (cudaHostAlloc / cudaHostRegister): pageable memory
  * works, but its copies do not overlap anything.  Per group of heads: H2D
- * copies of Q, K, V on the workspace's copy-in stream, the step's kernels on
- * `stream` once they have landed, the D2H copy of O on the copy-out stream
- * once they are done.  Returns once everything is enqueued; `done` (optional,
+ * copies of Q, K, V on the workspace's copy-in stream, the step's kernels once
+ * they have landed (even groups on `stream`, odd groups on a workspace stream
+ * that starts after `stream`'s earlier work, so that a group's kernels can
+ * start while the previous group's drain; `stream` is ordered after all of
+ * them when the call returns), the D2H copy of O on the copy-out stream once
+ * they are done.  Returns once everything is enqueued; `done` (optional,
  * a caller-created event) is recorded after the last D2H copy: do not read hO,
  * or change the inputs, before it completes.  The map must be of the
  * workspace's geometry (H, N, d).  Not thread-safe per workspace.
