@@ -62,6 +62,8 @@ def parse_args():
                          "profiling runs")
     ap.add_argument("--cpu-rows-per-head", type=int, default=6144,
                     help="oracle sample of the cpu_baseline entry (about 20 s on 16 cores)")
+    ap.add_argument("--cpu-rows-per-head-1core", type=int, default=64,
+                    help="oracle sample of the cpu_baseline's one-core figure")
     ap.add_argument("--ref-rows-per-head", type=int, default=256,
                     help="oracle sample per step of --impl reference")
     return ap.parse_args()
@@ -845,13 +847,25 @@ def cpu_baseline(w, Q, K, V, flags, args, flops):
     import oracle
     H = Q.shape[0]
     q, k, v = (x.cpu() for x in (Q, K, V))
+    cores = oracle.num_threads()
     dt, nrows = oracle_sample(w, q, k, v, flags, args.cpu_rows_per_head, seed=2000)
     rows_total = H * w.N
     full_s = dt * rows_total / nrows
-    return {"value": flops / full_s / 1e12, "unit": UNIT, "cores": oracle.num_threads(), "kind": "oracle",
+    # the same oracle on one core, a smaller sample
+    oracle.set_num_threads(1)
+    try:
+        dt1, nrows1 = oracle_sample(w, q, k, v, flags, args.cpu_rows_per_head_1core, seed=3000)
+    finally:
+        oracle.set_num_threads(cores)
+    full_s1 = dt1 * rows_total / nrows1
+    return {"value": flops / full_s / 1e12, "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": f"{args.cpu_rows_per_head} seeded query rows per head x {H} heads "
                       f"({100.0 * nrows / rows_total:.2f}% of rows, {dt:.1f} s), time scaled to all rows",
-            "seconds_full_workload_extrapolated": full_s}
+            "seconds_full_workload_extrapolated": full_s,
+            "single_core": {"value": flops / full_s1 / 1e12, "unit": UNIT, "cores": 1,
+                            "sample": f"{args.cpu_rows_per_head_1core} seeded query rows per head x {H} heads "
+                                      f"({dt1:.1f} s), time scaled to all rows",
+                            "seconds_full_workload_extrapolated": full_s1}}
 
 
 if __name__ == "__main__":

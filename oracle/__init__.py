@@ -74,12 +74,19 @@ def _load():
         lib.orc_attention.argtypes = [p, p, p, i64, ctypes.c_int, ctypes.POINTER(_Geom), ctypes.c_double,
                                       p, i64, i64, p, i64, p, p]
         lib.orc_num_threads.restype = ctypes.c_int
+        lib.orc_set_num_threads.restype = None
+        lib.orc_set_num_threads.argtypes = [ctypes.c_int]
         _lib = lib
     return _lib
 
 
 def num_threads() -> int:
     return int(_load().orc_num_threads())
+
+
+def set_num_threads(n: int) -> None:
+    """Threads the oracle's parallel loops use from now on."""
+    _load().orc_set_num_threads(int(n))
 
 
 class Geometry:

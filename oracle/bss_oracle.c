@@ -59,6 +59,15 @@ int orc_num_threads(void) {
 #endif
 }
 
+/* Threads of the parallel loops that follow (timing on fewer cores). */
+void orc_set_num_threads(int n) {
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
 /* Token permutation (F,H,W) -> (H,W,F): the blog's section "Arrange tokens for
  * efficient temporal access" and Figure 9.  Token t = f*S + s goes to p = s*F + f. */
 int64_t orc_perm_index(int64_t t, int64_t F, int64_t S) {
