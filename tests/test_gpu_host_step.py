@@ -121,3 +121,37 @@ def test_host_steps_at_full_size_match_device_step(bss):
         for c in range(calls):
             assert torch.equal(outs[c].view(torch.int16), expect[c].view(torch.int16)), f"call {c}"
         wsp.destroy()
+
+
+@pytest.mark.gpu
+def test_device_step_without_flags_or_permutation_is_plain_attention(bss):
+    # bss_attention_step falls back to one sparse-attention launch when nothing
+    # is permuted: no flags (every head spatial), or a map that keeps temporal
+    # heads in (F,H,W) order; bit for bit the direct call in both cases, and the
+    # host-buffer step on such a map gives the same O
+    w = W.SMALL
+    H = 3
+    dev = torch.device("cuda")
+    q, k, v = W.qkv(w, H=H, seed=41)
+    Q, K, V = (x.to(dev) for x in (q, k, v))
+    for tperm, flags in ((1, None), (0, [1, 0, 1])):
+        p = bss.MaskParams(w.F, w.Hs, w.Ws, w.d, w.wf, w.ws, temporal_permuted=tperm)
+        fl = None if flags is None else torch.tensor(flags, dtype=torch.uint8, device=dev)
+        with bss.build_tile_map(p) as tm:
+            O1, O2 = torch.empty_like(Q), torch.empty_like(Q)
+            l1 = torch.empty(H, w.N, device=dev)
+            l2 = torch.empty(H, w.N, device=dev)
+            bss.attention_step(Q, K, V, O1, tm, fl, None, None, None, lse=l1)
+            bss.sparse_attention(Q, K, V, O2, tm, fl, lse=l2)
+            torch.cuda.synchronize()
+            assert bss.get_device_status() == 0
+            assert torch.equal(O1.view(torch.int16), O2.view(torch.int16))
+            assert torch.equal(l1.view(torch.int32), l2.view(torch.int32))
+            if flags is not None:
+                with bss.step_workspace(p, H, depth=2, heads_per_group=2) as wsp:
+                    hq, hk, hv = (x.pin_memory() for x in (q, k, v))
+                    ho = torch.empty_like(hq).pin_memory()
+                    e = bss.attention_step_host(hq, hk, hv, ho, tm, torch.tensor(flags, dtype=torch.uint8), wsp)
+                    e.synchronize()
+                    torch.cuda.synchronize()
+                assert torch.equal(ho.view(torch.int16), O1.cpu().view(torch.int16))
