@@ -64,7 +64,8 @@ def test_exact_mask_coverage_every_row_every_head(bss, case):
 
 @pytest.mark.gpu
 @pytest.mark.parametrize("BQ", [128, 256])
-def test_rounded_mask_coverage_small_is_distinct_keys(bss, BQ):
+@pytest.mark.parametrize("BKV", [128, 64])
+def test_rounded_mask_coverage_small_is_distinct_keys(bss, BQ, BKV):
     wl = W.SMALL
     dev = torch.device("cuda")
     g = torch.Generator(device=dev).manual_seed(91)
@@ -75,15 +76,15 @@ def test_rounded_mask_coverage_small_is_distinct_keys(bss, BQ):
     O = torch.empty_like(Q)
     lse = torch.empty(2, wl.N, device=dev)
     p = bss.MaskParams(wl.F, wl.Hs, wl.Ws, wl.d, wl.wf, wl.ws, temporal_permuted=1, rounding=1)
-    with bss.build_tile_map(p, BQ=BQ) as tm:
+    with bss.build_tile_map(p, BQ=BQ, BKV=BKV) as tm:
         assert tm.stats(1)["columns"] > 0  # sink tiles that lose their band twins
         bss.attention_step(Q, K, V, O, tm, fl, *[torch.empty_like(Q) for _ in range(3)], lse=lse)
         torch.cuda.synchronize()
     assert bss.get_device_status() == 0
     go = oracle.Geometry(wl.F, wl.Hs, wl.Ws, wf=wl.wf, ws=wl.ws)
     got = lse.double().cpu().numpy()
-    want0 = rounded_row_counts(oracle.SPATIAL, go, BQ, 128)
-    want1 = rounded_row_counts(oracle.TEMPORAL_PERMUTED, go, BQ, 128)   # layout order
+    want0 = rounded_row_counts(oracle.SPATIAL, go, BQ, BKV)
+    want1 = rounded_row_counts(oracle.TEMPORAL_PERMUTED, go, BQ, BKV)   # layout order
     np.testing.assert_array_equal(_counts_of(got[0]), want0)
     np.testing.assert_array_equal(_counts_of(got[1]), want1)
 
