@@ -17,7 +17,7 @@ import workloads as W
 from _util import exact_row_counts, fhw_of_layout, rounded_row_counts
 
 
-def _zero_query_step(bss, wl, tperm, rounding, H=None, seed=None):
+def _zero_query_step(bss, wl, tperm, rounding, H=None, seed=None, BQ=None, BKV=None):
     """Run the step with Q = 0 and seeded K, V on the device; LSE per head in
     (F,H,W) token order (float64, CPU)."""
     dev = torch.device("cuda")
@@ -32,7 +32,7 @@ def _zero_query_step(bss, wl, tperm, rounding, H=None, seed=None):
     lse = torch.empty(H, wl.N, device=dev)
     ws = [torch.empty_like(Q) for _ in range(3)]
     p = bss.MaskParams(wl.F, wl.Hs, wl.Ws, wl.d, wl.wf, wl.ws, temporal_permuted=tperm, rounding=rounding)
-    with bss.build_tile_map(p) as tm:
+    with bss.build_tile_map(p, BQ=BQ or bss.ATTN_BQ, BKV=BKV or bss.ATTN_BKV) as tm:
         bss.attention_step(Q, K, V, O, tm, fl, *ws, lse=lse)
         torch.cuda.synchronize()
     assert bss.get_device_status() == 0
@@ -60,6 +60,40 @@ def test_exact_mask_coverage_every_row_every_head(bss, case):
         got = _counts_of(lse[h])
         bad = np.nonzero(got != exp)[0]
         assert bad.size == 0, f"{name} head {h}: {bad.size} rows differ, first {bad[:8]}"
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("tile", [(128, 128), (256, 64), (128, 64)], ids=lambda t: f"{t[0]}x{t[1]}")
+def test_exact_mask_coverage_every_row_other_tiles_75k(bss, tile):
+    # the other kernel instances (one 128-row half per CTA, 64-key tiles) at the
+    # benchmark's size, both head kinds, every row
+    wl = W.MIXED_75K
+    BQ, BKV = tile
+    flags, lse = _zero_query_step(bss, wl, 1, 0, BQ=BQ, BKV=BKV)
+    want = {k: exact_row_counts(k, wl.F, wl.S, wl.wf, wl.ws) for k in (oracle.SPATIAL, oracle.TEMPORAL_FHW)}
+    for h, fl in enumerate(flags):
+        got = _counts_of(lse[h])
+        bad = np.nonzero(got != want[oracle.TEMPORAL_FHW if fl else oracle.SPATIAL])[0]
+        assert bad.size == 0, f"{tile} head {h}: {bad.size} rows differ, first {bad[:8]}"
+
+
+@pytest.mark.gpu
+def test_dense_control_coverage_every_row(bss):
+    # Q = 0: every row of the dense control keeps all N keys, also through the
+    # ragged last kv tile (75,600 = 590 x 128 + 80)
+    wl = W.MIXED_75K
+    dev = torch.device("cuda")
+    g = torch.Generator(device=dev).manual_seed(17)
+    K = torch.randn(wl.H, wl.N, wl.d, generator=g, device=dev).to(torch.bfloat16)
+    V = torch.randn(wl.H, wl.N, wl.d, generator=g, device=dev).to(torch.bfloat16)
+    Q = torch.zeros_like(K)
+    O = torch.empty_like(Q)
+    lse = torch.empty(wl.H, wl.N, device=dev)
+    bss.dense_attention(Q, K, V, O, lse=lse)
+    torch.cuda.synchronize()
+    assert bss.get_device_status() == 0
+    got = _counts_of(lse.double().cpu().numpy())
+    assert np.all(got == wl.N), np.nonzero(got != wl.N)
 
 
 @pytest.mark.gpu
