@@ -94,3 +94,51 @@ def test_routing_writes_only_its_outputs(bss):
     assert bss.get_device_status() == 0
     assert intact(fbuf, 9) and intact(ebuf, -3.0)
     assert set(flags.cpu().tolist()) <= {0, 1}
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("geom", GEOMS, ids=["s63_d64", "s130_d128", "one_token", "n100"])
+@pytest.mark.parametrize("rounding", [0, 1])
+def test_step_writes_only_its_output_and_workspaces(bss, geom, rounding):
+    # bss_attention_step writes O and the temporal heads' rows of the three
+    # permutation workspaces (one launch), nothing around them; tile-aligned
+    # maps include column-masked sink tiles where the geometry has them
+    F, Hs, Ws, d, wf, ws, flags = geom
+    N, H = F * Hs * Ws, len(flags)
+    dev = torch.device("cuda")
+    q, k, v = W.qkv(W.SMALL, H=H, N=N, d=d, seed=73)
+    Q, K, V = (x.to(dev) for x in (q, k, v))
+    fl = torch.tensor(flags, dtype=torch.uint8, device=dev)
+    sent = -7.0
+    obuf, O = guarded((H, N, d), torch.bfloat16, sent, dev)
+    wbufs = [guarded((H, N, d), torch.bfloat16, sent, dev) for _ in range(3)]
+    p = bss.MaskParams(F, Hs, Ws, d, wf, ws, rounding=rounding)
+    with bss.build_tile_map(p) as tm:
+        bss.attention_step(Q, K, V, O, tm, fl, *[w[1] for w in wbufs])
+        torch.cuda.synchronize()
+    assert bss.get_device_status() == 0
+    assert intact(obuf, sent)
+    for buf, wsp in wbufs:
+        assert intact(buf, sent)
+        for h, f in enumerate(flags):
+            if not f:
+                assert torch.all(wsp[h] == sent)  # spatial heads are never copied
+    assert torch.isfinite(O.float()).all()
+
+
+@pytest.mark.gpu
+def test_multi_permute_writes_only_its_outputs(bss):
+    F, Hs, Ws, d = 3, 10, 13, 128
+    N = F * Hs * Ws
+    dev = torch.device("cuda")
+    xs = [torch.randn(3, N, d, device=dev).to(torch.bfloat16) for _ in range(3)]
+    fl = torch.tensor([1, 0, 1], dtype=torch.uint8, device=dev)
+    sent = 5.0
+    outs = [guarded((3, N, d), torch.bfloat16, sent, dev) for _ in range(3)]
+    p = bss.MaskParams(F, Hs, Ws, d, 1, 1)
+    for inverse in (False, True):
+        bss.permute_flagged_multi(xs, [o[1] for o in outs], fl, p, inverse)
+        torch.cuda.synchronize()
+        for buf, out in outs:
+            assert intact(buf, sent)
+            assert torch.all(out[1] == sent)
