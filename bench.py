@@ -13,10 +13,12 @@ before timing (it depends only on the geometry, as on the pages).
 
 value = effective TFLOP/s = 4 * d * (retained query-key pairs, all heads) /
 step time; ms_per_step is the step time.  Extra keys report the attention
-kernel alone, its roofline against the measured bf16 peak, the dense control,
-the tile-aligned (B3) and the no-permutation variants, the permutation
-bandwidth, an end-to-end number through host buffers, and the fp64 oracle on
-the host cores.
+kernel alone, its roofline against the measured bf16 peak (over the timed
+steps, and again as a burst after idle and sustained for seconds at the
+board's power limit, each against the peak measured in that regime), the
+dense control, the tile-aligned (B3) and the no-permutation variants, the
+permutation bandwidth, an end-to-end number through host buffers, and the fp64
+oracle on the host cores.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 """
@@ -516,6 +518,11 @@ def main():
     line["roofline"] = {"bound": "tensor", "achieved": attn_tflops, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                         "frac": attn_tflops / peaks["bf16_tflops"], "traffic": traffic,
                         "peak_source": f"{peak_src} bf16 burst (cuBLAS 8192^3)", "kernel": "attn_fwd_kernel<128, false, 2>"}
+    if not args.dense and not args.no_extras and rank == 0:
+        # the timed region above sits on the power ramp (the board reaches its
+        # limit after ~0.1-0.5 s of load); these two legs time the kernel at
+        # either end of it, each against the peak measured in the same regime
+        line["roofline"].update(power_regimes(bss, torch, Q, K, V, O, Qp, Kp, Vp, tm, fl, flops, peaks, local_rank))
 
     if not args.no_extras and rank == 0:
         line["variants"] = variants(bss, torch, W, w, H, Q, K, V, dev, peaks, flags)
@@ -584,6 +591,60 @@ def _time_interleaved(torch, fns, rounds=9, warm=2):
             ev[n].append((a, b))
     torch.cuda.synchronize()
     return {n: statistics.median(a.elapsed_time(b) for a, b in ev[n]) for n in names}
+
+
+def power_regimes(bss, torch, Q, K, V, O, Qp, Kp, Vp, tm, fl, flops, peaks, local_rank, sustain_s=3.0):
+    """The attention kernel in the two regimes the two measured peaks describe.
+
+    burst: one launch after 0.5 s with the GPU idle (median of 3), against the
+    burst peak (a short cuBLAS GEMM run).  sustained: launches back to back for
+    about `sustain_s` seconds, the mean over the second half (after the power
+    controller has settled at the board's limit), against the sustained peak
+    (cuBLAS back to back for seconds), with the clocks of that half.  Qp, Kp, Vp
+    already hold the step's permuted temporal heads."""
+    def attn():
+        bss.sparse_attention_split(Q, K, V, O, Qp, Kp, Vp, None, tm, fl)
+
+    s = torch.cuda.current_stream()
+    burst = []
+    for _ in range(3):
+        torch.cuda.synchronize()
+        time.sleep(0.5)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(s)
+        attn()
+        b.record(s)
+        torch.cuda.synchronize()
+        burst.append(a.elapsed_time(b))
+    burst_ms = statistics.median(burst)
+
+    half = max(4, int(sustain_s / 2 / (burst_ms * 1e-3)))
+    for _ in range(half):
+        attn()
+    torch.cuda.synchronize()
+    sampler = clock_sampler(torch, local_rank)
+    sampler.start()
+    time.sleep(0.05)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler.mark_begin()
+    a.record(s)
+    for _ in range(half):
+        attn()
+    b.record(s)
+    torch.cuda.synchronize()
+    sampler.mark_end()
+    clocks = sampler.stop()
+    sus_ms = a.elapsed_time(b) / half
+    status = bss.get_device_status()
+    if status != 0:
+        raise RuntimeError(f"device status {bss.status_string(status)} in the power-regime runs")
+    bt, st = flops / (burst_ms * 1e-3) / 1e12, flops / (sus_ms * 1e-3) / 1e12
+    return {"burst": {"ms": burst_ms, "achieved": bt, "peak": peaks["bf16_tflops"], "frac": bt / peaks["bf16_tflops"],
+                      "how": "one launch after 0.5 s idle, median of 3; peak: cuBLAS bf16 burst"},
+            "sustained": {"ms": sus_ms, "achieved": st, "peak": peaks["bf16_tflops_sustained"],
+                          "frac": st / peaks["bf16_tflops_sustained"], "launches": half, "clocks": clocks,
+                          "how": f"{2 * half} launches back to back (about {2 * half * sus_ms / 1e3:.1f} s), mean of "
+                                 f"the second half; peak: cuBLAS bf16 back to back for seconds"}}
 
 
 def dense_control(bss, torch, Q, K, V, O, Qp, Kp, Vp, tm, fl, retained, peaks, rounds=7):

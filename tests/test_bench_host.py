@@ -1,6 +1,7 @@
 """Host-side logic of bench.py, without a GPU: the clock record parsed from
 nvidia-smi lines, the staleness rule of the committed DRAM-traffic figure, the
-code-only hash it rests on, and the whole-job throughput."""
+code-only hash it rests on, the whole-job throughput, and the burst / sustained
+legs of the roofline (against a fake device clock)."""
 import datetime
 
 import pytest
@@ -112,3 +113,101 @@ def test_nvml_sampler_without_the_driver_falls_back():
                 def get_device_properties(i):
                     raise RuntimeError("no GPU")
         assert isinstance(bench.clock_sampler(_T, 0), bench.ClockSampler)
+
+
+class _FakeDevice:
+    """Device clock of a fake torch: every attention launch advances it by the
+    next duration (ms) from a list."""
+
+    def __init__(self, durations):
+        self.now, self.durations, self.launches = 0.0, list(durations), 0
+
+    def launch(self):
+        self.now += self.durations[min(self.launches, len(self.durations) - 1)]
+        self.launches += 1
+
+
+def _fake_torch(dev):
+    class Event:
+        def __init__(self, enable_timing=False):
+            self.t = None
+
+        def record(self, stream=None):
+            self.t = dev.now
+
+        def elapsed_time(self, other):
+            return other.t - self.t
+
+    class Cuda:
+        pass
+
+    cuda = Cuda()
+    cuda.Event = Event
+    cuda.current_stream = lambda: None
+    cuda.synchronize = lambda: None
+
+    class Torch:
+        pass
+
+    t = Torch()
+    t.cuda = cuda
+    return t
+
+
+def _fake_bss(dev, status=0):
+    class Bss:
+        @staticmethod
+        def sparse_attention_split(*a):
+            dev.launch()
+
+        @staticmethod
+        def get_device_status():
+            return status
+
+        @staticmethod
+        def status_string(s):
+            return f"status {s}"
+
+    return Bss
+
+
+class _FakeSampler:
+    def start(self):
+        pass
+
+    def mark_begin(self):
+        pass
+
+    def mark_end(self):
+        pass
+
+    def stop(self):
+        return {"sm_mhz": 1740.0, "reasons": ["sw_power_cap"], "samples": 9}
+
+
+def test_power_regimes_time_each_end_of_the_ramp_against_its_own_peak(monkeypatch):
+    monkeypatch.setattr(bench.time, "sleep", lambda s: None)
+    monkeypatch.setattr(bench, "clock_sampler", lambda torch, idx: _FakeSampler())
+    # three bursts (5.0, 5.4, 5.2 ms), then every launch 6.0 ms (the settled regime)
+    dev = _FakeDevice([5.0, 5.4, 5.2, 6.0])
+    peaks = {"bf16_tflops": 2000.0, "bf16_tflops_sustained": 1500.0}
+    flops = 10e12
+    out = bench.power_regimes(_fake_bss(dev), _fake_torch(dev), *[None] * 9, flops, peaks, 0, sustain_s=0.12)
+    b, s = out["burst"], out["sustained"]
+    assert b["ms"] == pytest.approx(5.2)  # median of the three
+    assert b["achieved"] == pytest.approx(flops / 5.2e-3 / 1e12)
+    assert b["peak"] == 2000.0 and b["frac"] == pytest.approx(b["achieved"] / 2000.0)
+    # 0.12 s / 2 / 5.2 ms -> 11 launches a half; only the second half is timed
+    assert s["launches"] == 11 and dev.launches == 3 + 2 * 11
+    assert s["ms"] == pytest.approx(6.0)
+    assert s["peak"] == 1500.0 and s["frac"] == pytest.approx(flops / 6.0e-3 / 1e12 / 1500.0)
+    assert s["clocks"]["reasons"] == ["sw_power_cap"]
+
+
+def test_power_regimes_refuse_a_device_error(monkeypatch):
+    monkeypatch.setattr(bench.time, "sleep", lambda s: None)
+    monkeypatch.setattr(bench, "clock_sampler", lambda torch, idx: _FakeSampler())
+    dev = _FakeDevice([5.0])
+    with pytest.raises(RuntimeError, match="power-regime"):
+        bench.power_regimes(_fake_bss(dev, status=3), _fake_torch(dev), *[None] * 9, 1e12,
+                            {"bf16_tflops": 1.0, "bf16_tflops_sustained": 1.0}, 0, sustain_s=0.05)
