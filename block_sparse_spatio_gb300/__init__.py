@@ -519,7 +519,8 @@ def attention_step_host(hQ, hK, hV, hO, tile_map: TileMap, head_is_temporal, wor
     pipelined over groups of heads on the workspace's copy streams and
     ``stream`` (default: current).  hQ, hK, hV, hO: CPU bf16 [H][N][d], pinned
     for overlap; head_is_temporal: CPU uint8[H].  Returns a CUDA event that
-    completes when hO is written; the inputs must not change before it."""
+    completes when hO is written; until then the host buffers must stay alive
+    (the copies read and write them asynchronously) and the inputs unchanged."""
     import torch
     for t, n in ((hQ, "hQ"), (hK, "hK"), (hV, "hV"), (hO, "hO")):
         _host_tensor(t, n, torch.bfloat16)

@@ -232,13 +232,27 @@ bss_status bss_attention_step_host(const void* hQ, const void* hK, const void* h
     StepSet& s = ws->sets[ws->next];
     const size_t row_bytes = static_cast<size_t>(ws->N) * ws->d * 2;  // one head of one tensor
     bss_status st;
+    // A failure after the first enqueue leaves earlier groups' copies and
+    // kernels in flight on this set: order them before the caller's later work
+    // and before the set's next use, as a successful call would (the message of
+    // the failure is kept: these calls do not set the error text).
+    auto settle = [&](bss_status failed) {
+        if (ws->ngroups > 1 && cudaEventRecord(ws->join, ws->compute2) == cudaSuccess)
+            cudaStreamWaitEvent(stream, ws->join, 0);
+        if (cudaEventRecord(ws->fork, stream) == cudaSuccess) cudaStreamWaitEvent(ws->copy_out, ws->fork, 0);
+        if (cudaEventRecord(s.free_ev, ws->copy_out) == cudaSuccess) s.used = true;
+        ws->next = (ws->next + 1) % ws->depth;
+        return failed;
+    };
 #define BSS_TRY(call, what)                                              \
     do {                                                                 \
-        if ((st = cuda_check((call), what)) != BSS_OK) return st;        \
+        if ((st = cuda_check((call), what)) != BSS_OK) return settle(st); \
     } while (0)
     // the set's previous call must be done with it: its kernels read Q, K, V and
     // its D2H copy reads O
-    if (s.used) BSS_TRY(cudaStreamWaitEvent(ws->copy_in, s.free_ev, 0), "wait for the buffer set");
+    if (s.used && (st = cuda_check(cudaStreamWaitEvent(ws->copy_in, s.free_ev, 0), "wait for the buffer set")) !=
+                      BSS_OK)
+        return st;
     // the second compute stream starts after the caller's work so far
     if (ws->ngroups > 1) {
         BSS_TRY(cudaEventRecord(ws->fork, stream), "record fork");
@@ -262,7 +276,7 @@ bss_status bss_attention_step_host(const void* hQ, const void* hK, const void* h
         BSS_TRY(cudaStreamWaitEvent(cs, s.ready[g], 0), "wait for inputs");
         if ((st = step_device(at(s.Q), at(s.K), at(s.V), at_mut(s.O), nullptr, map, s.flags + h0, h1 - h0,
                               at_mut(s.Qp), at_mut(s.Kp), at_mut(s.Vp), cs)) != BSS_OK)
-            return st;
+            return settle(st);
         BSS_TRY(cudaEventRecord(s.done[g], cs), "record outputs done");
         BSS_TRY(cudaStreamWaitEvent(ws->copy_out, s.done[g], 0), "wait for outputs");
         BSS_TRY(cudaMemcpyAsync(at_mut(hO), at(s.O), n, cudaMemcpyDeviceToHost, ws->copy_out), "copy O out");
