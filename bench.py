@@ -724,7 +724,7 @@ def variants(bss, torch, W, w, H, Q, K, V, dev, peaks, flags):
         fl_ = 4.0 * w.d * H * tp
 
         def with_perm():
-            bss.attention_step(Q, K, V, O, tm1, ones, Qp, Kp, Vp, Op)
+            bss.attention_step(Q, K, V, O, tm1, ones, Qp, Kp, Vp)
 
         tms = _time_interleaved(torch, {
             "perm": with_perm,
@@ -743,7 +743,7 @@ def variants(bss, torch, W, w, H, Q, K, V, dev, peaks, flags):
         mixed_fl = 4.0 * w.d * sum(tm1.stats(f)["retained_pairs"] for f in flags)
 
         def explicit_step():
-            bss.attention_step(Q, K, V, O, tm1, fl_mixed, Qp, Kp, Vp, Op)
+            bss.attention_step(Q, K, V, O, tm1, fl_mixed, Qp, Kp, Vp)
 
         mms = _time_interleaved(torch, {"explicit": explicit_step,
                                         "fused": lambda: bss.sparse_attention_fused(Q, K, V, O, tm1, fl_mixed)},

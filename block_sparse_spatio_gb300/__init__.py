@@ -427,13 +427,13 @@ def route_heads(Q, K, V, params: MaskParams, rows, head_is_temporal, errors, str
     return head_is_temporal, errors
 
 
-def attention_step(Q, K, V, O, tile_map: TileMap, head_is_temporal, Qp, Kp, Vp, Op=None, lse=None, stream=None):
+def attention_step(Q, K, V, O, tile_map: TileMap, head_is_temporal, Qp, Kp, Vp, lse=None, stream=None):
     """The per-layer path of the blog's Figure 8 on one GPU (``bss_attention_step``):
     permute the temporal heads' Q, K, V to (H,W,F) into the workspaces Qp, Kp,
     Vp, run block-sparse attention, and store their O rows back in (F,H,W)
-    order.  Q, K, V, O are in (F,H,W) order; Op is not needed (accepted for
-    callers that pass four workspaces).  lse, if given, is in each head's own
-    layout."""
+    order.  Q, K, V, O are in (F,H,W) order; Qp, Kp, Vp may be None when no
+    head is permuted (no flags, or a map with temporal_permuted = 0).  lse, if
+    given, is in each head's own layout."""
     import torch
     named = [(Q, "Q"), (K, "K"), (V, "V"), (O, "O")] + [(t, n) for t, n in ((Qp, "Qp"), (Kp, "Kp"), (Vp, "Vp"))
                                                           if t is not None]

@@ -33,7 +33,7 @@ def run_gpu(bss, q, k, v, flags, params, want_lse=True, dense=False, BQ=None, BK
     if dense:
         bss.dense_attention(Q, K, V, O, lse=lse)
     else:
-        ws = [torch.empty_like(Q) for _ in range(4)]
+        ws = [torch.empty_like(Q) for _ in range(3)]
         with bss.build_tile_map(params, BQ=BQ or bss.ATTN_BQ, BKV=BKV or bss.ATTN_BKV) as tm:
             bss.attention_step(Q, K, V, O, tm, fl, *ws, lse=lse)
             stats = (tm.stats(0), tm.stats(1))

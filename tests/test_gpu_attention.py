@@ -143,7 +143,7 @@ def test_rounded_mask_with_empty_q_tiles_gives_zero_rows(bss, path):
     dev = torch.device("cuda")
     Q, K, V = (x.to(dev) for x in (q, k, v))
     fl = torch.tensor(flags, dtype=torch.uint8, device=dev)
-    ws_ = [torch.empty_like(Q) for _ in range(4)]
+    ws_ = [torch.empty_like(Q) for _ in range(3)]
     with bss.build_tile_map(p, BQ=BQ) as tm:
         for it in range(10):
             O = torch.full_like(Q, 3.0)
@@ -171,7 +171,7 @@ def _full_size(bss, wl, tperm, rounding, heads, nrows, tile_stride=1):
     O = torch.empty_like(Q)
     lse = torch.empty(wl.H, wl.N, device=dev)
     fl = torch.tensor(flags, dtype=torch.uint8, device=dev)
-    ws_ = [torch.empty_like(Q) for _ in range(4)]
+    ws_ = [torch.empty_like(Q) for _ in range(3)]
     with bss.build_tile_map(p) as tm:
         bss.attention_step(Q, K, V, O, tm, fl, *ws_, lse=lse)
         torch.cuda.synchronize()
@@ -278,7 +278,7 @@ def test_split_step_equals_full_permutation_step(bss, wl_name):
     O1, O2 = torch.empty_like(Q), torch.empty_like(Q)
     l1 = torch.empty(H, wl.N, device=dev)
     l2 = torch.empty(H, wl.N, device=dev)
-    ws = [torch.empty_like(Q) for _ in range(4)]
+    ws = [torch.empty_like(Q) for _ in range(3)]
     with bss.build_tile_map(p) as tm:
         bss.attention_step(Q, K, V, O1, tm, fl, *ws, lse=l1)
         Qp, Kp, Vp, Op = (torch.empty_like(Q) for _ in range(4))

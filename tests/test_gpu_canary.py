@@ -44,11 +44,11 @@ def test_attention_writes_only_its_outputs(bss, geom, path):
         bss.dense_attention(Q, K, V, O, lse=L)
     else:
         with bss.build_tile_map(p, BQ=128 if path == "bq128" else bss.ATTN_BQ) as tm:
-            wsp = [torch.empty_like(Q) for _ in range(4)]
+            wsp = [torch.empty_like(Q) for _ in range(3)]
             if path in ("step", "bq128"):
                 bss.attention_step(Q, K, V, O, tm, fl, *wsp, lse=L)
             elif path == "explicit":
-                Qp, Kp, Vp, Op = wsp
+                Qp, Kp, Vp = wsp
                 bss.permute(Q, Qp, fl, p, False)
                 bss.permute(K, Kp, fl, p, False)
                 bss.permute(V, Vp, fl, p, False)

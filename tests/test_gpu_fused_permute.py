@@ -97,7 +97,7 @@ def _full_size_equal(bss, wl, rounding, nrows, heads_checked):
     O1, O2 = torch.empty_like(Q), torch.empty_like(Q)
     l1 = torch.empty(wl.H, wl.N, device=dev)
     l2 = torch.empty(wl.H, wl.N, device=dev)
-    ws_ = [torch.empty_like(Q) for _ in range(4)]
+    ws_ = [torch.empty_like(Q) for _ in range(3)]
     with bss.build_tile_map(p) as tm:
         bss.attention_step(Q, K, V, O1, tm, fl, *ws_, lse=l1)
         bss.sparse_attention_fused(Q, K, V, O2, tm, fl, lse=l2)

@@ -26,7 +26,7 @@ def test_host_steps_match_device_step(bss, hpc, pinned, depth):
         for q, k, v in inputs:
             Q, K, V = (x.to(dev) for x in (q, k, v))
             O = torch.empty_like(Q)
-            ws = [torch.empty_like(Q) for _ in range(4)]
+            ws = [torch.empty_like(Q) for _ in range(3)]
             bss.attention_step(Q, K, V, O, tm, fl, *ws)
             expect.append(O.cpu())
         pin = (lambda x: x.pin_memory()) if pinned else (lambda x: x.clone())  # pageable copies work too
@@ -81,7 +81,7 @@ def test_head_local_path_on_one_rank_is_the_attention_step(bss):
     with bss.build_tile_map(p) as tm:
         O = head_local_attention(Q, K, V, fl, make_attention_step(tm, 4, w.N, w.d, dev)).clone()
         O2 = torch.empty_like(Q)
-        ws = [torch.empty_like(Q) for _ in range(4)]
+        ws = [torch.empty_like(Q) for _ in range(3)]
         bss.attention_step(Q, K, V, O2, tm, fl, *ws)
         torch.cuda.synchronize()
     assert bss.get_device_status() == 0
