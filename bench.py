@@ -174,6 +174,7 @@ class NvmlClockSampler:
         self.t_begin = self.t_end = None
         self._stop = threading.Event()
         self.thread = None
+        self.power_instant = True  # cleared once the instantaneous field is refused
         try:
             lib = ctypes.CDLL("libnvidia-ml.so.1")
             if lib.nvmlInit_v2() != 0:
@@ -197,12 +198,41 @@ class NvmlClockSampler:
         except Exception:
             self.ok = False
 
+    def _instant_power_w(self):
+        """The instantaneous board power (field NVML_FI_DEV_POWER_INSTANT, mW),
+        or None where the driver does not serve it.  nvmlDeviceGetPowerUsage
+        averages over about a second, which lags a timed region of 0.1-0.4 s."""
+        ct = self.ct
+
+        class FieldValue(ct.Structure):  # nvmlFieldValue_t (nvml.h)
+            _fields_ = [("fieldId", ct.c_uint), ("scopeId", ct.c_uint), ("timestamp", ct.c_longlong),
+                        ("latencyUsec", ct.c_longlong), ("valueType", ct.c_int), ("nvmlReturn", ct.c_int),
+                        ("value", ct.c_ulonglong)]
+
+        fv = FieldValue(fieldId=186)
+        try:
+            if self.lib.nvmlDeviceGetFieldValues(self.h, 1, ct.byref(fv)) != 0 or fv.nvmlReturn != 0:
+                return None
+        except Exception:
+            return None
+        raw = fv.value
+        if fv.valueType == 0:  # double
+            mw = ct.c_double.from_buffer_copy(ct.c_ulonglong(raw)).value
+        elif fv.valueType in (1, 5, 6):  # 32- or 16-bit integers
+            mw = raw & (0xFFFF if fv.valueType == 6 else 0xFFFFFFFF)
+        else:
+            mw = raw
+        return float(mw) / 1e3
+
     def _one(self):
         ct, lib, h = self.ct, self.lib, self.h
         mhz, mw, rs = ct.c_uint(), ct.c_uint(), ct.c_ulonglong()
         if lib.nvmlDeviceGetClockInfo(h, 1, ct.byref(mhz)) != 0:
             return None
-        power = float(mw.value) / 1e3 if lib.nvmlDeviceGetPowerUsage(h, ct.byref(mw)) == 0 else None
+        power = self._instant_power_w() if self.power_instant else None
+        if power is None:
+            self.power_instant = False
+            power = float(mw.value) / 1e3 if lib.nvmlDeviceGetPowerUsage(h, ct.byref(mw)) == 0 else None
         reasons = int(rs.value) if self.reason_fn(h, ct.byref(rs)) == 0 else 0
         return (time.monotonic(), float(mhz.value), power, reasons)
 
@@ -232,7 +262,8 @@ class NvmlClockSampler:
         return summarize_clocks([x[1] for x in kept], [self.max_mhz] if self.max_mhz else [],
                                 [x[2] for x in kept if x[2] is not None],
                                 {nm for x in kept for bit, nm in self.REASONS.items() if x[3] & bit},
-                                f"in-process NVML every {self.period * 1e3:.0f} ms")
+                                f"in-process NVML every {self.period * 1e3:.0f} ms; power: "
+                                + ("instantaneous" if self.power_instant else "NVML's one-second average"))
 
 
 def summarize_clocks(sm, smax, power, reasons, how):

@@ -84,7 +84,7 @@ def test_nvml_clock_record_window_and_reason_bits():
     # the in-process sampler keeps samples inside the timed region only and
     # decodes the clock-event reason bits of each kept sample
     s = bench.NvmlClockSampler.__new__(bench.NvmlClockSampler)
-    s.period, s.max_mhz, s.thread = 0.005, 2070.0, None
+    s.period, s.max_mhz, s.thread, s.power_instant = 0.005, 2070.0, None, True
     s._stop = bench.threading.Event()
     s.t_begin, s.t_end = 10.0, 11.0
     s.samples = [
@@ -99,7 +99,61 @@ def test_nvml_clock_record_window_and_reason_bits():
     assert rec["sm_mhz"] == 1790.0 and rec["sm_mhz_min"] == 1755.0 and rec["sm_max_mhz"] == 2070.0
     assert rec["power_w_max"] == 1395.0
     assert rec["reasons"] == ["sw_power_cap"]
-    assert "NVML" in rec["window"]
+    assert "NVML" in rec["window"] and "instantaneous" in rec["window"]
+
+
+class _FakeNvml:
+    """NVML calls of one sample: SM clock 1740 MHz, one-second average power
+    900 W, instantaneous power 1391.5 W as a field value (or refused)."""
+
+    def __init__(self, serve_field, value_type=1):
+        self.serve_field, self.value_type, self.field_calls = serve_field, value_type, 0
+
+    def nvmlDeviceGetClockInfo(self, h, kind, out):
+        out._obj.value = 1740
+        return 0
+
+    def nvmlDeviceGetPowerUsage(self, h, out):
+        out._obj.value = 900000
+        return 0
+
+    def nvmlDeviceGetFieldValues(self, h, n, fv):
+        import ctypes
+        self.field_calls += 1
+        v = fv._obj
+        assert n == 1 and v.fieldId == 186
+        if not self.serve_field:
+            v.nvmlReturn = 3  # NVML_ERROR_NOT_SUPPORTED
+            return 0
+        v.nvmlReturn, v.valueType = 0, self.value_type
+        if self.value_type == 0:
+            v.value = ctypes.c_ulonglong.from_buffer_copy(ctypes.c_double(1391500.0)).value
+        else:
+            v.value = 1391500
+        return 0
+
+
+def _nvml_sampler(lib):
+    import ctypes
+    s = bench.NvmlClockSampler.__new__(bench.NvmlClockSampler)
+    s.ct, s.lib, s.h, s.power_instant = ctypes, lib, None, True
+    s.reason_fn = lambda h, out: (setattr(out._obj, "value", 0x4), 0)[1]
+    return s
+
+
+@pytest.mark.parametrize("value_type", [0, 1, 3])
+def test_nvml_sample_takes_the_instantaneous_power_field(value_type):
+    s = _nvml_sampler(_FakeNvml(True, value_type))
+    _, mhz, power, reasons = s._one()
+    assert mhz == 1740.0 and power == pytest.approx(1391.5) and reasons == 0x4
+    assert s.power_instant
+
+
+def test_nvml_sample_falls_back_to_the_average_power_once_the_field_is_refused():
+    lib = _FakeNvml(False)
+    s = _nvml_sampler(lib)
+    assert s._one()[2] == pytest.approx(900.0) and not s.power_instant
+    assert s._one()[2] == pytest.approx(900.0) and lib.field_calls == 1  # not asked again
 
 
 def test_nvml_sampler_without_the_driver_falls_back():
