@@ -102,8 +102,8 @@ struct AttnArgs {
     const uint16_t *q_rows, *k_rows, *v_rows;  // Q, K, V as bf16 bits (fused permutation: row gathers)
     uint16_t* o_rows;                 // O as bf16 bits (fused permutation: row-wise stores)
     const int32_t* qmap;              // routing: token index of each query row (mask predicate)
-    float* o_f32;                     // routing: [splits][3H][Nq][D] normalised fp32 outputs
-    float* lse_f32;                   // routing: [splits][3H][Nq] natural-log LSE
+    float* o_f32;                     // routing: [3H][Nq][splits][D] normalised fp32 outputs
+    float* lse_f32;                   // routing: [3H][Nq][splits] natural-log LSE
     const int32_t* row_ptr[2];
     const int32_t* entries[2];
     const int32_t* order[2];
@@ -306,22 +306,22 @@ __global__ void __launch_bounds__(threads_for<HALVES>(), 1) attn_fwd_kernel(cons
     int* status = args.status;
 
     // ---- work item: (head, q tile); heads in order, q tiles longest first.
-    // Routing: (output head vh = mask * H + head, q tile, kv split), masks dense /
-    // spatial / temporal in (F,H,W) order, every kv tile of the split.
+    // Routing: (head, q tile, kv split) over the head's 3 * Nq virtual query rows
+    // (its sampled rows once for each mask: dense, spatial, temporal in (F,H,W)
+    // order), every kv tile of the split; each row decodes its own mask.
     const int item = blockIdx.x;
     int h, vh = 0, split = 0, j0 = 0, code;
     bool tbuf = false;  // head with flag 1: its tensors come from the temporal-head buffers
     int qt, n;
     const int32_t* ents = nullptr;
     if constexpr (ROUTE) {
-        vh = item / (args.nq * args.splits);
-        const int rem = item - vh * args.nq * args.splits;
+        h = item / (args.nq * args.splits);
+        const int rem = item - h * args.nq * args.splits;
         qt = rem / args.splits;
         split = rem - qt * args.splits;
-        const int mk = vh / args.H;
-        h = vh - mk * args.H;
-        code = mk == 0 ? static_cast<int>(MASK_DENSE) : (mk == 1 ? static_cast<int>(MASK_SPATIAL)
-                                                                  : static_cast<int>(MASK_TEMPORAL_FHW));
+        // the item's rows mix the three masks, so every tile is masked row by row
+        // (a masked kind here makes every entry BOUNDARY; rows use their own kind)
+        code = static_cast<int>(MASK_SPATIAL);
         j0 = static_cast<int>(static_cast<int64_t>(split) * args.nkv_dense / args.splits);
         n = static_cast<int>(static_cast<int64_t>(split + 1) * args.nkv_dense / args.splits) - j0;
     } else {
@@ -660,18 +660,55 @@ __global__ void __launch_bounds__(threads_for<HALVES>(), 1) attn_fwd_kernel(cons
         const uint32_t t_s0 = tmem + lane_base + kColS + hf * 128;
         const uint32_t t_o = tmem + lane_base + kColO + hf * 128;
         const int q = qt * kBQt + hf * kHalf + r;
-        // mask predicate row: the query itself, or (routing) the sampled token
+        // mask predicate row: the query itself, or (routing) the sampled token of
+        // virtual row q = mask * Nq + sampled row, under that mask; the padding
+        // rows past 3 * Nq repeat the last one and are not stored
         int qo = q;
+        int rcode = code;
+        int rr = q;
         if constexpr (ROUTE) {
-            qo = __ldg(args.qmap + (q < args.Nq ? q : args.Nq - 1));
+            int mk = q / args.Nq;
+            mk = mk > 2 ? 2 : mk;
+            rr = q - mk * args.Nq;
+            rr = rr >= args.Nq ? args.Nq - 1 : rr;
+            vh = mk * args.H + h;
+            rcode = mk == 0 ? static_cast<int>(MASK_DENSE)
+                            : (mk == 1 ? static_cast<int>(MASK_SPATIAL) : static_cast<int>(MASK_TEMPORAL_FHW));
+            qo = __ldg(args.qmap + rr);
             qo = qo < 0 ? 0 : (qo >= args.N ? args.N - 1 : qo);
         }
-        const RowPred rp = row_pred(args, code, qo);
+        const RowPred rp = row_pred(args, rcode, qo);
         // output row of this query: its own index, or its (F,H,W) position when the
         // kernel applies the permutation
         const int orow = (scatter && q < args.N) ? (q % args.F) * args.S + q / args.F : q;
         const float c = args.scale_log2;
         float m = -INFINITY;
+        if constexpr (ROUTE) {
+            // The sampled token's own key is retained by all three masks, so its
+            // score is at most the row's maximum.  The reference starts there (log2
+            // units): every tile can take the single pass from the first one on,
+            // and only terms more than 2^126 below the row's maximum can underflow;
+            // a tile whose sum of P passes kSumLimit moves the reference up as
+            // usual.  Starting from -inf instead sent a warp through the two-pass
+            // path at each of its rows' first retained key in the kv split (a
+            // temporal row's band starts at a different tile for every row).
+            const int qv = q < 3 * args.Nq ? q : 3 * args.Nq - 1;
+            const uint4* qr =
+                reinterpret_cast<const uint4*>(args.q_rows + (static_cast<int64_t>(h) * 3 * args.Nq + qv) * D);
+            const uint4* kr = reinterpret_cast<const uint4*>(args.k_rows + (static_cast<int64_t>(h) * args.N + qo) * D);
+            float acc0 = 0.0f, acc1 = 0.0f;
+#pragma unroll 4
+            for (int u = 0; u < D / 8; ++u) {
+                const uint4 x = __ldg(qr + u), y = __ldg(kr + u);
+                const uint32_t xs[4] = {x.x, x.y, x.z, x.w}, ys[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    acc0 = fmaf(__uint_as_float(xs[k] << 16), __uint_as_float(ys[k] << 16), acc0);
+                    acc1 = fmaf(__uint_as_float(xs[k] & 0xFFFF0000u), __uint_as_float(ys[k] & 0xFFFF0000u), acc1);
+                }
+            }
+            m = (acc0 + acc1) * c;
+        }
         float l = 0.0f;
         bool ok = true;
         for (int j = 0; j < n; ++j) {
@@ -757,7 +794,7 @@ __global__ void __launch_bounds__(threads_for<HALVES>(), 1) attn_fwd_kernel(cons
                     done = single_pass(std::integral_constant<bool, false>(), none);
                 } else {
                     uint32_t bits[4];
-                    tile_bits<kNW>(*reinterpret_cast<uint32_t(*)[kNW]>(bits), args, code, cls, c0, rp, tbuf ? 1 : 0, qt);
+                    tile_bits<kNW>(*reinterpret_cast<uint32_t(*)[kNW]>(bits), args, rcode, cls, c0, rp, tbuf ? 1 : 0, qt);
                     done = single_pass(std::integral_constant<bool, true>(), bits);
                 }
             } else if constexpr (ROUTE) {
@@ -768,7 +805,7 @@ __global__ void __launch_bounds__(threads_for<HALVES>(), 1) attn_fwd_kernel(cons
                 // sending the whole warp to the two-pass path on every tile.
                 if (cls != BSS_CLASS_FULL) {
                     uint32_t bits[4];
-                    tile_bits<kNW>(*reinterpret_cast<uint32_t(*)[kNW]>(bits), args, code, cls, c0, rp, tbuf ? 1 : 0, qt);
+                    tile_bits<kNW>(*reinterpret_cast<uint32_t(*)[kNW]>(bits), args, rcode, cls, c0, rp, tbuf ? 1 : 0, qt);
                     uint32_t any = 0u;
 #pragma unroll
                     for (int w = 0; w < kNW; ++w) any |= bits[w];
@@ -782,7 +819,7 @@ __global__ void __launch_bounds__(threads_for<HALVES>(), 1) attn_fwd_kernel(cons
                 // pass 2 exponentiates and writes P chunk by chunk.
                 uint32_t bits[4] = {0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu, 0xFFFFFFFFu};
                 if (cls != BSS_CLASS_FULL)
-                    tile_bits<kNW>(*reinterpret_cast<uint32_t(*)[kNW]>(bits), args, code, cls, c0, rp, tbuf ? 1 : 0, qt);
+                    tile_bits<kNW>(*reinterpret_cast<uint32_t(*)[kNW]>(bits), args, rcode, cls, c0, rp, tbuf ? 1 : 0, qt);
                 float mx[8];
 #pragma unroll
                 for (int t = 0; t < 8; ++t) mx[t] = -INFINITY;
@@ -881,10 +918,10 @@ __global__ void __launch_bounds__(threads_for<HALVES>(), 1) attn_fwd_kernel(cons
                     w[i] = pack_bf16x2(__uint_as_float(o[2 * i]) * inv_l, __uint_as_float(o[2 * i + 1]) * inv_l);
                 if constexpr (ROUTE) {
                     // routing: normalised fp32 row of this split
-                    if (q < args.Nq) {
+                    if (q < 3 * args.Nq) {
                         float4* dst = reinterpret_cast<float4*>(
                                           args.o_f32 +
-                                          ((static_cast<int64_t>(split) * 3 * args.H + vh) * args.Nq + q) * D) +
+                                          ((static_cast<int64_t>(vh) * args.Nq + rr) * args.splits + split) * D) +
                                       cc * 8;
 #pragma unroll
                         for (int u = 0; u < 8; ++u)
@@ -913,9 +950,9 @@ __global__ void __launch_bounds__(threads_for<HALVES>(), 1) attn_fwd_kernel(cons
                 }
             }
             if constexpr (ROUTE) {
-                if (q < args.Nq) {
+                if (q < 3 * args.Nq) {
                     const float lse = l > 0.0f ? (m + log2f(l)) * 0.69314718055994530942f : -INFINITY;
-                    args.lse_f32[(static_cast<int64_t>(split) * 3 * args.H + vh) * args.Nq + q] = lse;
+                    args.lse_f32[(static_cast<int64_t>(vh) * args.Nq + rr) * args.splits + split] = lse;
                 }
             } else if (args.lse != nullptr && q < args.N) {
                 const float lse = l > 0.0f ? (m + log2f(l)) * 0.69314718055994530942f : -INFINITY;
@@ -951,8 +988,9 @@ bss_status launch_d(const AttnLaunch& a, cudaStream_t stream) {
     const uint64_t rs = static_cast<uint64_t>(a.d) * 2;
     const uint64_t hs = rs * static_cast<uint64_t>(a.N);
     bss_status st;
-    // query rows per head: N, or the sampled rows in routing mode
-    const int64_t nq_rows = a.route ? a.Nq : a.N;
+    // query rows per head: N, or in routing mode the sampled rows once for each
+    // of the three masks
+    const int64_t nq_rows = a.route ? 3ll * a.Nq : a.N;
     // keys per kv tile: the map's BKV (routing and the dense control use 128;
     // the fused permutation needs a 128-key map)
     const int bkv = (a.route || a.dense || a.bkv == 0) ? kBKV : a.bkv;
@@ -1033,7 +1071,7 @@ bss_status launch_d(const AttnLaunch& a, cudaStream_t stream) {
     }
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return cuda_check(e, "cudaFuncSetAttribute(attention)");
-    const int64_t items = static_cast<int64_t>(a.H) * a.nq * (a.route ? 3 * a.splits : 1);
+    const int64_t items = static_cast<int64_t>(a.H) * a.nq * (a.route ? a.splits : 1);
     if (items <= 0) return BSS_OK;
     if (items > 0x7FFFFFFF) return set_error(BSS_ERR_UNSUPPORTED, "too many work items");
     const int threads = halves == 2 ? threads_for<2>() : threads_for<1>();

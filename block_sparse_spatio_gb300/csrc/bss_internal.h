@@ -96,8 +96,9 @@ struct AttnLaunch {
     // (F,H,W) positions in O (lse stays in layout order).
     int32_t fused;
     // routing mode: 3 x H output heads (dense, spatial, temporal in (F,H,W)
-    // order) over Nq sampled query rows per head whose tokens are qmap[r]; every
-    // kv tile, split into `splits` ranges; normalised fp32 O and LSE per split
+    // order) over Nq sampled query rows per head whose tokens are qmap[r]; Q
+    // holds each head's rows once per mask ([H][3 Nq][d], mask-major); every kv
+    // tile, split into `splits` ranges; normalised fp32 O and LSE per split
     int32_t route, Nq, splits;
     int32_t bq;   // query rows per CTA: the map's BQ (128 or 256)
     int32_t bkv;  // keys per kv tile: the map's BKV (64 or 128; 0 = 128)

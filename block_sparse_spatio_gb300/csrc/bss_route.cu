@@ -14,11 +14,14 @@
 //
 // GB300 form: routing is dense attention of the sampled rows under three
 // masks, so it runs on the tensor cores in the block-sparse attention kernel's
-// routing mode.  The sampled query rows are gathered into [H][R][d]; one
-// launch computes, for every head, the dense, spatial and temporal outputs of
-// those rows over every kv tile (the masked kinds evaluate their predicate at
-// each row's own token), with the kv range split so that the launch fills the
-// GPU; each split writes its normalised fp32 output and log-sum-exp.  Two
+// routing mode.  The sampled query rows are gathered three times into
+// [H][3R][d] (rows [mR, (m+1)R) for mask m: dense, spatial, temporal), so that
+// one work item holds every mask's copy of its rows (64 sampled rows: 192 of
+// the 256 rows of a two-half item, instead of three one-half items each half
+// padding); one launch computes, for every head, the three outputs of those
+// rows over every kv tile (each row evaluates its own mask's predicate at its
+// own token), with the kv range split so that the launch fills the GPU; each
+// split writes its normalised fp32 output and log-sum-exp.  Two
 // small kernels follow: one CTA per (sampled row, head) merges the splits
 // through their log-sum-exps and sums the row's squared deviations over the
 // channels; one CTA per head adds up its rows in a fixed order and sets the
@@ -38,8 +41,9 @@ namespace {
 
 constexpr int kDevThreads = 256;
 
-// Qs[h][r] = Q[h][rows[r]] (16 bytes per thread); a row outside [0, N) is
-// recorded in the status word and replaced by token 0 (its deviation is skipped)
+// Qs[h][m * R + r] = Q[h][rows[r]] for the three masks m (16 bytes per thread);
+// a row outside [0, N) is recorded in the status word and replaced by token 0
+// (its deviation is skipped)
 __global__ void gather_rows_kernel(const uint4* __restrict__ Q, uint4* __restrict__ Qs,
                                    const int32_t* __restrict__ rows, int R, int N, int vec, int* status) {
     const int r = blockIdx.x, h = blockIdx.y;
@@ -48,36 +52,60 @@ __global__ void gather_rows_kernel(const uint4* __restrict__ Q, uint4* __restric
         if (threadIdx.x == 0) record_status(status, BSS_ERR_INVALID_ARG);
         t = 0;
     }
-    for (int v = threadIdx.x; v < vec; v += blockDim.x)
-        Qs[(static_cast<size_t>(h) * R + r) * vec + v] = __ldg(Q + (static_cast<size_t>(h) * N + t) * vec + v);
+    for (int v = threadIdx.x; v < vec; v += blockDim.x) {
+        const uint4 x = __ldg(Q + (static_cast<size_t>(h) * N + t) * vec + v);
+#pragma unroll
+        for (int m = 0; m < 3; ++m) Qs[(static_cast<size_t>(h) * 3 * R + m * R + r) * vec + v] = x;
+    }
 }
 
 // One CTA per (sampled row, head), one thread per channel: merge the kv splits
 // of the dense (m = 0), spatial (1) and temporal (2) outputs of the row,
 // O = sum_p O_p exp(LSE_p - LSE) / sum_p exp(LSE_p - LSE), and write the row's
 // squared deviations of the masked outputs from the dense one, summed over
-// channels, to partial[h][r][0..1] (zero for a row outside [0, N)).
+// channels, to partial[h][r][0..1] (zero for a row outside [0, N)).  The split
+// weights of the row are computed once into shared memory (3 * splits floats
+// of dynamic shared memory); each thread then issues its channel's loads of all
+// splits back to back and sums them in split order.
 template <int D>
 __global__ void __launch_bounds__(D) route_merge_kernel(const float* __restrict__ o_f32,
                                                         const float* __restrict__ lse_f32,
                                                         const int32_t* __restrict__ rows, float* __restrict__ partial,
                                                         int H, int R, int N, int splits) {
+    extern __shared__ float s_w[];  // [3][splits]: LSE, then weight of each split
+    __shared__ float s_mx[3];
     const int r = blockIdx.x, h = blockIdx.y, ch = threadIdx.x;
     const int t = __ldg(rows + r);
     float dev[2] = {0.0f, 0.0f};
     if (t >= 0 && t < N) {
+        for (int i = ch; i < 3 * splits; i += D) {
+            const int m = i / splits, p = i - m * splits;
+            s_w[i] = __ldg(lse_f32 + ((static_cast<int64_t>(m) * H + h) * R + r) * splits + p);
+        }
+        __syncthreads();
+        if (ch < 3) {
+            float mx = -INFINITY;
+            for (int p = 0; p < splits; ++p) mx = fmaxf(mx, s_w[ch * splits + p]);
+            s_mx[ch] = mx;
+        }
+        __syncthreads();
+        for (int i = ch; i < 3 * splits; i += D) {
+            const float lp = s_w[i];
+            s_w[i] = lp == -INFINITY ? 0.0f : expf(lp - s_mx[i / splits]);
+        }
+        __syncthreads();
         float o[3];
 #pragma unroll
         for (int m = 0; m < 3; ++m) {
-            const int64_t vh = static_cast<int64_t>(m) * H + h;
-            float mx = -INFINITY;
-            for (int p = 0; p < splits; ++p) mx = fmaxf(mx, __ldg(lse_f32 + (p * 3 * H + vh) * R + r));
+            // the row's splits are contiguous: [3H][R][splits][D]
+            const float* src = o_f32 + ((static_cast<int64_t>(m) * H + h) * R + r) * splits * D + ch;
+            const int64_t step = D;  // next split
             float wsum = 0.0f, acc = 0.0f;
+#pragma unroll 8
             for (int p = 0; p < splits; ++p) {
-                const float lp = __ldg(lse_f32 + (p * 3 * H + vh) * R + r);
-                const float w = lp == -INFINITY ? 0.0f : expf(lp - mx);
+                const float w = s_w[m * splits + p];
                 wsum += w;
-                acc += w * __ldg(o_f32 + ((p * 3 * H + vh) * R + r) * D + ch);
+                acc += w * __ldg(src + p * step);
             }
             o[m] = wsum > 0.0f ? acc / wsum : 0.0f;
         }
@@ -152,18 +180,19 @@ extern "C" bss_status bss_route_heads(const void* Q, const void* K, const void* 
     const int d = params->head_dim;
     const int S = params->Hs * params->Ws;
     const int N = params->F * S;
-    // one 128-row MMA half per CTA when the sampled rows fit in it (no padding
-    // rows computed), else 256-row tiles
-    const int bq = R <= 128 ? 128 : attention_block_q();
-    const int nq = (R + bq - 1) / bq;
+    // the 3R virtual rows of a head (its sampled rows once per mask) in 256-row
+    // items, or one 128-row half when they fit in it
+    const int rows3 = 3 * R;
+    const int bq = rows3 <= 128 ? 128 : attention_block_q();
+    const int nq = (rows3 + bq - 1) / bq;
     const int nkv = (N + attention_block_kv() - 1) / attention_block_kv();
     // kv splits: enough CTAs for one wave of the GPU
-    const int64_t base = 3ll * H * nq;
+    const int64_t base = static_cast<int64_t>(H) * nq;
     int splits = static_cast<int>(num_sms() / base);
     splits = splits < 1 ? 1 : (splits > nkv ? nkv : splits);
     if (base * splits > 0x7FFFFFFFll) return set_error(BSS_ERR_UNSUPPORTED, "too many routing work items");
     // scratch, stream-ordered: gathered rows, per-split outputs and LSEs
-    const size_t q_bytes = static_cast<size_t>(H) * R * d * 2;
+    const size_t q_bytes = static_cast<size_t>(H) * rows3 * d * 2;
     const size_t o_bytes = static_cast<size_t>(splits) * 3 * H * R * d * 4;
     const size_t l_bytes = static_cast<size_t>(splits) * 3 * H * R * 4;
     const size_t p_bytes = static_cast<size_t>(H) * R * 2 * 4;
@@ -209,9 +238,11 @@ extern "C" bss_status bss_route_heads(const void* Q, const void* K, const void* 
     }
     if (st == BSS_OK) {
         if (d == 128)
-            route_merge_kernel<128><<<dim3(R, H), 128, 0, stream>>>(o32, l32, rows, partial, H, R, N, splits);
+            route_merge_kernel<128><<<dim3(R, H), 128, 3 * splits * sizeof(float), stream>>>(o32, l32, rows, partial,
+                                                                                              H, R, N, splits);
         else
-            route_merge_kernel<64><<<dim3(R, H), 64, 0, stream>>>(o32, l32, rows, partial, H, R, N, splits);
+            route_merge_kernel<64><<<dim3(R, H), 64, 3 * splits * sizeof(float), stream>>>(o32, l32, rows, partial,
+                                                                                            H, R, N, splits);
         st = cuda_check(cudaGetLastError(), "routing merge launch");
     }
     if (st == BSS_OK) {

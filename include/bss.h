@@ -261,9 +261,10 @@ bss_status bss_dense_attention(const void* Q, const void* K, const void* V, void
  *   head_is_temporal  device uint8[H] output (1 = temporal).
  *   errors            device float[2 * H] output: per head the spatial and the
  *                     temporal deviation.
- * Asynchronous on `stream`.  Scratch of H*R*d*2 + 3*H*R*(d+1)*4*splits bytes
- * (splits <= number of SMs / (3 * H * ceil(R / 256))) is taken from and
- * returned to the device's stream-ordered memory pool (cudaMallocAsync).
+ * Asynchronous on `stream`.  Scratch of 3*H*R*d*2 + 3*H*R*(d+1)*4*splits +
+ * 2*H*R*4 bytes (splits <= number of SMs / (H * ceil(3R / 256)), at least 1) is
+ * taken from and returned to the device's stream-ordered memory pool
+ * (cudaMallocAsync).
  * Errors: INVALID_ARG, UNSUPPORTED, CUDA. */
 bss_status bss_route_heads(const void* Q, const void* K, const void* V, int32_t H, const bss_mask_params* params,
                            const int32_t* rows, int32_t R, uint8_t* head_is_temporal, float* errors,
