@@ -65,8 +65,8 @@ __global__ void gather_rows_kernel(const uint4* __restrict__ Q, uint4* __restric
 // squared deviations of the masked outputs from the dense one, summed over
 // channels, to partial[h][r][0..1] (zero for a row outside [0, N)).  The split
 // weights of the row are computed once into shared memory (3 * splits floats
-// of dynamic shared memory); each thread then issues its channel's loads of all
-// splits back to back and sums them in split order.
+// of dynamic shared memory); each thread then loads its channel of every split
+// (the three masks' loads of a split together) and sums them in split order.
 template <int D>
 __global__ void __launch_bounds__(D) route_merge_kernel(const float* __restrict__ o_f32,
                                                         const float* __restrict__ lse_f32,
@@ -94,21 +94,24 @@ __global__ void __launch_bounds__(D) route_merge_kernel(const float* __restrict_
             s_w[i] = lp == -INFINITY ? 0.0f : expf(lp - s_mx[i / splits]);
         }
         __syncthreads();
+        // the row's splits are contiguous ([3H][R][splits][D]); the three masks'
+        // loads of a split are issued together
+        const float* src[3];
+        float wsum[3] = {0.0f, 0.0f, 0.0f}, acc[3] = {0.0f, 0.0f, 0.0f};
+#pragma unroll
+        for (int m = 0; m < 3; ++m) src[m] = o_f32 + ((static_cast<int64_t>(m) * H + h) * R + r) * splits * D + ch;
+#pragma unroll 4
+        for (int p = 0; p < splits; ++p) {
+#pragma unroll
+            for (int m = 0; m < 3; ++m) {
+                const float w = s_w[m * splits + p];
+                wsum[m] += w;
+                acc[m] += w * __ldg(src[m] + static_cast<int64_t>(p) * D);
+            }
+        }
         float o[3];
 #pragma unroll
-        for (int m = 0; m < 3; ++m) {
-            // the row's splits are contiguous: [3H][R][splits][D]
-            const float* src = o_f32 + ((static_cast<int64_t>(m) * H + h) * R + r) * splits * D + ch;
-            const int64_t step = D;  // next split
-            float wsum = 0.0f, acc = 0.0f;
-#pragma unroll 8
-            for (int p = 0; p < splits; ++p) {
-                const float w = s_w[m * splits + p];
-                wsum += w;
-                acc += w * __ldg(src + p * step);
-            }
-            o[m] = wsum > 0.0f ? acc / wsum : 0.0f;
-        }
+        for (int m = 0; m < 3; ++m) o[m] = wsum[m] > 0.0f ? acc[m] / wsum[m] : 0.0f;
         dev[0] = (o[1] - o[0]) * (o[1] - o[0]);
         dev[1] = (o[2] - o[0]) * (o[2] - o[0]);
     }
