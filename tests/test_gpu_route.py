@@ -35,11 +35,13 @@ def test_route_structured_heads(bss):
 
 @pytest.mark.gpu
 @pytest.mark.parametrize("wl", [W.SMALL, W.MIXED_75K], ids=lambda w: w.name)
-def test_route_random_heads_match_oracle(bss, wl):
-    dev = torch.device("cuda")
+@pytest.mark.parametrize("R", [24, 64])
+def test_route_random_heads_match_oracle(bss, wl, R):
+    # 24 sampled rows: the three masks' 72 copies fit one 128-row half; 64 (the
+    # benchmark's count): 192 copies in one two-half item
     H = 4
     q, k, v = W.qkv(wl, H=H, seed=11)
-    rows = W.sample_rows(wl.N, 24, seed=5)
+    rows = W.sample_rows(wl.N, R, seed=5)
     p = bss.MaskParams(wl.F, wl.Hs, wl.Ws, wl.d, wl.wf, wl.ws)
     flags, err = _run(bss, q, k, v, p, rows)
     oflags, oerr = oracle.route(W.bf16_bits(q), W.bf16_bits(k), W.bf16_bits(v),
@@ -52,8 +54,9 @@ def test_route_random_heads_match_oracle(bss, wl):
 @pytest.mark.gpu
 @pytest.mark.parametrize("d", [128, 64])
 def test_route_more_rows_than_one_query_tile_and_ragged_geometry(bss, d):
-    # 300 sampled rows span two 256-row query tiles; N = 390 is not a multiple of
-    # the 128-key tile (padding columns in the last kv tile)
+    # 300 sampled rows, 900 copies for the three masks: four 256-row items, the
+    # last one ragged; N = 390 is not a multiple of the 128-key tile (padding
+    # columns in the last kv tile)
     F, Hs, Ws, wf, ws = 3, 10, 13, 0, 20
     N = F * Hs * Ws
     q, k, v = W.qkv(W.SMALL, H=3, N=N, d=d, seed=31)
