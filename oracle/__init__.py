@@ -18,8 +18,12 @@ Mask kinds (oracle codes):
   DENSE = 3              every pair retained
 
 Parity status: every function here is pinned by ``tests/test_oracle.py``
-(brute-force dense masked softmax, closed-form counts, the hand-derived Tiny
-tile map, the permutation round trip, Q = 0 coverage, poison invariance).
+(brute-force dense masked softmax over explicit N x N matrices, closed-form
+counts, the hand-derived Tiny tile map, the permutation round trip and hand
+values, Q = 0 coverage, poison invariance; the tile-aligned mask against the
+set of physical pairs its kept tiles cover, built from token multiplicities;
+routing against constructed heads whose closer mask is known and against
+all-covering windows, where both deviations vanish).
 """
 from __future__ import annotations
 
