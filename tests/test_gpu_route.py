@@ -35,9 +35,10 @@ def test_route_structured_heads(bss):
 
 @pytest.mark.gpu
 @pytest.mark.parametrize("wl", [W.SMALL, W.MIXED_75K], ids=lambda w: w.name)
-@pytest.mark.parametrize("R", [24, 64])
+@pytest.mark.parametrize("R", [24, 43, 64])
 def test_route_random_heads_match_oracle(bss, wl, R):
-    # 24 sampled rows: the three masks' 72 copies fit one 128-row half; 64 (the
+    # 24 sampled rows: the three masks' 72 copies fit one 128-row half; 43: 129
+    # copies, one past a half, so a two-half item with 127 padding rows; 64 (the
     # benchmark's count): 192 copies in one two-half item
     H = 4
     q, k, v = W.qkv(wl, H=H, seed=11)
